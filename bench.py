@@ -1,0 +1,491 @@
+"""Benchmark of the Gated DeltaNet layer hot path on GB300.
+
+One JSON line on rank 0. The headline workload is one decode step of a
+Qwen3.5-9B-like GDN layer (B=64 rows, T=1, 16 key / 32 value heads, d=128,
+fp32 recurrent state): `value` is layer tokens/s with every input resident in
+HBM. The other paths of the layer are measured in the same run under
+"phases": speculative verify (8 paths x 8 draft tokens from one shared state,
+per-token checkpoints, commit of the winner), chunked prefill (one row of
+8192 tokens continued in 512-token calls) and packed varlen prefill
+(32 rows U{16..2048} padded to chunk buckets, 24 independent layers).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--phases decode,verify,prefill,varlen]
+
+--impl reference times the fp64 CPU oracle (the reference implementation of
+this path) on the same decode workload, on the host's cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+from pathlib import Path
+
+import torch
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+from gated_deltanet_recurrence_delta_gb300 import inputs as I  # noqa: E402
+
+METRIC = "GDN layer tokens/s (prefill, decode, verify) and % of HBM / tensor roofline"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_BYTES = 129 * 1024 * 1024
+ACTS = ("q", "k", "v", "z", "a", "b")
+WN = ("A_log", "dt_bias", "conv_w", "norm_w")
+
+
+# ----------------------------------------------------------------- helpers
+
+def peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return (float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "measured")
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def csrc_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted((ROOT / "gated_deltanet_recurrence_delta_gb300" / "csrc").glob("*")):
+        h.update(p.name.encode())
+        h.update(p.read_bytes())
+    return h.hexdigest()[:16]
+
+
+def dram_traffic(kernel: str):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, or None
+    when absent or taken on other kernel sources."""
+    p = ROOT / "profiles" / "dram_traffic.json"
+    if not p.exists():
+        return None
+    d = json.loads(p.read_text())
+    e = d.get(kernel)
+    if not e or e.get("csrc_hash") != csrc_hash():
+        return None
+    return float(e["bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+class Timer:
+    """CUDA events on the launching stream; per-launch pairs for one kernel."""
+
+    def __init__(self):
+        self.pairs = []
+
+    def around(self, fn):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        fn()
+        e.record()
+        self.pairs.append((s, e))
+
+    def mean_ms(self):
+        return sum(s.elapsed_time(e) for s, e in self.pairs) / max(1, len(self.pairs))
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def timed(world, steps, warmup, step_fn, kernel_fn=None):
+    """Run warmup steps, then `steps` timed steps bracketed by a barrier and a
+    synchronize on both sides; returns (ms per step max over ranks, mean ms of
+    the dominant kernel per launch)."""
+    for i in range(warmup):
+        step_fn(i, None)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    kt = Timer()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for i in range(steps):
+        step_fn(warmup + i, kt)
+    e.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = s.elapsed_time(e) / steps
+    return max_over_ranks(ms, world), kt.mean_ms()
+
+
+# ------------------------------------------------------------- workloads
+
+def _dims(gdn, s, B, T, n_slots):
+    return gdn.make_dims(B=B, T=T, nk=s.nk, nv=s.nv, dk=s.dk, dv=s.dv, n_slots=n_slots)
+
+
+def _inp(gdn, d, acts=None, **kw):
+    a = acts if acts is not None else d
+    return gdn.make_inputs(*(a[n] for n in ACTS), *(d[n] for n in WN), **kw)
+
+
+def decode_bytes(s, B):
+    state = 2 * B * s.nv * s.dk * s.dv * 4
+    per_row = (s.C + s.vd + 2 * s.nv + s.vd) * 2 + 2 * 3 * s.C * 2   # x, z, a, b, out; conv tail r+w
+    weights = s.C * 4 * 2 + s.nv * 8 + s.dv * 2
+    return state + B * per_row + weights
+
+
+def phase_decode(gdn, world, steps, warmup, peak_hbm, e2e=True):
+    s, B = I.QWEN35_9B, 64
+    per_set = B * s.nv * s.dk * s.dv * 4
+    n_sets = max(4, math.ceil(3 * L2_BYTES / per_set))
+    sets = []
+    for i in range(n_sets):
+        d = I.decode_batch(seed=1 + 1009 * i, B=B, device="cuda")
+        d["out"] = torch.empty((B, 1, s.nv, s.dv), dtype=torch.bfloat16, device="cuda")
+        d["dims"] = _dims(gdn, s, B, 1, B)
+        d["inp"] = _inp(gdn, d)
+        sets.append(d)
+
+    def step(i, kt):
+        d = sets[i % n_sets]
+        call = lambda: gdn.decode_step(d["dims"], d["inp"], d["conv_state"], d["state"], d["out"])
+        kt.around(call) if kt else call()
+
+    ms, kms = timed(world, steps, warmup, step)
+    nbytes = decode_bytes(s, B)
+    res = {"tokens_per_s": B * world / (ms * 1e-3), "ms_per_step": ms, "tokens_per_step": B,
+           "kernel_ms": kms, "launches_per_step": 1,
+           "roofline": {"bound": "hbm", "achieved": nbytes / (kms * 1e-3) / 1e9, "peak": peak_hbm,
+                        "unit": "GB/s", "frac": nbytes / (kms * 1e-3) / 1e9 / peak_hbm,
+                        "traffic": dram_traffic("decode_kernel"), "algorithmic_bytes": nbytes},
+           "l2": f"inputs larger than L2: {n_sets} rotating layer buffer sets of {per_set / 2**20:.0f} MiB state"}
+    if e2e:
+        # end to end through the C-ABI: pinned host inputs -> device, step, output -> host
+        d = sets[0]
+        host = {n: d[n].cpu().pin_memory() for n in ACTS}
+        out_h = torch.empty(d["out"].shape, dtype=d["out"].dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_h.numel() * out_h.element_size()
+
+        def e2e_step(i, kt):
+            dd = sets[i % n_sets]
+            for n in ACTS:
+                dd[n].copy_(host[n], non_blocking=True)
+            gdn.decode_step(dd["dims"], dd["inp"], dd["conv_state"], dd["state"], dd["out"])
+            out_h.copy_(dd["out"], non_blocking=True)
+
+        ems, _ = timed(world, steps, warmup, e2e_step)
+        res["e2e"] = {"value": B * world / (ems * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                      "d2h_bytes_per_step": d2h}
+    del sets
+    torch.cuda.empty_cache()
+    return res
+
+
+def verify_bytes(s, P, K):
+    ck = P * K * s.nv * s.dk * s.dv * 4 + P * K * 3 * s.C * 2
+    state = s.nv * s.dk * s.dv * 4 + 3 * s.C * 2
+    acts = P * K * ((s.C + s.vd + 2 * s.nv + s.vd) * 2)
+    commit = 2 * (s.nv * s.dk * s.dv * 4 + 3 * s.C * 2)
+    return ck + state + acts + commit
+
+
+def phase_verify(gdn, world, steps, warmup, peak_hbm):
+    s, P, K = I.QWEN35_9B, 8, 8
+    n_sets = 2
+    sets = []
+    for i in range(n_sets):
+        d = I.verify_paths(seed=3 + 1009 * i, device="cuda")
+        d["out"] = torch.empty((P, K, s.nv, s.dv), dtype=torch.bfloat16, device="cuda")
+        d["cks"] = torch.empty((P, K, s.nv, s.dk, s.dv), dtype=torch.float32, device="cuda")
+        d["ckc"] = torch.empty((P, K, 3, s.C), dtype=torch.bfloat16, device="cuda")
+        d["idx"] = torch.zeros(P, dtype=torch.int32, device="cuda")
+        L = d["accept_len"].tolist()
+        win = max(range(P), key=lambda p: (L[p], -p))
+        d["src"] = torch.tensor([win * K + L[win] - 1 if L[win] > 0 else -1], dtype=torch.int32, device="cuda")
+        d["dst"] = torch.zeros(1, dtype=torch.int32, device="cuda")
+        d["dims"] = _dims(gdn, s, P, K, 1)
+        d["inp"] = _inp(gdn, d, state_idx=d["idx"])
+        d["cdims"] = _dims(gdn, s, 1, 1, 1)
+        sets.append(d)
+
+    def step(i, kt):
+        d = sets[i % n_sets]
+        ver = lambda: gdn.verify_with_checkpoints(d["dims"], d["inp"], d["conv_state"], d["state"], d["out"],
+                                                  d["cks"], d["ckc"])
+        kt.around(ver) if kt else ver()
+        gdn.state_copy(d["cdims"], d["cks"], d["ckc"], d["state"], d["conv_state"], d["src"], d["dst"], 1, P * K, 1)
+
+    ms, kms = timed(world, steps, warmup, step)
+    nbytes = verify_bytes(s, P, K)
+    vbytes = nbytes - 2 * (s.nv * s.dk * s.dv * 4 + 3 * s.C * 2)
+    res = {"tokens_per_s": P * K * world / (ms * 1e-3), "ms_per_step": ms, "tokens_per_step": P * K,
+           "kernel_ms": kms, "launches_per_step": 2, "algorithmic_bytes_per_step": nbytes,
+           "step_hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peak_hbm,
+           "roofline": {"bound": "hbm", "kernel": "verify_kernel", "achieved": vbytes / (kms * 1e-3) / 1e9,
+                        "peak": peak_hbm, "unit": "GB/s", "frac": vbytes / (kms * 1e-3) / 1e9 / peak_hbm,
+                        "traffic": dram_traffic("verify_kernel")}}
+    del sets
+    torch.cuda.empty_cache()
+    return res
+
+
+def prefill_flops_per_token(s, C=64):
+    d = s.dk
+    return s.nv * (10 * C * d + 6 * d * d + (2 / 3) * C * C)
+
+
+def prefill_bytes_per_token(s):
+    return (s.C + s.vd + 2 * s.nv + s.vd) * 2
+
+
+def phase_prefill(gdn, world, steps, warmup, peak_tf):
+    s, T, call = I.QWEN35_9B, 8192, 512
+    d = I.prefill_long(seed=2, T=T, device="cuda")
+    d["out"] = torch.empty((1, T, s.nv, s.dv), dtype=torch.bfloat16, device="cuda")
+    dm = _dims(gdn, s, 1, call, 1)
+    ws = gdn.workspace(dm)
+    calls = []
+    for c in range(T // call):
+        sl = slice(c * call, (c + 1) * call)
+        a = {n: d[n][:, sl] for n in ACTS}
+        calls.append((_inp(gdn, d, acts=a), d["out"][:, sl]))
+
+    def step(i, kt):
+        def run():
+            for inp, out in calls:
+                gdn.prefill_chunked(dm, inp, d["conv_state"], d["state"], out, ws)
+        kt.around(run) if kt else run()
+
+    ms, kms = timed(world, steps, warmup, step)
+    flops = prefill_flops_per_token(s) * T
+    res = {"tokens_per_s": T * world / (ms * 1e-3), "ms_per_step": ms, "tokens_per_step": T,
+           "ms_per_512_call": ms / (T // call), "launches_per_step": 2 * (T // call),
+           "roofline": {"bound": "tensor", "achieved": flops / (kms * 1e-3) / 1e12, "peak": peak_tf,
+                        "unit": "TFLOP/s", "frac": flops / (kms * 1e-3) / 1e12 / peak_tf,
+                        "traffic": None, "algorithmic_flops_per_token": prefill_flops_per_token(s)}}
+    del d, calls, ws
+    torch.cuda.empty_cache()
+    return res
+
+
+def phase_varlen(gdn, world, steps, warmup, peak_tf, n_layers=24):
+    s = I.QWEN35_9B
+    layers = []
+    for l in range(n_layers):
+        d = I.varlen_layer(l, device="cuda")
+        d["cu_dev"] = d["cu_seqlens"].to("cuda")
+        total = int(d["cu_seqlens"][-1])
+        d["out"] = torch.empty((1, total, s.nv, s.dv), dtype=torch.bfloat16, device="cuda")
+        d["dims"] = _dims(gdn, s, 32, total, 32)
+        d["inp"] = _inp(gdn, d, mask=d["mask"][0], cu_seqlens=d["cu_dev"])
+        layers.append(d)
+    ws = gdn.workspace(layers[0]["dims"])
+    real = sum(layers[0]["real"])
+    padded = int(layers[0]["cu_seqlens"][-1])
+
+    def step(i, kt):
+        def run():
+            for d in layers:
+                gdn.prefill_chunked(d["dims"], d["inp"], d["conv_state"], d["state"], d["out"], ws)
+        kt.around(run) if kt else run()
+
+    ms, kms = timed(world, steps, warmup, step)
+    flops = prefill_flops_per_token(s) * real * n_layers
+    res = {"real_tokens_per_s": real * world / (ms * 1e-3),
+           "layer_tokens_per_s": real * n_layers * world / (ms * 1e-3), "ms_per_step": ms,
+           "real_tokens": real, "padded_tokens": padded, "layers": n_layers, "launches_per_step": 2 * n_layers,
+           "roofline": {"bound": "tensor", "achieved": flops / (kms * 1e-3) / 1e12, "peak": peak_tf,
+                        "unit": "TFLOP/s", "frac": flops / (kms * 1e-3) / 1e12 / peak_tf, "traffic": None}}
+    del layers, ws
+    torch.cuda.empty_cache()
+    return res
+
+
+# ---------------------------------------------------------- CPU oracle
+
+def oracle_decode_rate(seconds=10.0, max_steps=None):
+    """The fp64 oracle on the decode workload (64 rows x 1 token x 32 heads),
+    repeated for about `seconds`; returns (tokens/s, steps, threads)."""
+    from oracle import oracle
+    oracle.build()
+    d = I.decode_batch(seed=1)
+    s = d["shape"]
+    threads = os.cpu_count() or 1
+    kw = dict(**{n: d[n] for n in ACTS}, **{n: d[n] for n in WN}, conv_state=d["conv_state"], state=d["state"],
+              nk=s.nk, nv=s.nv, dk=s.dk, dv=s.dv, n_threads=threads)
+    oracle.layer(**kw)  # load + warm
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle.layer(**kw)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or (max_steps and n >= max_steps):
+            break
+    return 64 * n / el, n, threads
+
+
+# ------------------------------------------------------------------ main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
+    ap.add_argument("--phases", default="decode,verify,prefill,varlen")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_setup()
+    steps, warmup = args.steps, max(3, args.warmup)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        oracle_decode_rate(seconds=0.0, max_steps=warmup)               # untimed warm-up steps
+        rate, n, threads = oracle_decode_rate(seconds=0.0, max_steps=steps)
+        line = {"impl": "reference", "metric": METRIC, "value": rate, "unit": "tokens/s", "n_gpus": 1,
+                "steps": steps, "warmup": warmup, "ms_per_step": 64 / rate * 1e3, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": "decode step: B=64 rows, T=1, 16 key / 32 value heads, d=128, fp32 state",
+                           "global_batch": 64, "seq_len": 1, "parallelism": "host threads"},
+                "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                                 "sample": f"{n} full decode steps of the workload (64 rows x 32 heads)"},
+                "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    from gated_deltanet_recurrence_delta_gb300 import build as gbuild
+    from gated_deltanet_recurrence_delta_gb300 import gdn
+    if rank == 0:
+        gbuild.build()
+    barrier(world)
+    gdn.load_library()
+    peak_hbm, peak_tf, peak_tf_sus, peak_src = peaks()
+    phases = [p for p in args.phases.split(",") if p]
+    results = {}
+    with ClockSampler(local) as clk:
+        results["decode"] = phase_decode(gdn, world, steps, warmup, peak_hbm)
+    clocks = clk.summary()
+    if "verify" in phases:
+        results["verify"] = phase_verify(gdn, world, steps, warmup, peak_hbm)
+    if "prefill" in phases:
+        results["prefill"] = phase_prefill(gdn, world, max(3, steps // 4), warmup, peak_tf_sus)
+    if "varlen" in phases:
+        results["varlen"] = phase_varlen(gdn, world, max(2, steps // 10), 3, peak_tf_sus)
+    gdn.check_status()
+
+    dec = results["decode"]
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, n, threads = oracle_decode_rate(seconds=10.0)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"{n} full decode steps of the headline workload (64 rows x 32 heads), ~10 s"}
+    launches = steps * dec["launches_per_step"]
+    line = {
+        "metric": METRIC, "value": dec["tokens_per_s"], "unit": "tokens/s", "n_gpus": world, "steps": steps,
+        "warmup": warmup, "ms_per_step": dec["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32 state, bf16 activations", "data": "synthetic",
+        "config": {"workload": "decode step: B=64 rows, T=1, 16 key / 32 value heads, d=128, fp32 state "
+                               "(Qwen3.5-9B-like GDN layer)",
+                   "global_batch": 64 * world, "seq_len": 1, "parallelism": f"dp{world} (rows, no collective)",
+                   "l2": dec["l2"]},
+        "roofline": dict(dec["roofline"], kernel="decode_kernel", peak_source=peak_src),
+        "cpu_baseline": cpu,
+        "e2e": dec.get("e2e"),
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "phases": results,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,35 @@
+// Host-side plumbing shared by the launchers of libgdn (not part of the C-ABI).
+#pragma once
+
+#include "gdn_common.cuh"
+
+namespace gdn {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  int id;
+  int sms;                 // streaming multiprocessors
+  unsigned int *status;    // device address of this device's status word
+};
+
+// Per-device facts of the current device, set up on first use (SM count and
+// the status word's device address). Returns GDN_OK or GDN_ERR_CUDA.
+gdn_status current_device(const DeviceInfo **out);
+// The current device's info; valid only after current_device() succeeded.
+const DeviceInfo &device_info();
+
+// Record `msg` as this thread's last error and return `code`.
+gdn_status fail(gdn_status code, const char *msg);
+// GDN_OK, or GDN_ERR_CUDA with the launch error of `what`.
+gdn_status check_launch(const char *what);
+
+gdn_status launch_decode(const LayerArgs &A, cudaStream_t stream);
+gdn_status launch_verify(const LayerArgs &A, float *ckpt_state, bf16 *ckpt_conv, cudaStream_t stream);
+size_t prefill_workspace_bytes(int B, int T, int nk, int nv, int D, bool packed);
+gdn_status launch_prefill(const LayerArgs &A, void *workspace, size_t workspace_bytes, cudaStream_t stream);
+gdn_status launch_state_copy(const float *src_state, const bf16 *src_conv, float *dst_state, bf16 *dst_conv,
+                             const int32_t *src_slot, const int32_t *dst_slot, int n, int n_src, int n_dst,
+                             size_t state_floats, size_t conv_elems, cudaStream_t stream);
+
+}  // namespace gdn

@@ -1,0 +1,66 @@
+// gdn_state_copy: dst[dst_slot[i]] <- src[src_slot[i]] for (state, conv tail)
+// slot pairs, the commit of an accepted verify prefix (generate.py, sparkle:
+// commit_tree_row) and the O(1) state bridge (uni_engine.py,
+// Qwen3.5-9B-SpeedX9-GDN32: copy_cache_ copies in place, addresses preserved).
+// A plain HBM copy: 16-byte vector loads and streaming stores, grid sized to
+// the SM count. Slot indices are device data, so a commit chosen on the GPU
+// needs no host round trip.
+#include "gdn_launch.h"
+
+namespace gdn {
+
+__global__ void __launch_bounds__(256) state_copy_kernel(const float4 *__restrict__ src_state,
+                                                         const uint4 *__restrict__ src_conv,
+                                                         float4 *__restrict__ dst_state, uint4 *__restrict__ dst_conv,
+                                                         const int32_t *src_slot, const int32_t *dst_slot, int n_src,
+                                                         int n_dst, size_t state_vec, size_t conv_vec,
+                                                         unsigned int *status) {
+  const int i = blockIdx.y;
+  const int ss = src_slot[i], ds = dst_slot[i];
+  if (ss == -1) return;  // nothing to commit for this pair
+  if (ss < 0 || ss >= n_src || ds < 0 || ds >= n_dst) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) set_status(status, GDN_ERR_INDEX);
+    return;
+  }
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  const size_t start = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const float4 *s = src_state + (size_t)ss * state_vec;
+  float4 *d = dst_state + (size_t)ds * state_vec;
+  size_t e = start;
+  // four independent 16-byte loads in flight per thread
+  for (; e + 3 * stride < state_vec; e += 4 * stride) {
+    const float4 a0 = __ldg(s + e), a1 = __ldg(s + e + stride), a2 = __ldg(s + e + 2 * stride),
+                 a3 = __ldg(s + e + 3 * stride);
+    __stcs(d + e, a0);
+    __stcs(d + e + stride, a1);
+    __stcs(d + e + 2 * stride, a2);
+    __stcs(d + e + 3 * stride, a3);
+  }
+  for (; e < state_vec; e += stride) __stcs(d + e, __ldg(s + e));
+  if (src_conv) {
+    const uint4 *sc = src_conv + (size_t)ss * conv_vec;
+    uint4 *dc = dst_conv + (size_t)ds * conv_vec;
+    for (size_t c = start; c < conv_vec; c += stride) dc[c] = __ldg(sc + c);
+  }
+}
+
+gdn_status launch_state_copy(const float *src_state, const bf16 *src_conv, float *dst_state, bf16 *dst_conv,
+                             const int32_t *src_slot, const int32_t *dst_slot, int n, int n_src, int n_dst,
+                             size_t state_floats, size_t conv_elems, cudaStream_t stream) {
+  const DeviceInfo &dev = device_info();
+  const size_t state_vec = state_floats / 4, conv_vec = conv_elems / 8;
+  // enough CTAs to keep every SM streaming; each thread moves >= 4 vectors
+  size_t want = (state_vec + 256 * 4 - 1) / (256 * 4);
+  size_t cap = (size_t)dev.sms * 4 / (size_t)n;
+  if (cap < 1) cap = 1;
+  if (want > cap) want = cap;
+  if (want < 1) want = 1;
+  dim3 grid((unsigned)want, (unsigned)n);
+  state_copy_kernel<<<grid, 256, 0, stream>>>(
+      reinterpret_cast<const float4 *>(src_state), reinterpret_cast<const uint4 *>(src_conv),
+      reinterpret_cast<float4 *>(dst_state), reinterpret_cast<uint4 *>(dst_conv), src_slot, dst_slot, n_src, n_dst,
+      state_vec, conv_vec, dev.status);
+  return check_launch("state_copy");
+}
+
+}  // namespace gdn

@@ -1,0 +1,171 @@
+// Per-token arithmetic of the Gated DeltaNet layer shared by the decode and the
+// verify kernels. Both kernels call exactly these functions with the same
+// thread mapping, so a verify checkpoint after token t equals, bit for bit, the
+// state after t+1 decode steps (generate.py, sparkle mlx_streaming/mtp: the
+// per-token checkpoints of the verify forward are committed without replay).
+//
+// Every rounding step is explicit (__fmaf_rn / __fmul_rn / __fadd_rn cannot be
+// contracted or reassociated by the compiler).
+#pragma once
+
+#include "gdn_common.cuh"
+
+namespace gdn {
+
+// Thread layout of a D x D fp32 state St[k][v] over 256 threads: each thread
+// owns 4 consecutive value columns (one float4) of RPT key rows; rows are
+// strided by NG so that a warp touches whole contiguous rows.
+template <int D>
+struct StateLayout {
+  static constexpr int NT = 256;
+  static constexpr int TPR = D / 4;     // threads per row
+  static constexpr int NG = NT / TPR;   // row groups
+  static constexpr int RPT = D / NG;    // rows per thread
+  static_assert(TPR <= 32 && NG * TPR == NT && RPT * NG == D, "unsupported head size");
+};
+
+__device__ __forceinline__ float sigmoid_f(float x) { return __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-x))); }
+__device__ __forceinline__ float silu_f(float x) { return __fmul_rn(x, sigmoid_f(x)); }
+// softplus(x) = log(1 + e^x); above 20 the correction is below 2.1e-9 and x is returned.
+__device__ __forceinline__ float softplus_f(float x) { return x > 20.0f ? x : log1pf(expf(x)); }
+
+// Depthwise conv of one channel at one token over xin rows t..t+3 (tap 3 is the
+// current token), then SiLU: statecache.py, CacheQwen35._gdn (fla_conv, no bias).
+__device__ __forceinline__ float conv4_silu(float w0, float w1, float w2, float w3, float x0, float x1,
+                                            float x2, float x3) {
+  float acc = __fmul_rn(w0, x0);
+  acc = __fmaf_rn(w1, x1, acc);
+  acc = __fmaf_rn(w2, x2, acc);
+  acc = __fmaf_rn(w3, x3, acc);
+  return silu_f(acc);
+}
+
+// L2-normalise a D-vector in shared memory in place and multiply by `scale`
+// (use_qk_l2norm_in_kernel: x / sqrt(sum x^2 + eps)). Called by one whole warp.
+template <int D>
+__device__ __forceinline__ void warp_l2norm(float *x, float eps, float scale, int lane) {
+  float s = 0.0f;
+#pragma unroll
+  for (int i = lane; i < D; i += 32) s = __fmaf_rn(x[i], x[i], s);
+  s = warp_sum_bcast(s);
+  const float r = __fdiv_rn(scale, sqrtf(__fadd_rn(s, eps)));
+#pragma unroll
+  for (int i = lane; i < D; i += 32) x[i] = __fmul_rn(x[i], r);
+  __syncwarp();
+}
+
+template <int D>
+__device__ __forceinline__ float warp_dot(const float *x, const float *y, int lane) {
+  float s = 0.0f;
+#pragma unroll
+  for (int i = lane; i < D; i += 32) s = __fmaf_rn(x[i], y[i], s);
+  return warp_sum_bcast(s);
+}
+
+// Gates of one (token, head): g = -exp(A_log) softplus(a + dt_bias),
+// beta = sigmoid(b) (gdn_gates). Returned as exp(g) and beta.
+__device__ __forceinline__ void gdn_gates(float a, float b, float A_log, float dt_bias, float &decay,
+                                          float &beta) {
+  const float g = __fmul_rn(-expf(A_log), softplus_f(__fadd_rn(a, dt_bias)));
+  decay = expf(g);
+  beta = sigmoid_f(b);
+}
+
+__device__ __forceinline__ float4 f4add(float4 a, float4 b) {
+  return make_float4(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y), __fadd_rn(a.z, b.z), __fadd_rn(a.w, b.w));
+}
+
+// One token of the delta rule on the thread's slice s[] of St (fla_gdr):
+//   St <- decay St;  u = v - St^T k;  St += beta k u^T;  o = St^T q
+// computed as  KS = St_old^T k, QS = St_old^T q  (one pass over the old state),
+//   u = v - decay KS,  St_new = decay St_old + (beta k) u^T,
+//   o = decay QS + (beta k.q) u          (bkq = beta * k.q)
+// qn, kn, vv: shared D-vectors (q already scaled). red: shared [2][NG][D]
+// scratch (k partials then q partials). Contains one __syncthreads. Threads of
+// row group 0 (tid < TPR, all in warp 0) return o for their 4 columns.
+template <int D>
+__device__ __forceinline__ void state_step(float4 (&s)[StateLayout<D>::RPT], const float *qn, const float *kn,
+                                           const float *vv, float decay, float beta, float bkq, float *red,
+                                           int tid, float4 &o) {
+  using L = StateLayout<D>;
+  const int cq = tid % L::TPR, grp = tid / L::TPR;
+  float4 pk = make_float4(0.f, 0.f, 0.f, 0.f), pq = pk;
+#pragma unroll
+  for (int i = 0; i < L::RPT; ++i) {
+    const int r = grp + i * L::NG;
+    const float kr = kn[r], qr = qn[r];
+    pk.x = __fmaf_rn(s[i].x, kr, pk.x);
+    pk.y = __fmaf_rn(s[i].y, kr, pk.y);
+    pk.z = __fmaf_rn(s[i].z, kr, pk.z);
+    pk.w = __fmaf_rn(s[i].w, kr, pk.w);
+    pq.x = __fmaf_rn(s[i].x, qr, pq.x);
+    pq.y = __fmaf_rn(s[i].y, qr, pq.y);
+    pq.z = __fmaf_rn(s[i].z, qr, pq.z);
+    pq.w = __fmaf_rn(s[i].w, qr, pq.w);
+  }
+  float4 *redk = reinterpret_cast<float4 *>(red);
+  float4 *redq = reinterpret_cast<float4 *>(red + L::NG * D);
+  redk[grp * L::TPR + cq] = pk;
+  redq[grp * L::TPR + cq] = pq;
+  __syncthreads();
+  float4 KS = redk[cq], QS = redq[cq];
+#pragma unroll
+  for (int g2 = 1; g2 < L::NG; ++g2) {
+    KS = f4add(KS, redk[g2 * L::TPR + cq]);
+    QS = f4add(QS, redq[g2 * L::TPR + cq]);
+  }
+  const float4 v4 = reinterpret_cast<const float4 *>(vv)[cq];
+  float4 u;
+  u.x = __fmaf_rn(-decay, KS.x, v4.x);
+  u.y = __fmaf_rn(-decay, KS.y, v4.y);
+  u.z = __fmaf_rn(-decay, KS.z, v4.z);
+  u.w = __fmaf_rn(-decay, KS.w, v4.w);
+#pragma unroll
+  for (int i = 0; i < L::RPT; ++i) {
+    const float bk = __fmul_rn(beta, kn[grp + i * L::NG]);
+    s[i].x = __fmaf_rn(bk, u.x, __fmul_rn(decay, s[i].x));
+    s[i].y = __fmaf_rn(bk, u.y, __fmul_rn(decay, s[i].y));
+    s[i].z = __fmaf_rn(bk, u.z, __fmul_rn(decay, s[i].z));
+    s[i].w = __fmaf_rn(bk, u.w, __fmul_rn(decay, s[i].w));
+  }
+  o.x = __fmaf_rn(bkq, u.x, __fmul_rn(decay, QS.x));
+  o.y = __fmaf_rn(bkq, u.y, __fmul_rn(decay, QS.y));
+  o.z = __fmaf_rn(bkq, u.z, __fmul_rn(decay, QS.z));
+  o.w = __fmaf_rn(bkq, u.w, __fmul_rn(decay, QS.w));
+}
+
+// Gated RMSNorm of one head's o (gated_rmsnorm: o / sqrt(mean o^2 + eps) * w *
+// silu(z)) and its bf16 store. Called by warp 0; lanes < TPR hold o.
+template <int D>
+__device__ __forceinline__ void rmsnorm_store(float4 o, int lane, const bf16 *z, const bf16 *w, float eps,
+                                              bf16 *out) {
+  using L = StateLayout<D>;
+  float ss = 0.0f;
+  if (lane < L::TPR) {
+    ss = __fmul_rn(o.x, o.x);
+    ss = __fmaf_rn(o.y, o.y, ss);
+    ss = __fmaf_rn(o.z, o.z, ss);
+    ss = __fmaf_rn(o.w, o.w, ss);
+  }
+  ss = warp_sum_bcast(ss);
+  const float r = __fdiv_rn(1.0f, sqrtf(__fadd_rn(__fdiv_rn(ss, (float)D), eps)));
+  if (lane < L::TPR) {
+    const int c = 4 * lane;
+    const float ov[4] = {o.x, o.y, o.z, o.w};
+    __align__(8) bf16 res[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float y = __fmul_rn(__fmul_rn(__fmul_rn(ov[e], r), ldbf(w + c + e)), silu_f(ldbf(z + c + e)));
+      res[e] = __float2bfloat16_rn(y);
+    }
+    *reinterpret_cast<uint2 *>(out + c) = *reinterpret_cast<const uint2 *>(res);
+  }
+}
+
+// Zero one head's bf16 output (padded tokens, skipped rows).
+template <int D>
+__device__ __forceinline__ void zero_head(bf16 *out, int tid) {
+  if (tid < D / 8) reinterpret_cast<uint4 *>(out)[tid] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+}  // namespace gdn

@@ -1,0 +1,150 @@
+"""Thin ctypes binding of ``libgdn.so`` (the C-ABI declared in ``include/gdn.h``).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA
+kernels. Tensors are torch CUDA tensors (device memory and streams come from
+PyTorch); their data pointers are handed to the C entry points of the same
+names. A non-OK status raises :class:`GdnError`. If the library has not been
+built, the first call raises instead of falling back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+import torch
+
+_PKG = Path(__file__).resolve().parent
+LIB_PATH = _PKG / "_build" / "libgdn.so"
+
+STATUS = {0: "GDN_OK", 1: "GDN_ERR_ARG", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_MASK", 4: "GDN_ERR_INDEX",
+          5: "GDN_ERR_CUDA", 6: "GDN_ERR_WORKSPACE", 7: "GDN_ERR_TIMEOUT"}
+EXPORTS = ("gdn_decode_step", "gdn_verify_with_checkpoints", "gdn_prefill_chunked",
+           "gdn_prefill_workspace_size", "gdn_state_copy", "gdn_check_status", "gdn_last_error")
+
+
+class GdnError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{STATUS.get(code, code)}: {msg}")
+        self.code = code
+        self.name = STATUS.get(code, str(code))
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("B", "T", "nk", "nv", "dk", "dv", "conv_k", "n_slots")] + [
+        ("scale", ctypes.c_float), ("l2_eps", ctypes.c_float), ("rms_eps", ctypes.c_float)]
+
+
+class Inputs(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("q", "k", "v", "z", "a", "b", "A_log", "dt_bias", "conv_w",
+                                               "norm_w", "mask", "cu_seqlens", "state_idx")]
+
+
+_lib = None
+
+
+def load_library(path: Path | str | None = None):
+    """Load libgdn.so (in-tree build). Raises if it is missing."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = Path(path) if path else LIB_PATH
+    if not p.exists():
+        raise RuntimeError(f"{p} is not built; run gated_deltanet_recurrence_delta_gb300.build.build()")
+    lib = ctypes.CDLL(str(p))
+    P = ctypes.c_void_p
+    DP = ctypes.POINTER(Dims)
+    IP = ctypes.POINTER(Inputs)
+    lib.gdn_decode_step.argtypes = [DP, IP, P, P, P, P]
+    lib.gdn_verify_with_checkpoints.argtypes = [DP, IP, P, P, P, P, P, P]
+    lib.gdn_prefill_chunked.argtypes = [DP, IP, P, P, P, P, ctypes.c_size_t, P]
+    lib.gdn_prefill_workspace_size.argtypes = [DP]
+    lib.gdn_prefill_workspace_size.restype = ctypes.c_size_t
+    lib.gdn_state_copy.argtypes = [DP, P, P, P, P, P, P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, P]
+    lib.gdn_check_status.argtypes = [P]
+    lib.gdn_last_error.restype = ctypes.c_char_p
+    for name in ("gdn_decode_step", "gdn_verify_with_checkpoints", "gdn_prefill_chunked", "gdn_state_copy",
+                 "gdn_check_status"):
+        getattr(lib, name).restype = ctypes.c_int
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def last_error() -> str:
+    return load_library().gdn_last_error().decode()
+
+
+def _check(code: int):
+    if code != 0:
+        raise GdnError(code, last_error())
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def make_dims(B, T, nk, nv, dk, dv, n_slots, conv_k=4, scale=None, l2_eps=1e-6, rms_eps=1e-6) -> Dims:
+    return Dims(B=B, T=T, nk=nk, nv=nv, dk=dk, dv=dv, conv_k=conv_k, n_slots=n_slots,
+                scale=dk ** -0.5 if scale is None else scale, l2_eps=l2_eps, rms_eps=rms_eps)
+
+
+def make_inputs(q, k, v, z, a, b, A_log, dt_bias, conv_w, norm_w, mask=None, cu_seqlens=None,
+                state_idx=None) -> Inputs:
+    return Inputs(q=_ptr(q), k=_ptr(k), v=_ptr(v), z=_ptr(z), a=_ptr(a), b=_ptr(b), A_log=_ptr(A_log),
+                  dt_bias=_ptr(dt_bias), conv_w=_ptr(conv_w), norm_w=_ptr(norm_w), mask=_ptr(mask),
+                  cu_seqlens=_ptr(cu_seqlens), state_idx=_ptr(state_idx))
+
+
+def decode_step(dims: Dims, inputs: Inputs, conv_state, recurrent_state, out, stream=None):
+    _check(load_library().gdn_decode_step(ctypes.byref(dims), ctypes.byref(inputs), _ptr(conv_state),
+                                          _ptr(recurrent_state), _ptr(out), _stream(stream)))
+
+
+def verify_with_checkpoints(dims: Dims, inputs: Inputs, conv_state, recurrent_state, out, ckpt_state, ckpt_conv,
+                            stream=None):
+    _check(load_library().gdn_verify_with_checkpoints(
+        ctypes.byref(dims), ctypes.byref(inputs), _ptr(conv_state), _ptr(recurrent_state), _ptr(out),
+        _ptr(ckpt_state), _ptr(ckpt_conv), _stream(stream)))
+
+
+def prefill_workspace_size(dims: Dims) -> int:
+    return int(load_library().gdn_prefill_workspace_size(ctypes.byref(dims)))
+
+
+def prefill_chunked(dims: Dims, inputs: Inputs, conv_state, recurrent_state, out, workspace, workspace_bytes=None,
+                    stream=None):
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load_library().gdn_prefill_chunked(ctypes.byref(dims), ctypes.byref(inputs), _ptr(conv_state),
+                                              _ptr(recurrent_state), _ptr(out), _ptr(workspace),
+                                              int(workspace_bytes), _stream(stream)))
+
+
+def state_copy(dims: Dims, src_state, src_conv, dst_state, dst_conv, src_slot, dst_slot, n, n_src_slots,
+               n_dst_slots, stream=None):
+    _check(load_library().gdn_state_copy(ctypes.byref(dims), _ptr(src_state), _ptr(src_conv), _ptr(dst_state),
+                                         _ptr(dst_conv), _ptr(src_slot), _ptr(dst_slot), int(n),
+                                         int(n_src_slots), int(n_dst_slots), _stream(stream)))
+
+
+def check_status(stream=None):
+    """Synchronise the stream and raise on a device-detected error."""
+    _check(load_library().gdn_check_status(_stream(stream)))
+
+
+def workspace(dims: Dims, device="cuda") -> torch.Tensor:
+    """A workspace tensor for gdn_prefill_chunked (torch allocations are 256-byte aligned)."""
+    n = prefill_workspace_size(dims)
+    return torch.empty(max(n, 1), dtype=torch.uint8, device=device)

@@ -1,0 +1,172 @@
+/*
+ * libgdn -- the Gated DeltaNet layer hot path on one GB300 GPU (sm_103a).
+ *
+ * The layer (statecache.py, squad-0.8b qev_fast: CacheQwen35._gdn):
+ *   xin = [conv_state (K-1 rows) ; x], x = q | k | v channels of each token
+ *   y   = silu(depthwise causal conv(xin, conv_w))  (no bias, last T outputs)
+ *   conv_state <- the last K-1 real inputs of xin (old rows if fewer arrive)
+ *   q, k <- L2-normalised per key head (q then times `scale`)
+ *   g = -exp(A_log) * softplus(a + dt_bias),  beta = sigmoid(b),  both * mask
+ *   value head h reads key head h / (nv / nk)
+ *   S_t = exp(g_t) S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,  o_t = S_t q_t
+ *   out = o / sqrt(mean(o^2) + rms_eps) * norm_w * silu(z)
+ * The recurrent state is stored transposed, St[k][v] (key-major, value
+ * contiguous), as StateCache keeps it: fp32 [slot][nv][dk][dv].
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     never allocates, frees or keeps them. All tensors are dense, row-major.
+ *   - bf16 = IEEE bfloat16 (2 bytes). Every pointer must be 16-byte aligned.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and is asynchronous: no entry point synchronises, except
+ *     gdn_check_status. No entry point reads device memory on the host, so
+ *     each call can be captured in a CUDA graph.
+ *   - Arguments are validated on the host before anything is launched; an
+ *     invalid call returns an error status, launches nothing and leaves every
+ *     buffer untouched. gdn_last_error() then describes it.
+ *   - Errors that only the device can see (a mask row that is not ones then
+ *     zeros, a slot index outside [0, n_slots)) are recorded in a device status
+ *     word; the offending row is skipped (its state, conv tail and outputs are
+ *     not written). gdn_check_status() reports and clears it.
+ *   - Rows of one decode or prefill call must name distinct state slots (they
+ *     are updated in place). Verify only reads the state, so its rows may share
+ *     one slot.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gdn_status {
+  GDN_OK = 0,
+  GDN_ERR_ARG = 1,       /* null or misaligned pointer, bad scalar */
+  GDN_ERR_SHAPE = 2,     /* unsupported dimensions */
+  GDN_ERR_MASK = 3,      /* (device) a mask row is not ones followed by zeros */
+  GDN_ERR_INDEX = 4,     /* (device) a slot index is outside [0, n_slots) */
+  GDN_ERR_CUDA = 5,      /* a CUDA runtime call failed */
+  GDN_ERR_WORKSPACE = 6, /* workspace missing or smaller than required */
+  GDN_ERR_TIMEOUT = 7    /* (device) a bounded wait inside a kernel expired */
+} gdn_status;
+
+/* Dimensions of one call.
+ *   B        rows (sequences) in the call
+ *   T        tokens per row (dense layout), or the total packed tokens when
+ *            cu_seqlens is given (prefill only)
+ *   nk, nv   key and value heads; nv % nk == 0 (GQA group G = nv / nk, G <= 8)
+ *   dk, dv   head sizes; dk == dv, one of 32, 64, 128
+ *   conv_k   conv kernel width; must be 4 (the saved tail holds conv_k-1 = 3 rows)
+ *   n_slots  rows of the conv_state / recurrent_state pools (slot range)
+ *   scale    multiplies q after its L2 normalisation (dk^-0.5 is usual)
+ *   l2_eps   q/k normalisation: x / sqrt(sum x^2 + l2_eps)
+ *   rms_eps  gated RMSNorm epsilon
+ * Channel count C = 2*nk*dk + nv*dv; C must be a multiple of 8. */
+typedef struct gdn_dims {
+  int32_t B, T, nk, nv, dk, dv, conv_k, n_slots;
+  float scale, l2_eps, rms_eps;
+} gdn_dims;
+
+/* Per-call inputs (device pointers; read only).
+ *   q, k    bf16 [B][T][nk*dk]   pre-conv query / key channels
+ *   v       bf16 [B][T][nv*dv]   pre-conv value channels
+ *   z       bf16 [B][T][nv*dv]   output gate
+ *   a, b    bf16 [B][T][nv]      decay and write-strength projections
+ *   A_log   fp32 [nv];  dt_bias fp32 [nv]
+ *   conv_w  bf16 [C][conv_k], channels ordered q | k | v; tap conv_k-1
+ *           multiplies the current token
+ *   norm_w  bf16 [dv], shared by all heads
+ *   mask    fp32 [B][T] (or [T] packed), 1 for a real token, 0 for padding,
+ *           ones then zeros within a row; NULL = all ones
+ *   cu_seqlens  NULL, or int32 [B+1] packed row offsets (prefill only): row r
+ *           holds packed tokens [cu_seqlens[r], cu_seqlens[r+1]); tensors are
+ *           then [1][T][...]
+ *   state_idx   NULL (row r uses slot r), or int32 [B] slot of each row */
+typedef struct gdn_inputs {
+  const void *q, *k, *v, *z, *a, *b;
+  const float *A_log, *dt_bias;
+  const void *conv_w, *norm_w;
+  const float *mask;
+  const int32_t *cu_seqlens;
+  const int32_t *state_idx;
+} gdn_inputs;
+
+/* One decode step (T == 1) for B rows, in place.
+ * statecache.py (squad-0.8b), CacheQwen35._gdn with a one-token chunk; the
+ * per-token decode of uni_engine.py (Qwen3.5-9B-SpeedX9-GDN32), whose decode
+ * graph this replaces at layer level.
+ *   conv_state       bf16 [n_slots][conv_k-1][C]   in/out
+ *   recurrent_state  fp32 [n_slots][nv][dk][dv]    in/out
+ *   out              bf16 [B][1][nv][dv]           gated-RMSNorm output
+ * A row whose mask is 0 is left untouched and gets zero output. */
+gdn_status gdn_decode_step(const gdn_dims *dims, const gdn_inputs *in, void *conv_state,
+                           float *recurrent_state, void *out, void *stream);
+
+/* Speculative verify of T <= 8 draft tokens per row with per-token checkpoints.
+ * generate.py (sparkle, mlx_streaming/mtp), tree_verify_step and the verify
+ * forward with per-token gated-delta checkpoints: the state after every token
+ * is kept so that an accepted prefix is committed without replay; the
+ * checkpoints equal, bit for bit, the state after that many gdn_decode_step
+ * calls on the same tokens.
+ *   conv_state, recurrent_state  as above, READ ONLY (rows may share a slot)
+ *   out        bf16 [B][T][nv][dv]
+ *   ckpt_state fp32 [B][T][nv][dk][dv]  state after token t of row b
+ *   ckpt_conv  bf16 [B][T][conv_k-1][C] conv tail after token t of row b
+ * For a padded token (mask 0) the checkpoints repeat the last real one and the
+ * output is zero. Commit with gdn_state_copy (src_slot = b*T + accepted-1). */
+gdn_status gdn_verify_with_checkpoints(const gdn_dims *dims, const gdn_inputs *in,
+                                       const void *conv_state, const float *recurrent_state,
+                                       void *out, float *ckpt_state, void *ckpt_conv,
+                                       void *stream);
+
+/* Chunked prefill of B rows continuing from their saved conv tail and state,
+ * in place (chunk size 64).
+ * statecache.py (squad-0.8b), CacheQwen35._gdn and StateCache's chunk graphs
+ * (rows continue from a saved state; padding masked by g = beta = 0 so that the
+ * state stops at the real end); generate.py (sparkle), prefill_chunked.
+ *   Dense layout: tensors [B][T][...]. Packed layout (cu_seqlens != NULL):
+ *   tensors [1][T][...], T = total packed tokens, mask [T].
+ *   out        bf16 [B][T][nv][dv] (or [1][T][nv][dv]); zero at padded tokens
+ *   workspace  device scratch of at least gdn_prefill_workspace_size(dims)
+ *              bytes, 256-byte aligned; its contents need not be preserved. */
+gdn_status gdn_prefill_chunked(const gdn_dims *dims, const gdn_inputs *in, void *conv_state,
+                               float *recurrent_state, void *out, void *workspace,
+                               size_t workspace_bytes, void *stream);
+
+/* Workspace bytes gdn_prefill_chunked needs for these dimensions (0 on invalid dims). */
+size_t gdn_prefill_workspace_size(const gdn_dims *dims);
+
+/* Copy n (recurrent state, conv tail) slot pairs: dst[dst_slot[i]] <- src[src_slot[i]].
+ * uni_engine.py (Qwen3.5-9B-SpeedX9-GDN32), copy_cache_: the O(1) state bridge
+ * copies only the fixed-size recurrent state in place, addresses preserved;
+ * generate.py (sparkle), commit_tree_row: commit a verified row's checkpoint.
+ * A state slot is nv*dk*dv fp32; a conv slot is (conv_k-1)*C bf16.
+ *   src_state / src_conv  [n_src_slots][...]   (e.g. the verify checkpoints,
+ *                         n_src_slots = B*T)
+ *   dst_state / dst_conv  [n_dst_slots][...]   (e.g. the persistent pools)
+ *   src_slot, dst_slot    DEVICE int32 [n]; src_slot[i] == -1 skips pair i
+ *                         (commit of an accept length of zero)
+ * Either conv pointer pair may be NULL to copy states only. Pairs must not
+ * write the same destination slot twice. */
+gdn_status gdn_state_copy(const gdn_dims *dims, const float *src_state, const void *src_conv,
+                          float *dst_state, void *dst_conv, const int32_t *src_slot,
+                          const int32_t *dst_slot, int32_t n, int32_t n_src_slots,
+                          int32_t n_dst_slots, void *stream);
+
+/* Synchronise `stream`, then return (and clear) a device-detected error
+ * recorded on the current device since the last check (GDN_ERR_MASK,
+ * GDN_ERR_INDEX, GDN_ERR_TIMEOUT; the lowest code wins when several were
+ * recorded), GDN_ERR_CUDA if the stream reports a CUDA error, else GDN_OK. */
+gdn_status gdn_check_status(void *stream);
+
+/* Description of the last non-OK status returned on this host thread. */
+const char *gdn_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

@@ -1,0 +1,56 @@
+"""Shared plumbing of the GPU parity tests: move seeded inputs to the device,
+call the C-ABI through the binding, run the oracle on the same inputs, and the
+spec tolerances (bf16 outputs max-abs <= 2e-2, final fp32 state
+relative Frobenius <= 1e-3)."""
+import numpy as np
+import torch
+
+from gated_deltanet_recurrence_delta_gb300 import gdn
+
+OUT_ATOL = 2e-2
+STATE_RTOL = 1e-3
+ACTS = ("q", "k", "v", "z", "a", "b")
+WEIGHTS = ("A_log", "dt_bias", "conv_w", "norm_w")
+
+
+def dev(x):
+    return x.to("cuda") if isinstance(x, torch.Tensor) else x
+
+
+def inputs(w, acts, mask=None, cu=None, state_idx=None):
+    """Device tensors -> gdn.Inputs (tensors must stay alive during the call)."""
+    return gdn.make_inputs(acts["q"], acts["k"], acts["v"], acts["z"], acts["a"], acts["b"], w["A_log"],
+                           w["dt_bias"], w["conv_w"], w["norm_w"], mask=mask, cu_seqlens=cu, state_idx=state_idx)
+
+
+def dims(shape, B, T, n_slots):
+    return gdn.make_dims(B=B, T=T, nk=shape.nk, nv=shape.nv, dk=shape.dk, dv=shape.dv, n_slots=n_slots)
+
+
+def oracle_layer(oracle, shape, w, acts, conv_state, state, mask=None, checkpoints=False):
+    return oracle.layer(**{n: acts[n].cpu() for n in ACTS}, **{n: w[n].cpu() for n in WEIGHTS},
+                        conv_state=conv_state.cpu(), state=state.cpu(),
+                        mask=None if mask is None else mask.cpu(), nk=shape.nk, nv=shape.nv, dk=shape.dk,
+                        dv=shape.dv, checkpoints=checkpoints)
+
+
+def max_abs(gpu, ref):
+    return float(np.max(np.abs(gpu.detach().cpu().double().numpy() - np.asarray(ref)))) if np.asarray(ref).size else 0.0
+
+
+def rel_fro(gpu, ref):
+    g = gpu.detach().cpu().double().numpy()
+    r = np.asarray(ref)
+    return float(np.linalg.norm(g - r) / max(np.linalg.norm(r), 1e-30))
+
+
+def assert_out(gpu, ref, what="out"):
+    err = max_abs(gpu, ref)
+    assert err <= OUT_ATOL, f"{what}: max abs err {err:.3e} > {OUT_ATOL}"
+    return err
+
+
+def assert_state(gpu, ref, what="state"):
+    err = rel_fro(gpu, ref)
+    assert err <= STATE_RTOL, f"{what}: rel Frobenius err {err:.3e} > {STATE_RTOL}"
+    return err

@@ -1,0 +1,159 @@
+"""The C-ABI library builds, loads, exports every entry point declared in
+include/gdn.h, and rejects invalid calls on the host before touching a GPU.
+(No call here reaches a CUDA API: every case fails validation first.)"""
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+from gated_deltanet_recurrence_delta_gb300 import build, gdn
+
+ROOT = Path(__file__).resolve().parent.parent
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return gdn.load_library()
+
+
+def _declared():
+    text = (ROOT / "include" / "gdn.h").read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared()
+    for n in ("gdn_prefill_chunked", "gdn_decode_step", "gdn_verify_with_checkpoints", "gdn_state_copy"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def _good_dims(**kw):
+    d = dict(B=2, T=1, nk=2, nv=4, dk=32, dv=32, n_slots=2)
+    d.update(kw)
+    return gdn.make_dims(**d)
+
+
+def _fake_inputs(base=1 << 20, **over):
+    # distinct 16-byte aligned fake device addresses: validation never dereferences them
+    names = [f for f, _ in gdn.Inputs._fields_]
+    vals = {n: base + 256 * i for i, n in enumerate(names)}
+    for n in ("mask", "cu_seqlens", "state_idx"):
+        vals[n] = None
+    vals.update(over)
+    return gdn.Inputs(**vals)
+
+
+P = 1 << 30  # fake aligned pointer
+
+
+def _status(fn, *args):
+    return fn(*args)
+
+
+@pytest.mark.parametrize("dims_kw,code", [
+    (dict(T=2), "GDN_ERR_SHAPE"),             # decode needs T == 1
+    (dict(dk=48, dv=48), "GDN_ERR_SHAPE"),    # unsupported head size
+    (dict(dk=32, dv=64), "GDN_ERR_SHAPE"),    # dk != dv
+    (dict(nv=3), "GDN_ERR_SHAPE"),            # nv % nk != 0
+    (dict(nk=1, nv=16), "GDN_ERR_SHAPE"),     # group > 8
+    (dict(n_slots=0), "GDN_ERR_SHAPE"),
+    (dict(B=-1), "GDN_ERR_SHAPE"),
+])
+def test_decode_rejects_bad_dims(lib, dims_kw, code):
+    d = _good_dims(**dims_kw)
+    st = lib.gdn_decode_step(ctypes.byref(d), ctypes.byref(_fake_inputs()), P, P, P, None)
+    assert gdn.STATUS[st] == code, gdn.last_error()
+
+
+def test_decode_rejects_conv_k(lib):
+    d = _good_dims(conv_k=3)
+    assert gdn.STATUS[lib.gdn_decode_step(ctypes.byref(d), ctypes.byref(_fake_inputs()), P, P, P, None)] == "GDN_ERR_SHAPE"
+
+
+@pytest.mark.parametrize("field", ["q", "k", "v", "z", "a", "b", "A_log", "dt_bias", "conv_w", "norm_w"])
+def test_decode_rejects_null_inputs(lib, field):
+    d = _good_dims()
+    st = lib.gdn_decode_step(ctypes.byref(d), ctypes.byref(_fake_inputs(**{field: None})), P, P, P, None)
+    assert gdn.STATUS[st] == "GDN_ERR_ARG"
+    assert field in gdn.last_error()
+
+
+def test_rejects_misaligned_pointer(lib):
+    d = _good_dims()
+    st = lib.gdn_decode_step(ctypes.byref(d), ctypes.byref(_fake_inputs(q=(1 << 20) + 2)), P, P, P, None)
+    assert gdn.STATUS[st] == "GDN_ERR_ARG" and "aligned" in gdn.last_error()
+    st = lib.gdn_decode_step(ctypes.byref(d), ctypes.byref(_fake_inputs()), P + 8, P, P, None)
+    assert gdn.STATUS[st] == "GDN_ERR_ARG"
+
+
+def test_null_dims_and_inputs(lib):
+    assert gdn.STATUS[lib.gdn_decode_step(None, ctypes.byref(_fake_inputs()), P, P, P, None)] == "GDN_ERR_ARG"
+    d = _good_dims()
+    assert gdn.STATUS[lib.gdn_decode_step(ctypes.byref(d), None, P, P, P, None)] == "GDN_ERR_ARG"
+
+
+def test_decode_rejects_cu_seqlens(lib):
+    d = _good_dims()
+    st = lib.gdn_decode_step(ctypes.byref(d), ctypes.byref(_fake_inputs(cu_seqlens=P)), P, P, P, None)
+    assert gdn.STATUS[st] == "GDN_ERR_ARG"
+
+
+@pytest.mark.parametrize("T", [0, 9])
+def test_verify_rejects_T(lib, T):
+    d = _good_dims(T=T)
+    st = lib.gdn_verify_with_checkpoints(ctypes.byref(d), ctypes.byref(_fake_inputs()), P, P, P, P, P, None)
+    assert gdn.STATUS[st] == "GDN_ERR_SHAPE"
+
+
+def test_verify_rejects_null_checkpoints(lib):
+    d = _good_dims(T=4)
+    st = lib.gdn_verify_with_checkpoints(ctypes.byref(d), ctypes.byref(_fake_inputs()), P, P, P, None, P, None)
+    assert gdn.STATUS[st] == "GDN_ERR_ARG"
+
+
+def test_prefill_workspace_rules(lib):
+    d = _good_dims(T=100)
+    need = lib.gdn_prefill_workspace_size(ctypes.byref(d))
+    assert need > 0
+    bad = _good_dims(dk=48, dv=48)
+    assert lib.gdn_prefill_workspace_size(ctypes.byref(bad)) == 0
+    st = lib.gdn_prefill_chunked(ctypes.byref(d), ctypes.byref(_fake_inputs()), P, P, P, P, need - 1, None)
+    assert gdn.STATUS[st] == "GDN_ERR_WORKSPACE"
+    st = lib.gdn_prefill_chunked(ctypes.byref(d), ctypes.byref(_fake_inputs()), P, P, P, None, need, None)
+    assert gdn.STATUS[st] == "GDN_ERR_WORKSPACE"
+    st = lib.gdn_prefill_chunked(ctypes.byref(d), ctypes.byref(_fake_inputs()), P, P, P, P + 16, need, None)
+    assert gdn.STATUS[st] == "GDN_ERR_WORKSPACE"  # not 256-byte aligned
+
+
+def test_empty_calls_launch_nothing(lib):
+    # B == 0 returns OK before any device work
+    d = _good_dims(B=0)
+    assert lib.gdn_decode_step(ctypes.byref(d), ctypes.byref(_fake_inputs()), P, P, P, None) == 0
+    d = _good_dims(B=0, T=3)
+    assert lib.gdn_verify_with_checkpoints(ctypes.byref(d), ctypes.byref(_fake_inputs()), P, P, P, P, P, None) == 0
+    d = _good_dims(T=0)
+    assert lib.gdn_prefill_chunked(ctypes.byref(d), ctypes.byref(_fake_inputs()), P, P, P, None, 0, None) == 0
+
+
+def test_state_copy_validation(lib):
+    d = _good_dims()
+    f = lib.gdn_state_copy
+    assert gdn.STATUS[f(ctypes.byref(d), None, None, P, None, P, P, 1, 1, 1, None)] == "GDN_ERR_ARG"
+    assert gdn.STATUS[f(ctypes.byref(d), P, P, P, None, P, P, 1, 1, 1, None)] == "GDN_ERR_ARG"  # conv pair
+    assert gdn.STATUS[f(ctypes.byref(d), P, None, P, None, P, P, -1, 1, 1, None)] == "GDN_ERR_SHAPE"
+    assert gdn.STATUS[f(ctypes.byref(d), P, None, P, None, P, P, 1, 0, 1, None)] == "GDN_ERR_SHAPE"
+    assert f(ctypes.byref(d), P, None, P, None, P, P, 0, 1, 1, None) == 0  # nothing to copy
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(RuntimeError):
+        gdn.load_library(tmp_path / "missing" / "libgdn.so")

@@ -1,0 +1,135 @@
+"""GPU parity of gdn_prefill_chunked against the fp64 oracle, through the C-ABI:
+a long row continued in 512-token calls, packed varlen rows padded to chunk
+buckets, short rows (conv tail shorter than the kernel), ragged tails."""
+import numpy as np
+import pytest
+import torch
+
+from gated_deltanet_recurrence_delta_gb300 import gdn
+from gated_deltanet_recurrence_delta_gb300 import inputs as I
+from tests.gpu_cases import ACTS, WEIGHTS, assert_out, assert_state, dev, dims, inputs, oracle_layer
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from gated_deltanet_recurrence_delta_gb300 import build
+    build.build()
+    gdn.load_library()
+
+
+def _wd(d):
+    return {n: dev(d[n]) for n in WEIGHTS}
+
+
+def _prefill(shape, w, acts, conv, S, mask=None, cu=None, B=None, state_idx=None, n_slots=None):
+    Bx, T = acts["q"].shape[0], acts["q"].shape[1]
+    B = Bx if B is None else B
+    out = torch.empty((Bx, T, shape.nv, shape.dv), dtype=torch.bfloat16, device="cuda")
+    dm = dims(shape, B, T, n_slots or conv.shape[0])
+    ws = gdn.workspace(dm)
+    gdn.prefill_chunked(dm, inputs(w, acts, mask=mask, cu=cu, state_idx=state_idx), conv, S, out, ws)
+    return out
+
+
+def test_long_row_in_512_token_calls(oracle_mod):
+    """T=8192 continued from a saved state in 16 calls of 512 tokens, against
+    one uninterrupted oracle pass."""
+    d = I.prefill_long(seed=2)
+    s = d["shape"]
+    w = _wd(d)
+    conv, S = dev(d["conv_state"]).clone(), dev(d["state"]).clone()
+    outs = []
+    for c in range(16):
+        sl = slice(512 * c, 512 * (c + 1))
+        outs.append(_prefill(s, w, {n: dev(d[n][:, sl].contiguous()) for n in ACTS}, conv, S))
+    gdn.check_status()
+    out = torch.cat(outs, 1)
+    ref = oracle_layer(oracle_mod, s, d, d, d["conv_state"], d["state"])
+    assert_out(out, ref["out"])
+    assert_state(S, ref["state"])
+    assert torch.equal(conv.cpu().double(), torch.from_numpy(ref["conv_state"]))
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 5, 64, 100, 130])
+def test_ragged_lengths_and_short_tails(oracle_mod, T):
+    """Lengths below the conv width, exactly one chunk, and ragged tails."""
+    shape = I.TINY
+    d = I.decode_batch(seed=30 + T, B=3, shape=shape)
+    g = torch.Generator().manual_seed(T)
+    acts = I.activations(shape, 3, T, g)
+    w = _wd(d)
+    conv, S = dev(d["conv_state"]).clone(), dev(d["state"]).clone()
+    out = _prefill(shape, w, {n: dev(a) for n, a in acts.items()}, conv, S)
+    gdn.check_status()
+    ref = oracle_layer(oracle_mod, shape, d, acts, d["conv_state"], d["state"])
+    assert_out(out, ref["out"])
+    assert_state(S, ref["state"])
+    assert torch.equal(conv.cpu().double(), torch.from_numpy(ref["conv_state"]))
+
+
+@pytest.mark.parametrize("shape", [I.Shape(nk=4, nv=8, dk=64, dv=64), I.Shape(nk=2, nv=4, dk=128, dv=128)])
+def test_head_sizes_with_padding(oracle_mod, shape):
+    d = I.decode_batch(seed=40, B=3, shape=shape)
+    T = 150
+    acts = I.activations(shape, 3, T, torch.Generator().manual_seed(41))
+    mask = torch.zeros((3, T))
+    for r, Lr in enumerate((150, 77, 0)):
+        mask[r, :Lr] = 1
+    w = _wd(d)
+    conv, S = dev(d["conv_state"]).clone(), dev(d["state"]).clone()
+    out = _prefill(shape, w, {n: dev(a) for n, a in acts.items()}, conv, S, mask=dev(mask))
+    gdn.check_status()
+    ref = oracle_layer(oracle_mod, shape, d, acts, d["conv_state"], d["state"], mask=mask)
+    for r, Lr in enumerate((150, 77, 0)):
+        assert_out(out[r, :Lr], ref["out"][r, :Lr])
+        assert torch.count_nonzero(out[r, Lr:]) == 0
+    assert_state(S, ref["state"])
+    assert torch.equal(conv.cpu().double(), torch.from_numpy(ref["conv_state"]))
+    # the row with no real token is untouched bit for bit
+    assert torch.equal(S[2].cpu(), d["state"][2]) and torch.equal(conv[2].cpu(), d["conv_state"][2])
+
+
+def test_varlen_rows_sampled(oracle_mod):
+    """32 packed rows, lengths U{16..2048} padded to chunk buckets (mask 0 on the
+    padding), each from its own state: layer 0 of the varlen stack at full size,
+    with the oracle run on the shortest, the longest and two other rows."""
+    d = I.varlen_layer(0)
+    s = d["shape"]
+    cu = d["cu_seqlens"]
+    w = _wd(d)
+    acts = {n: dev(d[n]) for n in ACTS}
+    conv, S = dev(d["conv_state"]).clone(), dev(d["state"]).clone()
+    out = _prefill(s, w, acts, conv, S, mask=dev(d["mask"][0]), cu=dev(cu), B=32)
+    gdn.check_status()
+    real = d["real"]
+    rows = sorted({int(np.argmin(real)), int(np.argmax(real)), 5, 17})
+    for r in rows:
+        a, b_ = int(cu[r]), int(cu[r + 1])
+        ra = {n: d[n][:, a:b_] for n in ACTS}
+        ref = oracle_layer(oracle_mod, s, d, ra, d["conv_state"][r:r + 1], d["state"][r:r + 1],
+                           mask=d["mask"][:, a:b_])
+        Lr = real[r]
+        assert_out(out[:, a:a + Lr], ref["out"][:, :Lr], f"row {r}")
+        assert torch.count_nonzero(out[:, a + Lr:b_]) == 0
+        assert_state(S[r], ref["state"][0], f"row {r}")
+        assert torch.equal(conv[r].cpu().double(), torch.from_numpy(ref["conv_state"][0]))
+
+
+def test_split_call_equals_whole_call(oracle_mod):
+    shape = I.TINY
+    d = I.decode_batch(seed=50, B=2, shape=shape)
+    acts = {n: dev(a) for n, a in I.activations(shape, 2, 192, torch.Generator().manual_seed(51)).items()}
+    w = _wd(d)
+    c1, S1 = dev(d["conv_state"]).clone(), dev(d["state"]).clone()
+    whole = _prefill(shape, w, acts, c1, S1)
+    c2, S2 = dev(d["conv_state"]).clone(), dev(d["state"]).clone()
+    parts = [_prefill(shape, w, {n: a[:, sl].contiguous() for n, a in acts.items()}, c2, S2)
+             for sl in (slice(0, 64), slice(64, 101), slice(101, 192))]
+    gdn.check_status()
+    assert torch.equal(c1, c2)
+    assert_state(S2, S1.cpu().double().numpy())
+    assert_out(torch.cat(parts, 1), whole.cpu().double().numpy())
