@@ -8,9 +8,15 @@
 //     alone (no cross-CTA hazard on the in-place tail);
 //   * each value head's state (one contiguous D*D fp32 block) is streamed into
 //     a ring of NS shared-memory stages by one bulk copy (cp.async.bulk, TMA
-//     engine) completing on an mbarrier; thread 0 refills a stage as soon as
-//     every thread has taken its slice into registers, so NS-1 heads are in
-//     flight while one is computed;
+//     engine) completing on a "full" mbarrier; a dedicated producer warp
+//     refills a stage as soon as the 8 compute warps have taken their slices
+//     into registers ("empty" mbarrier), so NS-1 heads are in flight while one
+//     is computed; the compute warps synchronise among themselves only
+//     (barrier 1), never with the producer;
+//   * the small per-unit inputs (token channels, conv tail, conv taps, z,
+//     gates) are loaded into registers one unit ahead, so their latency hides
+//     behind the current unit's state stream; row slots are resolved once
+//     into a shared table;
 //   * the new state goes straight from registers to HBM with streaming stores.
 // The per-token arithmetic is the shared code of gdn_token.cuh.
 #include "gdn_launch.h"
@@ -19,17 +25,88 @@
 namespace gdn {
 
 constexpr int kMaxG = 8;
+constexpr int kPre = 3;        // channels per thread prefetched one unit ahead
+constexpr int kZPre = 4;       // z values per thread prefetched one unit ahead
+constexpr int kSlotTable = 64; // units per CTA whose slots are tabulated
 
 template <int D, int NS>
 struct DecodeSmem {
   static constexpr int kStage = D * D;                          // floats per stage
-  static constexpr int kRed = 2 * 2 * StateLayout<D>::NG * D;   // [parity][k|q][NG][D]
-  static constexpr int kFront = (2 + kMaxG) * D + 4 * kMaxG;    // q, k, v[G], gates
-  static constexpr size_t kBytes = sizeof(float) * (size_t)(NS * kStage + kRed + kFront) + 8 * NS;
+  static constexpr int kRed = StepScratch<D>::kFloats;
+  static constexpr int kFront = (2 + kMaxG) * D + kMaxG * D + D + 4 * kMaxG;  // q,k,v[G], z[G], norm_w, gates
+  static constexpr size_t kBytes =
+      sizeof(float) * (size_t)(NS * kStage + kRed + kFront) + sizeof(int) * kSlotTable + 16 * NS;
 };
 
+// One unit's raw inputs, loaded a unit ahead of their use.
+struct FrontRegs {
+  uint2 w[kPre];                    // 4 conv taps (bf16) per channel
+  bf16 x[kPre], t0[kPre], t1[kPre], t2[kPre];
+  bf16 z[kZPre];
+  bf16 ga, gb;
+  float alog, dtb;
+};
+
+struct UnitGeom {
+  int D, G, kd, nv, C;
+  // channel (global index) and token source of unit-local channel e
+  __device__ __forceinline__ int chan(int e, int kh) const {
+    return e < D ? kh * D + e : (e < 2 * D ? kd + kh * D + (e - D) : 2 * kd + kh * G * D + (e - 2 * D));
+  }
+  __device__ __forceinline__ const bf16 *src(const LayerArgs &A, int b, int ch) const {
+    return ch < kd ? A.q + (size_t)b * kd + ch
+                   : (ch < 2 * kd ? A.k + (size_t)b * kd + (ch - kd) : A.v + (size_t)b * nv * D + (ch - 2 * kd));
+  }
+};
+
+__device__ __forceinline__ void load_front(FrontRegs &R, const LayerArgs &A, const UnitGeom &U, int b, int kh,
+                                           int slot, int tid) {
+  const int nch = (2 + U.G) * U.D;
+  const bf16 *cs = A.conv_state + (size_t)slot * KC * U.C;
+#pragma unroll
+  for (int i = 0; i < kPre; ++i) {
+    const int e = tid + 256 * i;
+    if (e < nch) {
+      const int ch = U.chan(e, kh);
+      R.x[i] = *U.src(A, b, ch);
+      R.t0[i] = cs[ch];
+      R.t1[i] = cs[U.C + ch];
+      R.t2[i] = cs[2 * U.C + ch];
+      R.w[i] = *reinterpret_cast<const uint2 *>(A.conv_w + (size_t)ch * 4);
+    }
+  }
+  const bf16 *zb = A.z + ((size_t)b * A.nv + kh * U.G) * U.D;
+#pragma unroll
+  for (int i = 0; i < kZPre; ++i) {
+    const int e = tid + 256 * i;
+    if (e < U.G * U.D) R.z[i] = zb[e];
+  }
+  if (tid < U.G) {
+    const int hh = kh * U.G + tid;
+    R.ga = A.a[(size_t)b * A.nv + hh];
+    R.gb = A.b[(size_t)b * A.nv + hh];
+    R.alog = A.A_log[hh];
+    R.dtb = A.dt_bias[hh];
+  }
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+// Barrier 1 over the compute threads with an OR reduction of `pred`.
+__device__ __forceinline__ bool compute_sync_or(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
+      " bar.red.or.pred q, 1, 256, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)pred)
+      : "memory");
+  return r != 0;
+}
+
 template <int D, int NS>
-__global__ void __launch_bounds__(256, 1) decode_kernel(LayerArgs A) {
+__global__ void __launch_bounds__(288, 1) decode_kernel(LayerArgs A) {
   using L = StateLayout<D>;
   using S = DecodeSmem<D, NS>;
   extern __shared__ __align__(128) float smem[];
@@ -38,27 +115,28 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(LayerArgs A) {
   float *fq = red + S::kRed;
   float *fk = fq + D;
   float *fv = fk + D;                  // [G][D]
-  float *fdecay = fv + kMaxG * D;      // [G]
+  float *fz = fv + kMaxG * D;          // [G][D]
+  float *fw = fz + kMaxG * D;          // [D] norm weight
+  float *fdecay = fw + D;              // [G]
   float *fbeta = fdecay + kMaxG;       // [G]
   float *fbkq = fbeta + kMaxG;         // [G]
-  uint64_t *full = reinterpret_cast<uint64_t *>(fbkq + 2 * kMaxG);
+  int *slot_tab = reinterpret_cast<int *>(fbkq + 2 * kMaxG);
+  uint64_t *full = reinterpret_cast<uint64_t *>(slot_tab + kSlotTable);
+  uint64_t *empty = full + NS;
+  const SyncCompute csync;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int G = A.G, kd = A.nk * D;
+  const int G = A.G;
+  const UnitGeom U{D, G, A.nk * D, A.nv, A.C};
   const int n_units = A.B * A.nk;
   if ((int)blockIdx.x >= n_units) return;
   const int my_units = (n_units - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
   const int n_tasks = my_units * G;
+  const int nch = (2 + G) * D;
 
-  // Task n of this CTA -> (row b, key head kh, value head h); -1 slot = skip.
-  auto task = [&](int n, int &b, int &kh, int &h) {
-    const int u = (int)blockIdx.x + (n / G) * (int)gridDim.x;
-    b = u / A.nk;
-    kh = u % A.nk;
-    h = kh * G + n % G;
-  };
-  // Slot of an active row, else -1 (bad slot or bad mask value recorded; mask 0 = skip).
-  auto active_slot = [&](int b, bool record) -> int {
+  // Slot of unit i's row, or -1 (mask 0 = skip; a bad mask value or slot is recorded).
+  auto resolve = [&](int i, bool record) -> int {
+    const int b = ((int)blockIdx.x + i * (int)gridDim.x) / A.nk;
     if (A.mask) {
       const float m = A.mask[b];
       if (m != 1.0f) {
@@ -70,10 +148,12 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(LayerArgs A) {
     if (s < 0 && record) set_status(A.status, GDN_ERR_INDEX);
     return s;
   };
-  auto issue = [&](int n) {  // thread 0 only
-    int b, kh, h;
-    task(n, b, kh, h);
-    const int slot = active_slot(b, false);
+  auto unit_slot = [&](int i) -> int { return i < kSlotTable ? slot_tab[i] : resolve(i, false); };
+  auto issue = [&](int n) {  // producer lane only
+    const int i = n / G;
+    const int u = (int)blockIdx.x + i * (int)gridDim.x;
+    const int h = (u % A.nk) * G + n % G;
+    const int slot = unit_slot(i);
     uint64_t *bar = &full[n % NS];
     if (slot >= 0) {
       mbar_arrive_expect_tx(bar, D * D * 4);
@@ -83,74 +163,113 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(LayerArgs A) {
     }
   };
 
+  for (int i = tid; i < my_units && i < kSlotTable; i += blockDim.x) slot_tab[i] = resolve(i, true);
+  for (int i = kSlotTable + tid; i < my_units; i += blockDim.x) (void)resolve(i, true);
+  for (int c = tid; c < D; c += blockDim.x) fw[c] = ldbf(A.norm_w + c);
   if (tid == 0) {
-    for (int s = 0; s < NS; ++s) mbar_init(&full[s], 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 8);  // one arrival per compute warp
+    }
     fence_mbar_init();
   }
   __syncthreads();
-  if (tid == 0)
-    for (int n = 0; n < NS && n < n_tasks; ++n) issue(n);
+
+  if (warp == 8) {
+    // ---- producer: stream every task's state into the stage ring
+    if (lane == 0) {
+      for (int n = 0; n < n_tasks; ++n) {
+        if (n >= NS && !mbar_wait_bounded(&empty[n % NS], (uint32_t)(((n / NS) - 1) & 1))) {
+          set_status(A.status, GDN_ERR_TIMEOUT);
+          break;
+        }
+        issue(n);
+      }
+    }
+    return;
+  }
+
+  FrontRegs R;
+  {
+    const int s0 = unit_slot(0);
+    const int u0 = (int)blockIdx.x;
+    if (s0 >= 0) load_front(R, A, U, u0 / A.nk, u0 % A.nk, s0, tid);
+  }
 
   for (int n = 0; n < n_tasks; ++n) {
-    int b, kh, h;
-    task(n, b, kh, h);
-    const int j = n % G;
-    const int slot = active_slot(b, j == 0 && tid == 0);
+    const int i = n / G, j = n % G;
+    const int u = (int)blockIdx.x + i * (int)gridDim.x;
+    const int b = u / A.nk, kh = u % A.nk, h = kh * G + j;
+    const int slot = unit_slot(i);
 
     if (j == 0 && slot >= 0) {
-      // ---- unit front end: conv (+ in-place tail shift), L2 norms, gates
-      __syncthreads();  // the previous unit is done with fq / fk / fv
+      // ---- unit front end from the prefetched registers
+      csync();  // the previous unit is done with fq / fk / fv / fz / gates
       bf16 *cs = A.conv_state + (size_t)slot * KC * A.C;
-      const int nch = (2 + G) * D;
-      for (int e = tid; e < nch; e += 256) {
-        int ch;
-        const bf16 *src;
-        if (e < D) {
-          ch = kh * D + e;
-          src = A.q + (size_t)b * kd + ch;
-        } else if (e < 2 * D) {
-          ch = kd + kh * D + (e - D);
-          src = A.k + (size_t)b * kd + (ch - kd);
-        } else {
-          ch = 2 * kd + kh * G * D + (e - 2 * D);
-          src = A.v + (size_t)b * A.nv * D + (ch - 2 * kd);
+#pragma unroll
+      for (int p = 0; p < kPre; ++p) {
+        const int e = tid + 256 * p;
+        if (e < nch) {
+          const int ch = U.chan(e, kh);
+          fq[e] = conv4_silu(bf_lo(R.w[p].x), bf_hi(R.w[p].x), bf_lo(R.w[p].y), bf_hi(R.w[p].y),
+                             __bfloat162float(R.t0[p]), __bfloat162float(R.t1[p]), __bfloat162float(R.t2[p]),
+                             __bfloat162float(R.x[p]));
+          cs[ch] = R.t1[p];
+          cs[A.C + ch] = R.t2[p];
+          cs[2 * A.C + ch] = R.x[p];
         }
-        const bf16 x0 = cs[ch], x1 = cs[A.C + ch], x2 = cs[2 * A.C + ch], x3 = *src;
+      }
+      for (int e = tid + 256 * kPre; e < nch; e += 256) {  // groups wider than the prefetch
+        const int ch = U.chan(e, kh);
+        const bf16 x0 = cs[ch], x1 = cs[A.C + ch], x2 = cs[2 * A.C + ch], x3 = *U.src(A, b, ch);
         const bf16 *w = A.conv_w + (size_t)ch * 4;
-        const float y = conv4_silu(ldbf(w), ldbf(w + 1), ldbf(w + 2), ldbf(w + 3), __bfloat162float(x0),
-                                   __bfloat162float(x1), __bfloat162float(x2), __bfloat162float(x3));
-        fq[e] = y;  // fq, fk, fv are contiguous
+        fq[e] = conv4_silu(ldbf(w), ldbf(w + 1), ldbf(w + 2), ldbf(w + 3), __bfloat162float(x0),
+                           __bfloat162float(x1), __bfloat162float(x2), __bfloat162float(x3));
         cs[ch] = x1;
         cs[A.C + ch] = x2;
         cs[2 * A.C + ch] = x3;
       }
-      __syncthreads();
+#pragma unroll
+      for (int p = 0; p < kZPre; ++p) {
+        const int e = tid + 256 * p;
+        if (e < G * D) fz[e] = __bfloat162float(R.z[p]);
+      }
+      for (int e = tid + 256 * kZPre; e < G * D; e += 256)
+        fz[e] = ldbf(A.z + ((size_t)b * A.nv + kh * G) * D + e);
+      float decay = 0.f, beta = 0.f;
+      if (tid < G) gdn_gates(__bfloat162float(R.ga), __bfloat162float(R.gb), R.alog, R.dtb, decay, beta);
+      // next unit's inputs, in flight while this unit's heads stream
+      if (i + 1 < my_units) {
+        const int s1 = unit_slot(i + 1);
+        const int u1 = u + (int)gridDim.x;
+        if (s1 >= 0) load_front(R, A, U, u1 / A.nk, u1 % A.nk, s1, tid);
+      }
+      csync();
       if (warp == 0) warp_l2norm<D>(fq, A.l2_eps, A.scale, lane);
       if (warp == 1) warp_l2norm<D>(fk, A.l2_eps, 1.0f, lane);
-      __syncthreads();
+      csync();
       if (warp == 0) {
         const float kq = warp_dot<D>(fq, fk, lane);
         if (lane < G) {
-          const int hh = kh * G + lane;
-          float decay, beta;
-          gdn_gates(ldbf(A.a + (size_t)b * A.nv + hh), ldbf(A.b + (size_t)b * A.nv + hh), A.A_log[hh],
-                    A.dt_bias[hh], decay, beta);
           fdecay[lane] = decay;
           fbeta[lane] = beta;
           fbkq[lane] = __fmul_rn(beta, kq);
         }
       }
-      __syncthreads();
+      csync();
+    } else if (j == 0 && i + 1 < my_units) {
+      // skipped unit: still prefetch the next one
+      const int s1 = unit_slot(i + 1);
+      const int u1 = u + (int)gridDim.x;
+      if (s1 >= 0) load_front(R, A, U, u1 / A.nk, u1 % A.nk, s1, tid);
     }
 
     // ---- the value head's state
     const bool ok = mbar_wait_bounded(&full[n % NS], (uint32_t)((n / NS) & 1));
-    if (__syncthreads_or(!ok)) {
-      if (tid == 0) {
-        set_status(A.status, GDN_ERR_TIMEOUT);
-        for (int m = n; m < n + NS && m < n_tasks; ++m)
-          (void)mbar_wait_bounded(&full[m % NS], (uint32_t)((m / NS) & 1));
-      }
+    if (compute_sync_or(!ok)) {
+      if (tid == 0) set_status(A.status, GDN_ERR_TIMEOUT);
+      // let copies already in flight land before the CTA's memory is released
+      if (tid < NS && n + tid < n_tasks) (void)mbar_wait_bounded(&full[(n + tid) % NS], (uint32_t)(((n + tid) / NS) & 1));
       return;
     }
     bf16 *out = A.out + ((size_t)b * A.nv + h) * D;
@@ -159,20 +278,17 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(LayerArgs A) {
       const float4 *st = reinterpret_cast<const float4 *>(stage + (n % NS) * S::kStage);
       float4 s[L::RPT];
 #pragma unroll
-      for (int i = 0; i < L::RPT; ++i) s[i] = st[(grp + i * L::NG) * L::TPR + cq];
+      for (int r = 0; r < L::RPT; ++r) s[r] = st[(grp + r * L::NG) * L::TPR + cq];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[n % NS]);  // this warp's slice is in registers
       float4 o;
-      state_step<D>(s, fq, fk, fv + j * D, fdecay[j], fbeta[j], fbkq[j], red + (n & 1) * 2 * L::NG * D, tid, o);
-      // every thread holds its slice: the stage may be refilled
-      if (tid == 0 && n + NS < n_tasks) {
-        fence_proxy_async_smem();
-        issue(n + NS);
-      }
+      state_step<D>(s, fq, fk, fv + j * D, fdecay[j], fbeta[j], fbkq[j], red, tid, o, csync);
       float4 *gs = reinterpret_cast<float4 *>(A.state + ((size_t)slot * A.nv + h) * D * D);
 #pragma unroll
-      for (int i = 0; i < L::RPT; ++i) st_cs(gs + (grp + i * L::NG) * L::TPR + cq, s[i]);
-      if (warp == 0) rmsnorm_store<D>(o, lane, A.z + ((size_t)b * A.nv + h) * D, A.norm_w, A.rms_eps, out);
+      for (int r = 0; r < L::RPT; ++r) st_cs(gs + (grp + r * L::NG) * L::TPR + cq, s[r]);
+      if (warp == 7) rmsnorm_store_smem<D>(o, lane, fz + j * D, fw, A.rms_eps, out);
     } else {
-      if (tid == 0 && n + NS < n_tasks) issue(n + NS);
+      if (lane == 0) mbar_arrive(&empty[n % NS]);
       zero_head<D>(out, tid);
     }
   }
@@ -190,12 +306,12 @@ static gdn_status launch_decode_t(const LayerArgs &A, cudaStream_t stream) {
     attr_set[dev.id] = true;
   }
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<D, NS>, 256, S::kBytes) != cudaSuccess ||
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<D, NS>, 288, S::kBytes) != cudaSuccess ||
       per_sm < 1)
     return fail(GDN_ERR_CUDA, "decode: kernel does not fit on an SM");
   const int n_units = A.B * A.nk;
   const int grid = n_units < dev.sms * per_sm ? n_units : dev.sms * per_sm;
-  decode_kernel<D, NS><<<grid, 256, S::kBytes, stream>>>(A);
+  decode_kernel<D, NS><<<grid, 288, S::kBytes, stream>>>(A);
   return check_launch("decode");
 }
 

@@ -112,8 +112,9 @@ __global__ void __launch_bounds__(256) prefill_front_kernel(LayerArgs A, int Tto
 template <int D>
 __global__ void __launch_bounds__(256, 2) prefill_recur_kernel(LayerArgs A, int Ttot, PrefillWs W) {
   using L = StateLayout<D>;
-  __shared__ __align__(16) float F[2][3][D];
-  __shared__ __align__(16) float red[2][2 * L::NG * D];
+  __shared__ __align__(16) float F[2][4][D];  // q, k, v, z of the current / next token
+  __shared__ float fw[D];
+  __shared__ __align__(16) float red[StepScratch<D>::kFloats];
   __shared__ float s_gate[3];
   __shared__ int s_min_zero, s_max_one, s_bad;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -183,15 +184,18 @@ __global__ void __launch_bounds__(256, 2) prefill_recur_kernel(LayerArgs A, int 
 #pragma unroll
   for (int i = 0; i < L::RPT; ++i) s[i] = gs[(grp + i * L::NG) * L::TPR + cq];
 
+  for (int c = tid; c < D; c += 256) fw[c] = ldbf(A.norm_w + c);
   auto fetch = [&](int t, float (&reg)[2]) {
     const size_t p = (size_t)start + t;
 #pragma unroll
     for (int k2 = 0; k2 < 2; ++k2) {
       const int e = tid + k2 * 256;
-      if (e < 3 * D) {
+      if (e < 4 * D) {
         const int which = e / D, c = e % D;
-        reg[k2] = which == 0 ? W.qn[(p * A.nk + kh) * D + c]
-                             : (which == 1 ? W.kn[(p * A.nk + kh) * D + c] : W.vv[(p * A.nv + h) * D + c]);
+        reg[k2] = which == 0   ? W.qn[(p * A.nk + kh) * D + c]
+                  : which == 1 ? W.kn[(p * A.nk + kh) * D + c]
+                  : which == 2 ? W.vv[(p * A.nv + h) * D + c]
+                               : ldbf(A.z + (p * A.nv + h) * D + c);
       }
     }
   };
@@ -202,7 +206,7 @@ __global__ void __launch_bounds__(256, 2) prefill_recur_kernel(LayerArgs A, int 
 #pragma unroll
     for (int k2 = 0; k2 < 2; ++k2) {
       const int e = tid + k2 * 256;
-      if (e < 3 * D) F[par][e / D][e % D] = cur[k2];
+      if (e < 4 * D) F[par][e / D][e % D] = cur[k2];
     }
     if (t + 1 < Lr) fetch(t + 1, cur);
     __syncthreads();
@@ -219,10 +223,9 @@ __global__ void __launch_bounds__(256, 2) prefill_recur_kernel(LayerArgs A, int 
     }
     __syncthreads();
     float4 o;
-    state_step<D>(s, F[par][0], F[par][1], F[par][2], s_gate[0], s_gate[1], s_gate[2], red[par], tid, o);
+    state_step<D>(s, F[par][0], F[par][1], F[par][2], s_gate[0], s_gate[1], s_gate[2], red, tid, o, SyncAll());
     if (warp == 0)
-      rmsnorm_store<D>(o, lane, A.z + ((size_t)start + t) * A.nv * D + h * D, A.norm_w, A.rms_eps,
-                       A.out + ((size_t)start + t) * A.nv * D + h * D);
+      rmsnorm_store_smem<D>(o, lane, F[par][3], fw, A.rms_eps, A.out + ((size_t)start + t) * A.nv * D + h * D);
     __syncthreads();  // s_gate is rewritten by the next token
   }
   for (int t = Lr; t < len; ++t) zero_head<D>(A.out + ((size_t)start + t) * A.nv * D + h * D, tid);

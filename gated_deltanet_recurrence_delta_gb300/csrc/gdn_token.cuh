@@ -71,22 +71,35 @@ __device__ __forceinline__ void gdn_gates(float a, float b, float A_log, float d
   beta = sigmoid_f(b);
 }
 
-__device__ __forceinline__ float4 f4add(float4 a, float4 b) {
-  return make_float4(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y), __fadd_rn(a.z, b.z), __fadd_rn(a.w, b.w));
-}
+// CTA-wide barrier over all threads.
+struct SyncAll {
+  __device__ __forceinline__ void operator()() const { __syncthreads(); }
+};
+// Barrier 1 over the 256 compute threads only (a producer warp stays out).
+struct SyncCompute {
+  __device__ __forceinline__ void operator()() const { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+};
+
+// Shared-memory floats state_step needs for its reductions.
+template <int D>
+struct StepScratch {
+  static constexpr int kFloats = 2 * StateLayout<D>::NG * D + 2 * D;  // partials [k|q][NG][D], totals [k|q][D]
+};
 
 // One token of the delta rule on the thread's slice s[] of St (fla_gdr):
 //   St <- decay St;  u = v - St^T k;  St += beta k u^T;  o = St^T q
 // computed as  KS = St_old^T k, QS = St_old^T q  (one pass over the old state),
 //   u = v - decay KS,  St_new = decay St_old + (beta k) u^T,
 //   o = decay QS + (beta k.q) u          (bkq = beta * k.q)
-// qn, kn, vv: shared D-vectors (q already scaled). red: shared [2][NG][D]
-// scratch (k partials then q partials). Contains one __syncthreads. Threads of
-// row group 0 (tid < TPR, all in warp 0) return o for their 4 columns.
-template <int D>
+// The column sums over the key rows run in two levels: per-thread partials
+// over its rows, then one thread per (k|q, column) adds the NG row-group
+// partials in order. qn, kn, vv: shared D-vectors (q already scaled). red:
+// StepScratch<D>::kFloats shared floats. Two barriers (Sync). Every thread
+// returns o for its 4 columns (threads with equal columns agree bit for bit).
+template <int D, class Sync>
 __device__ __forceinline__ void state_step(float4 (&s)[StateLayout<D>::RPT], const float *qn, const float *kn,
                                            const float *vv, float decay, float beta, float bkq, float *red,
-                                           int tid, float4 &o) {
+                                           int tid, float4 &o, Sync sync) {
   using L = StateLayout<D>;
   const int cq = tid % L::TPR, grp = tid / L::TPR;
   float4 pk = make_float4(0.f, 0.f, 0.f, 0.f), pq = pk;
@@ -103,17 +116,21 @@ __device__ __forceinline__ void state_step(float4 (&s)[StateLayout<D>::RPT], con
     pq.z = __fmaf_rn(s[i].z, qr, pq.z);
     pq.w = __fmaf_rn(s[i].w, qr, pq.w);
   }
-  float4 *redk = reinterpret_cast<float4 *>(red);
-  float4 *redq = reinterpret_cast<float4 *>(red + L::NG * D);
-  redk[grp * L::TPR + cq] = pk;
-  redq[grp * L::TPR + cq] = pq;
-  __syncthreads();
-  float4 KS = redk[cq], QS = redq[cq];
+  float *part = red;                       // [2][NG][D]
+  float *tot = red + 2 * L::NG * D;        // [2][D]
+  reinterpret_cast<float4 *>(part)[grp * L::TPR + cq] = pk;
+  reinterpret_cast<float4 *>(part + L::NG * D)[grp * L::TPR + cq] = pq;
+  sync();
+  if (tid < 2 * D) {
+    const float *p = part + (tid / D) * L::NG * D + tid % D;
+    float acc = p[0];
 #pragma unroll
-  for (int g2 = 1; g2 < L::NG; ++g2) {
-    KS = f4add(KS, redk[g2 * L::TPR + cq]);
-    QS = f4add(QS, redq[g2 * L::TPR + cq]);
+    for (int g2 = 1; g2 < L::NG; ++g2) acc = __fadd_rn(acc, p[g2 * D]);
+    tot[tid] = acc;
   }
+  sync();
+  const float4 KS = reinterpret_cast<const float4 *>(tot)[cq];
+  const float4 QS = reinterpret_cast<const float4 *>(tot + D)[cq];
   const float4 v4 = reinterpret_cast<const float4 *>(vv)[cq];
   float4 u;
   u.x = __fmaf_rn(-decay, KS.x, v4.x);
@@ -135,10 +152,12 @@ __device__ __forceinline__ void state_step(float4 (&s)[StateLayout<D>::RPT], con
 }
 
 // Gated RMSNorm of one head's o (gated_rmsnorm: o / sqrt(mean o^2 + eps) * w *
-// silu(z)) and its bf16 store. Called by warp 0; lanes < TPR hold o.
+// silu(z)) and its bf16 store. z and w are the head's values staged in shared
+// memory as fp32 (exact copies of the bf16 inputs). Called by one whole warp
+// whose lanes < TPR hold o for columns 4*lane .. 4*lane+3.
 template <int D>
-__device__ __forceinline__ void rmsnorm_store(float4 o, int lane, const bf16 *z, const bf16 *w, float eps,
-                                              bf16 *out) {
+__device__ __forceinline__ void rmsnorm_store_smem(float4 o, int lane, const float *z, const float *w, float eps,
+                                                   bf16 *out) {
   using L = StateLayout<D>;
   float ss = 0.0f;
   if (lane < L::TPR) {
@@ -155,7 +174,7 @@ __device__ __forceinline__ void rmsnorm_store(float4 o, int lane, const bf16 *z,
     __align__(8) bf16 res[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float y = __fmul_rn(__fmul_rn(__fmul_rn(ov[e], r), ldbf(w + c + e)), silu_f(ldbf(z + c + e)));
+      const float y = __fmul_rn(__fmul_rn(__fmul_rn(ov[e], r), w[c + e]), silu_f(z[c + e]));
       res[e] = __float2bfloat16_rn(y);
     }
     *reinterpret_cast<uint2 *>(out + c) = *reinterpret_cast<const uint2 *>(res);

@@ -17,10 +17,10 @@ constexpr int kMaxVerifyT = 8;
 
 template <int D>
 struct VerifySmem {
-  static constexpr int kFront = kMaxVerifyT * 3 * D;          // [t][q|k|v][D]
-  static constexpr int kRed = 2 * 2 * StateLayout<D>::NG * D;
+  static constexpr int kFront = kMaxVerifyT * 4 * D;          // [t][q|k|v|z][D]
+  static constexpr int kRed = StepScratch<D>::kFloats;
   static constexpr int kGates = 3 * kMaxVerifyT;
-  static constexpr size_t kBytes = sizeof(float) * (size_t)(kFront + kRed + kGates) + 16;
+  static constexpr size_t kBytes = sizeof(float) * (size_t)(kFront + kRed + kGates + D) + 16;
 };
 
 template <int D>
@@ -28,11 +28,13 @@ __global__ void __launch_bounds__(256, 2) verify_kernel(LayerArgs A, float *ckpt
   using L = StateLayout<D>;
   using S = VerifySmem<D>;
   extern __shared__ __align__(128) float smem[];
-  float *F = smem;                       // [T][3][D]
+  float *F = smem;                       // [T][3][D] conv outputs (q, k, v)
+  float *Z = F + kMaxVerifyT * 3 * D;    // [T][D] output gate
   float *red = F + S::kFront;
   float *gdecay = red + S::kRed;         // [T]
   float *gbeta = gdecay + kMaxVerifyT;   // [T]
   float *gbkq = gbeta + kMaxVerifyT;     // [T]
+  float *fw = gbkq + kMaxVerifyT;        // [D] norm weight
   __shared__ int s_Lr;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -43,6 +45,21 @@ __global__ void __launch_bounds__(256, 2) verify_kernel(LayerArgs A, float *ckpt
   if (slot < 0) {
     if (tid == 0) set_status(A.status, GDN_ERR_INDEX);
     return;
+  }
+  // ---- the state slice, in flight while the front end runs
+  const int cq = tid % L::TPR, grp = tid / L::TPR;
+  const float4 *gs = reinterpret_cast<const float4 *>(A.state + ((size_t)slot * A.nv + h) * D * D);
+  float4 s[L::RPT];
+#pragma unroll
+  for (int i = 0; i < L::RPT; ++i) s[i] = __ldg(gs + (grp + i * L::NG) * L::TPR + cq);
+
+  // gates of token tid (they do not depend on the conv)
+  if (tid < T) {
+    const size_t gi = ((size_t)b * T + tid) * A.nv + h;
+    float decay, beta;
+    gdn_gates(ldbf(A.a + gi), ldbf(A.b + gi), A.A_log[h], A.dt_bias[h], decay, beta);
+    gdecay[tid] = decay;
+    gbeta[tid] = beta;
   }
   if (tid == 0) {
     // The mask row must be ones then zeros; Lr = number of leading ones.
@@ -62,6 +79,8 @@ __global__ void __launch_bounds__(256, 2) verify_kernel(LayerArgs A, float *ckpt
   if (Lr < 0) return;
 
   // ---- front end for every token: conv over xin = [tail ; x], SiLU
+  for (int e = tid; e < T * D; e += 256) Z[e] = ldbf(A.z + (((size_t)b * T + e / D) * A.nv + h) * D + e % D);
+  for (int c = tid; c < D; c += 256) fw[c] = ldbf(A.norm_w + c);
   const bf16 *cs = A.conv_state + (size_t)slot * KC * C;
   const bool write_qk_tail = (h % A.G) == 0;  // one writer per key head's channels
   for (int e = tid; e < T * 3 * D; e += 256) {
@@ -111,31 +130,18 @@ __global__ void __launch_bounds__(256, 2) verify_kernel(LayerArgs A, float *ckpt
   __syncthreads();
   for (int t = warp; t < T; t += 8) {
     const float kq = warp_dot<D>(F + (t * 3) * D, F + (t * 3 + 1) * D, lane);
-    if (lane == 0) {
-      const size_t gi = ((size_t)b * T + t) * A.nv + h;
-      float decay, beta;
-      gdn_gates(ldbf(A.a + gi), ldbf(A.b + gi), A.A_log[h], A.dt_bias[h], decay, beta);
-      gdecay[t] = decay;
-      gbeta[t] = beta;
-      gbkq[t] = __fmul_rn(beta, kq);
-    }
+    if (lane == 0) gbkq[t] = __fmul_rn(gbeta[t], kq);
   }
   __syncthreads();
 
   // ---- the state: registers for all T tokens, a checkpoint after each
-  const int cq = tid % L::TPR, grp = tid / L::TPR;
-  const float4 *gs = reinterpret_cast<const float4 *>(A.state + ((size_t)slot * A.nv + h) * D * D);
-  float4 s[L::RPT];
-#pragma unroll
-  for (int i = 0; i < L::RPT; ++i) s[i] = __ldg(gs + (grp + i * L::NG) * L::TPR + cq);
-
   for (int t = 0; t < T; ++t) {
     bf16 *out = A.out + (((size_t)b * T + t) * A.nv + h) * D;
     if (t < Lr) {
       float4 o;
       state_step<D>(s, F + (t * 3) * D, F + (t * 3 + 1) * D, F + (t * 3 + 2) * D, gdecay[t], gbeta[t], gbkq[t],
-                    red + (t & 1) * 2 * L::NG * D, tid, o);
-      if (warp == 0) rmsnorm_store<D>(o, lane, A.z + (((size_t)b * T + t) * A.nv + h) * D, A.norm_w, A.rms_eps, out);
+                    red, tid, o, SyncAll());
+      if (warp == 0) rmsnorm_store_smem<D>(o, lane, Z + t * D, fw, A.rms_eps, out);
     } else {
       zero_head<D>(out, tid);
     }
