@@ -19,7 +19,8 @@ LIB_PATH = _PKG / "_build" / "libgdn.so"
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_ARG", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_MASK", 4: "GDN_ERR_INDEX",
           5: "GDN_ERR_CUDA", 6: "GDN_ERR_WORKSPACE", 7: "GDN_ERR_TIMEOUT"}
 EXPORTS = ("gdn_decode_step", "gdn_verify_with_checkpoints", "gdn_prefill_chunked",
-           "gdn_prefill_workspace_size", "gdn_state_copy", "gdn_check_status", "gdn_last_error")
+           "gdn_prefill_workspace_size", "gdn_state_copy", "gdn_check_status", "gdn_last_error",
+           "gdn_prefill_chunked_static_scratch")
 
 
 class GdnError(RuntimeError):
@@ -57,13 +58,14 @@ def load_library(path: Path | str | None = None):
     lib.gdn_decode_step.argtypes = [DP, IP, P, P, P, P]
     lib.gdn_verify_with_checkpoints.argtypes = [DP, IP, P, P, P, P, P, P]
     lib.gdn_prefill_chunked.argtypes = [DP, IP, P, P, P, P, ctypes.c_size_t, P]
+    lib.gdn_prefill_chunked_static_scratch.argtypes = [DP, IP, P, P, P, P]
     lib.gdn_prefill_workspace_size.argtypes = [DP]
     lib.gdn_prefill_workspace_size.restype = ctypes.c_size_t
     lib.gdn_state_copy.argtypes = [DP, P, P, P, P, P, P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, P]
     lib.gdn_check_status.argtypes = [P]
     lib.gdn_last_error.restype = ctypes.c_char_p
     for name in ("gdn_decode_step", "gdn_verify_with_checkpoints", "gdn_prefill_chunked", "gdn_state_copy",
-                 "gdn_check_status"):
+                 "gdn_check_status", "gdn_prefill_chunked_static_scratch"):
         getattr(lib, name).restype = ctypes.c_int
     if path is None:
         _lib = lib
@@ -130,6 +132,14 @@ def prefill_chunked(dims: Dims, inputs: Inputs, conv_state, recurrent_state, out
     _check(load_library().gdn_prefill_chunked(ctypes.byref(dims), ctypes.byref(inputs), _ptr(conv_state),
                                               _ptr(recurrent_state), _ptr(out), _ptr(workspace),
                                               int(workspace_bytes), _stream(stream)))
+
+
+def prefill_chunked_static_scratch(dims: Dims, inputs: Inputs, conv_state, recurrent_state, out, stream=None):
+    """gdn_prefill_chunked with the library's own 64 MiB static scratch (for
+    callers that cannot allocate device memory)."""
+    _check(load_library().gdn_prefill_chunked_static_scratch(ctypes.byref(dims), ctypes.byref(inputs),
+                                                             _ptr(conv_state), _ptr(recurrent_state), _ptr(out),
+                                                             _stream(stream)))
 
 
 def state_copy(dims: Dims, src_state, src_conv, dst_state, dst_conv, src_slot, dst_slot, n, n_src_slots,

@@ -139,6 +139,24 @@ gdn_status gdn_prefill_chunked(const gdn_dims *dims, const gdn_inputs *in, void 
 /* Workspace bytes gdn_prefill_chunked needs for these dimensions (0 on invalid dims). */
 size_t gdn_prefill_workspace_size(const gdn_dims *dims);
 
+/* gdn_prefill_chunked for callers that cannot allocate device memory (a
+ * serving engine whose pool owns all free HBM, a C host program without an
+ * allocator, a latency-critical loop where cudaMalloc could block or fail).
+ * No counterpart on the pages: it is a deployment variant of the call above.
+ * Same arguments and results as gdn_prefill_chunked, minus the workspace: the
+ * scratch is one 64 MiB device array inside this library, per GPU, held by
+ * every GPU on which this entry point has run until the process exits. It
+ * allocates nothing and calls no allocating routine.
+ *   - A call whose scratch need (gdn_prefill_workspace_size of its dims and
+ *     layout) exceeds 64 MiB returns GDN_ERR_WORKSPACE and launches nothing.
+ *   - All calls on a device share the array and it keeps the last call's
+ *     contents; calls that overlap on the GPU (unordered streams) race.
+ *   - The first call on a device looks up the array's device address (set-up
+ *     with that device current); make that first call before any stream
+ *     capture. */
+gdn_status gdn_prefill_chunked_static_scratch(const gdn_dims *dims, const gdn_inputs *in, void *conv_state,
+                                              float *recurrent_state, void *out, void *stream);
+
 /* Copy n (recurrent state, conv tail) slot pairs: dst[dst_slot[i]] <- src[src_slot[i]].
  * uni_engine.py (Qwen3.5-9B-SpeedX9-GDN32), copy_cache_: the O(1) state bridge
  * copies only the fixed-size recurrent state in place, addresses preserved;
