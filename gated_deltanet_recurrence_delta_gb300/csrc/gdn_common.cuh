@@ -100,6 +100,20 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
   return false;
 }
 
+// Wait for a phase with one polling thread: only `leader` spins on the
+// mbarrier (many threads spinning would flood the shared-memory pipe the TMA
+// and the other warps need); the rest sleep in the CTA barrier `sync_or`, then
+// take one (immediately successful) acquire test of their own. Returns false,
+// for every thread, when the leader's bounded wait expired.
+template <class SyncOr>
+__device__ __forceinline__ bool mbar_wait_leader(uint64_t *bar, uint32_t parity, bool leader, SyncOr sync_or) {
+  bool ok = true;
+  if (leader) ok = mbar_wait_bounded(bar, parity);
+  if (sync_or(!ok)) return false;
+  if (!leader) (void)mbar_try_wait(bar, parity);
+  return true;
+}
+
 // One bulk global -> shared copy completing on `bar` (16-byte aligned, size % 16 == 0).
 __device__ __forceinline__ void bulk_g2s(void *smem_dst, const void *gmem_src, uint32_t bytes, uint64_t *bar) {
   asm volatile(

@@ -265,8 +265,8 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(LayerArgs A) {
     }
 
     // ---- the value head's state
-    const bool ok = mbar_wait_bounded(&full[n % NS], (uint32_t)((n / NS) & 1));
-    if (compute_sync_or(!ok)) {
+    const bool ok = mbar_wait_leader(&full[n % NS], (uint32_t)((n / NS) & 1), tid == 0, compute_sync_or);
+    if (!ok) {
       if (tid == 0) set_status(A.status, GDN_ERR_TIMEOUT);
       // let copies already in flight land before the CTA's memory is released
       if (tid < NS && n + tid < n_tasks) (void)mbar_wait_bounded(&full[(n + tid) % NS], (uint32_t)(((n + tid) / NS) & 1));

@@ -5,7 +5,8 @@
 // g = beta = 0 so the state stops at the real end, and the conv tail keeps the
 // last K-1 real inputs.
 //
-// Kernels:
+// Head size 128 runs the chunked tensor-core path (gdn_prefill_tc.cu). Head
+// sizes 32 and 64 run the kernels below:
 //   1. front: depthwise conv + SiLU over [saved tail ; tokens] and the q/k L2
 //      norm, for every (token block, head channel group); results to the
 //      workspace (fp32). Reads the saved tail, writes nothing in place.
@@ -43,6 +44,7 @@ PrefillWs carve(void *ws, size_t Ttot, int nk, int nv, int D) {
 }  // namespace
 
 size_t prefill_workspace_bytes(int B, int T, int nk, int nv, int D, bool packed) {
+  if (D == 128) return prefill_tc_workspace_bytes(B, T, nk, nv, packed);
   const size_t Ttot = packed ? (size_t)T : (size_t)B * T;
   return 2 * align256(Ttot * nk * D * sizeof(float)) + align256(Ttot * nv * D * sizeof(float));
 }
@@ -246,7 +248,7 @@ static gdn_status launch_prefill_t(const LayerArgs &A, void *ws, cudaStream_t st
 
 gdn_status launch_prefill(const LayerArgs &A, void *ws, size_t, cudaStream_t stream) {
   switch (A.D) {
-    case 128: return launch_prefill_t<128>(A, ws, stream);
+    case 128: return launch_prefill_tc(A, ws, stream);
     case 64: return launch_prefill_t<64>(A, ws, stream);
     case 32: return launch_prefill_t<32>(A, ws, stream);
   }

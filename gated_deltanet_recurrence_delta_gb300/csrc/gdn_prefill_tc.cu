@@ -1,0 +1,949 @@
+// Chunked (WY / UT) prefill on the tcgen05 tensor cores, head size 128.
+//
+// statecache.py (squad-0.8b, qev_fast): fla_gdr over chunks of 64 tokens
+// ("fla's delta-rule chunk: 64"), continued from the saved fp32 state, padding
+// masked by g = beta = 0. Within a chunk, with G the inclusive prefix of g,
+// Gamma_ij = exp(G_i - G_j) (i >= j), gamma = exp(G), the state after token i is
+//   S_i = gamma_i S_0 + sum_{j<=i} Gamma_ij k_j u_j^T,
+// where the pseudo-values solve the unit-lower system (I + A) U' = diag(beta) V
+// - diag(beta gamma) K S_0 with A = strict_lower(diag(beta) (K K^T * Gamma)).
+// With T = (I + A)^-1, P = (Q K^T * Gamma) on and below the diagonal:
+//   W = T diag(beta gamma) K,  U = T diag(beta) V,  U' = U - W S_0
+//   O = diag(gamma) Q S_0 + P U' = Q' S_0 + P U,   Q' = diag(gamma) Q - P W
+//   S_C = gamma_C S_0 + (K * exp(G_C - G))^T U'
+// (S on the stored transpose St[k][v]). exp(-G) is never formed.
+//
+// Kernels (one call = front -> chunk -> state, stream ordered):
+//   front  conv + SiLU + q/k L2 norm per (chunk slot, head), written as split
+//          fp16 tiles (128B-swizzled K-major images): K and Q as [token][d],
+//          K^T and V^T as [d][token].
+//   chunk  per (chunk slot, value head), all chunks in parallel: [K;Q] K^T on
+//          tcgen05 (M=128,N=64,K=128); A and P in fp32 from TMEM; T by a
+//          blocked fp32 triangular inverse; R = P T (tcgen05); then one
+//          tcgen05 product [T; R] [beta gamma K | beta V] (M=128,N=256,K=64)
+//          yields W, U, P W (-> Q') and P U (= O_local). Writes W|Q' as one
+//          swizzled image, (K*exp(G_C-G))^T as another, U^T and O_local^T fp32.
+//   state  per (row, value head), sequential over its chunks with the state
+//          in registers (fp32) and an fp16 copy in shared memory:
+//          X = S_math [W;Q']^T (tcgen05 M=128,N=128,K=128) ->
+//          U' = U - X_W, O = X_Q + O_local (gated RMSNorm epilogue, bf16 out)
+//          dS = U'^T-image x (K~^T)-image (tcgen05 M=128,N=128,K=64) ->
+//          S = gamma_C S + dS.
+// Operand tiles move between HBM and shared memory with bulk copies (TMA).
+// Precision: accumulators are fp32. The chunk kernel runs every product in
+// split fp16 (x = hi + lo, hi = fp16(x), lo = fp16(x - hi); a*b ~ hi*hi +
+// hi*lo + lo*hi, ~21 significant bits), so W, U, Q', O_local reach the state
+// kernel nearly exact; the state kernel's two products take plain fp16
+// operands (10-bit mantissa; bf16 would leave the final state ~3e-3 off in
+// relative Frobenius norm). With every product in plain fp16 the normalised
+// outputs of badly conditioned tokens drift by ~1e-2.
+#include "gdn_launch.h"
+#include "gdn_token.cuh"
+#include "gdn_umma.cuh"
+
+namespace gdn {
+namespace tc {
+
+constexpr int CH = 64;   // chunk length
+constexpr int HD = 128;  // head size handled here
+
+// ------------------------------------------------------------ workspace
+
+struct Ws {
+  __half *kimg, *qimg;  // [S][nk][2 hi|lo][2][64][64]  K, Q as swizzled [token][dk] images (2 x 16 KiB)
+  __half *ktimg;        // [S][nk][2 hi|lo][128][64]    K^T as a swizzled [dk][token] image
+  __half *vtimg;        // [S][nv][2 hi|lo][128][64]    V^T as a swizzled [dv][token] image
+  __half *wq;           // [S][nv][2][128][64]  W (rows 0-63) | Q' (rows 64-127) image (32 KiB)
+  __half *kt;           // [S][nv][128][64]     (K * exp(G_C - G))^T image (16 KiB)
+  float *ut, *ot;       // [S][nv][128][64]     U^T and O_local^T (32 KiB each)
+  __half *gz;           // [S][nv][64][128]     norm_w * silu(z), row-major (16 KiB)
+  float *gc;            // [S][nv]              gamma_C
+};
+
+constexpr size_t kImg = 64 * 128;    // halves in a 64x128 image
+constexpr size_t kWQ = 128 * 128;    // halves in the W|Q' image
+constexpr size_t kRowF = 128 * 64;   // floats in U^T / O_local^T
+
+size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+size_t slots_total(int B, int T, bool packed) {
+  return packed ? (size_t)T / CH + (size_t)B + 1 : (size_t)B * (size_t)((T + CH - 1) / CH);
+}
+
+size_t ws_bytes(int B, int T, int nk, int nv, bool packed) {
+  const size_t S = slots_total(B, T, packed);
+  return 3 * a256(S * nk * kImg * 4) + a256(S * nv * kImg * 4) + a256(S * nv * kWQ * 2) +
+         a256(S * nv * kImg * 2) + 2 * a256(S * nv * kRowF * 4) + a256(S * nv * 4) + a256(S * nv * kImg * 2);
+}
+
+Ws carve(void *ws, int B, int T, int nk, int nv, bool packed) {
+  const size_t S = slots_total(B, T, packed);
+  char *p = static_cast<char *>(ws);
+  Ws w;
+  w.kimg = reinterpret_cast<__half *>(p);
+  p += a256(S * nk * kImg * 4);
+  w.qimg = reinterpret_cast<__half *>(p);
+  p += a256(S * nk * kImg * 4);
+  w.ktimg = reinterpret_cast<__half *>(p);
+  p += a256(S * nk * kImg * 4);
+  w.vtimg = reinterpret_cast<__half *>(p);
+  p += a256(S * nv * kImg * 4);
+  w.wq = reinterpret_cast<__half *>(p);
+  p += a256(S * nv * kWQ * 2);
+  w.kt = reinterpret_cast<__half *>(p);
+  p += a256(S * nv * kImg * 2);
+  w.ut = reinterpret_cast<float *>(p);
+  p += a256(S * nv * kRowF * 4);
+  w.ot = reinterpret_cast<float *>(p);
+  p += a256(S * nv * kRowF * 4);
+  w.gc = reinterpret_cast<float *>(p);
+  p += a256(S * nv * 4);
+  w.gz = reinterpret_cast<__half *>(p);
+  return w;
+}
+
+// ------------------------------------------------------------ row / slot map
+//
+// Dense rows: row r owns slots [r*cpr, (r+1)*cpr), cpr = ceil(T/64).
+// Packed rows: row r owns slots starting at floor(cu[r]/64) + r (one extra slot
+// per row covers its partial chunk; rows never overlap).
+
+struct Rows {
+  int B, T, cpr;  // cpr > 0: dense
+  const int32_t *cu;
+  __device__ __forceinline__ int start(int r) const { return cu ? cu[r] : r * T; }
+  __device__ __forceinline__ int len(int r) const { return cu ? cu[r + 1] - cu[r] : T; }
+  __device__ __forceinline__ int slot0(int r) const { return cu ? cu[r] / CH + r : r * cpr; }
+  // (row, chunk) of slot s, or row -1 when the slot holds no chunk
+  __device__ __forceinline__ void locate(int s, int Ttot, int &r, int &c) const {
+    if (!cu) {
+      r = s / cpr;
+      c = s % cpr;
+    } else {
+      int lo = 0, hi = B - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (slot0(mid) <= s) lo = mid; else hi = mid - 1;
+      }
+      r = lo;
+      c = s - slot0(lo);
+    }
+    const int st = start(r), ln = len(r);
+    if (r < 0 || r >= B || c < 0 || st < 0 || ln < 0 || st + ln > Ttot || c * CH >= ln) r = -1;
+  }
+};
+
+// Bounded mbarrier wait agreed across the CTA (thread 0 polls, the rest sleep
+// in the barrier); false = give up.
+__device__ __forceinline__ bool cta_wait(uint64_t *bar, uint32_t parity, unsigned int *status) {
+  const bool ok = mbar_wait_leader(bar, parity, threadIdx.x == 0, [](bool p) { return __syncthreads_or(p) != 0; });
+  if (!ok && threadIdx.x == 0) set_status(status, GDN_ERR_TIMEOUT);
+  return ok;
+}
+
+// ------------------------------------------------------------ split fp16
+
+__device__ __forceinline__ void split2(float a, float b, uint32_t &hi, uint32_t &lo) {
+  const __half ha = __float2half_rn(a), hb = __float2half_rn(b);
+  const __half la = __float2half_rn(a - __half2float(ha)), lb = __float2half_rn(b - __half2float(hb));
+  const __half2 h2 = __halves2half2(ha, hb), l2 = __halves2half2(la, lb);
+  hi = *reinterpret_cast<const uint32_t *>(&h2);
+  lo = *reinterpret_cast<const uint32_t *>(&l2);
+}
+__device__ __forceinline__ void split8(const float *x, uint4 &hi, uint4 &lo) {
+  split2(x[0], x[1], hi.x, lo.x);
+  split2(x[2], x[3], hi.y, lo.y);
+  split2(x[4], x[5], hi.z, lo.z);
+  split2(x[6], x[7], hi.w, lo.w);
+}
+// hi + lo of one fp16 pair of a split value
+__device__ __forceinline__ float2 join2(uint32_t hi, uint32_t lo) {
+  const float2 h = __half22float2(*reinterpret_cast<const __half2 *>(&hi));
+  const float2 l = __half22float2(*reinterpret_cast<const __half2 *>(&lo));
+  return make_float2(h.x + l.x, h.y + l.y);
+}
+// D = A B^T in split fp16: hi*hi + hi*lo + lo*hi (three accumulating tiles)
+__device__ __forceinline__ void umma_tile_split(uint32_t tmem_d, uint32_t a_hi, uint32_t a_lo, int RA, uint32_t b_hi,
+                                                uint32_t b_lo, int RB, int K, uint32_t idesc) {
+  umma_tile(tmem_d, a_hi, RA, b_hi, RB, K, idesc, false);
+  umma_tile(tmem_d, a_hi, RA, b_lo, RB, K, idesc, true);
+  umma_tile(tmem_d, a_lo, RA, b_hi, RB, K, idesc, true);
+}
+
+// ------------------------------------------------------------ front end
+
+__global__ void __launch_bounds__(256) front_kernel(LayerArgs A, Rows R, int Ttot, Ws W) {
+  __shared__ __align__(16) float Y[CH][HD];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int s = blockIdx.x, gi = blockIdx.y, kd = A.nk * HD;
+  int r, c;
+  R.locate(s, Ttot, r, c);
+  if (r < 0) return;
+  const int start = R.start(r), len = R.len(r);
+  const int which = gi < A.nk ? 0 : (gi < 2 * A.nk ? 1 : (gi < 2 * A.nk + A.nv ? 2 : 3));
+  const int head = which == 0 ? gi : (which == 1 ? gi - A.nk : (which == 2 ? gi - 2 * A.nk : gi - 2 * A.nk - A.nv));
+  const int slot = row_slot(A, r);
+  // thread -> 8 channels (cb) x 4 tokens (tb): 16-byte loads of 7 input rows
+  const int cb = tid & 15, tb = tid >> 4, pos0 = c * CH + 4 * tb;
+  if (which == 3) {
+    // output gate of value head `head`: norm_w * silu(z), fp16 [token][v]
+    const uint4 wv = __ldg(reinterpret_cast<const uint4 *>(A.norm_w) + cb);
+    const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
+    __half *gz = W.gz + ((size_t)s * A.nv + head) * kImg;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int pos = pos0 + t;
+      uint4 zv = make_uint4(0u, 0u, 0u, 0u);
+      if (pos < len) zv = __ldg(reinterpret_cast<const uint4 *>(A.z + ((size_t)(start + pos) * A.nv + head) * HD) + cb);
+      const uint32_t zs[4] = {zv.x, zv.y, zv.z, zv.w};
+      float y[8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        y[2 * e] = __uint_as_float(ws[e] << 16) * silu_fast(__uint_as_float(zs[e] << 16));
+        y[2 * e + 1] = __uint_as_float(ws[e] & 0xffff0000u) * silu_fast(__uint_as_float(zs[e] & 0xffff0000u));
+      }
+      reinterpret_cast<uint4 *>(gz)[(4 * tb + t) * 16 + cb] =
+          make_uint4(pack_h2(y[0], y[1]), pack_h2(y[2], y[3]), pack_h2(y[4], y[5]), pack_h2(y[6], y[7]));
+    }
+    return;
+  }
+  const int ch0 = which == 0 ? head * HD : (which == 1 ? kd + head * HD : 2 * kd + head * HD);
+  const bf16 *src = which == 0 ? A.q + head * HD : (which == 1 ? A.k + head * HD : A.v + head * HD);
+  const size_t rstride = which == 2 ? (size_t)A.nv * HD : (size_t)kd;
+  {
+    float wt[4][8];  // [tap][channel]
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {  // 8 channels x 4 taps = 64 bytes
+      const uint4 wq = __ldg(reinterpret_cast<const uint4 *>(A.conv_w + (size_t)(ch0 + 8 * cb) * 4) + q4);
+      const uint32_t wr[4] = {wq.x, wq.y, wq.z, wq.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {  // channel 2*q4 + e/2, taps 2*(e%2), 2*(e%2)+1
+        const int chl = 2 * q4 + (e >> 1), tap = 2 * (e & 1);
+        wt[tap][chl] = __uint_as_float(wr[e] << 16);
+        wt[tap + 1][chl] = __uint_as_float(wr[e] & 0xffff0000u);
+      }
+    }
+    float xr[7][8];  // input rows pos0-3 .. pos0+3, 8 channels
+#pragma unroll
+    for (int j = 0; j < 7; ++j) {
+      const int ip = pos0 - KC + j;
+      uint4 xv = make_uint4(0u, 0u, 0u, 0u);
+      if (slot >= 0 && ip < len) {
+        if (ip >= 0)
+          xv = __ldg(reinterpret_cast<const uint4 *>(src + (size_t)(start + ip) * rstride) + cb);
+        else
+          xv = *reinterpret_cast<const uint4 *>(A.conv_state + (size_t)slot * KC * A.C + (size_t)(KC + ip) * A.C + ch0 +
+                                                8 * cb);
+      }
+      const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        xr[j][2 * e] = __uint_as_float(xs[e] << 16);
+        xr[j][2 * e + 1] = __uint_as_float(xs[e] & 0xffff0000u);
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const bool ok = slot >= 0 && pos0 + t < len;
+      float y[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        y[e] = ok ? conv4_silu_fast(wt[0][e], wt[1][e], wt[2][e], wt[3][e], xr[t][e], xr[t + 1][e], xr[t + 2][e],
+                                    xr[t + 3][e])
+                  : 0.0f;
+      float4 *yr = reinterpret_cast<float4 *>(&Y[4 * tb + t][8 * cb]);
+      yr[0] = make_float4(y[0], y[1], y[2], y[3]);
+      yr[1] = make_float4(y[4], y[5], y[6], y[7]);
+    }
+  }
+  __syncthreads();
+  if (which < 2)
+    for (int i = warp; i < CH; i += 8) warp_l2norm<HD>(Y[i], A.l2_eps, which == 0 ? A.scale : 1.0f, lane);
+  __syncthreads();
+  // fp16 hi part and fp16 remainder (lo) of every value
+  if (which < 2) {
+    unsigned char *img = reinterpret_cast<unsigned char *>((which == 0 ? W.qimg : W.kimg) +
+                                                           ((size_t)s * A.nk + head) * 2 * kImg);
+    for (int e = tid; e < CH * 16; e += 256) {
+      const int i = e >> 4, c8 = e & 15;
+      uint4 hi, lo;
+      split8(&Y[i][c8 * 8], hi, lo);
+      *reinterpret_cast<uint4 *>(img + sw128_chunk(CH, i, c8)) = hi;
+      *reinterpret_cast<uint4 *>(img + kImg * 2 + sw128_chunk(CH, i, c8)) = lo;
+    }
+  }
+  if (which > 0) {
+    // transposed [channel][token] image: chunk (n, cj) holds tokens 8cj .. 8cj+7
+    unsigned char *img = reinterpret_cast<unsigned char *>(
+        which == 1 ? W.ktimg + ((size_t)s * A.nk + head) * 2 * kImg : W.vtimg + ((size_t)s * A.nv + head) * 2 * kImg);
+    for (int e = tid; e < HD * 8; e += 256) {
+      const int n = e & (HD - 1), cj = e >> 7;
+      float x[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) x[t] = Y[8 * cj + t][n];
+      uint4 hi, lo;
+      split8(x, hi, lo);
+      *reinterpret_cast<uint4 *>(img + sw128_chunk(HD, n, cj)) = hi;
+      *reinterpret_cast<uint4 *>(img + kImg * 2 + sw128_chunk(HD, n, cj)) = lo;
+    }
+  }
+}
+
+// ------------------------------------------------------------ chunk-local
+
+// Shared memory of chunk_kernel (bytes from a 1024-aligned base). "hi"/"lo"
+// are the two fp16 parts of a split operand.
+constexpr int kOffKQH = 0;       // [2 kb][128 rows][128 B]: K rows 0-63 | Q rows 64-127 (hi); later W|Q'
+constexpr int kOffKQL = 32768;   // the same, lo parts
+constexpr int kOffB2H = 65536;   // [256 rows][128 B]: (beta gamma K)^T rows 0-127 | (beta V)^T rows 128-255 (hi)
+constexpr int kOffB2L = 98304;   // the same, lo parts
+constexpr int kOffAF = 131072;   // fp32 [64][64]: A, then T in place; later the [T; R] image (hi)
+constexpr int kOffTRL = 147456;  // [T; R] image (lo)
+constexpr int kOffPTH = 163840;  // [128 rows][128 B]: P rows 0-63 | T^T rows 64-127 (hi)
+constexpr int kOffPTL = 180224;  // the same, lo parts
+constexpr int kOffSCR = 196608;  // fp32 [3][16][16] solve scratch
+constexpr int kOffSm = 199680;   // g, beta, G, exp(G), exp(G_C - G): fp32 [5][64]; barriers; tmem base
+constexpr int kChunkSmem = kOffSm + 2048 + 1024;  // + alignment slack
+
+__device__ __forceinline__ void store_split8(unsigned char *hi_img, unsigned char *lo_img, uint32_t off,
+                                             const float *x) {
+  uint4 hi, lo;
+  split8(x, hi, lo);
+  *reinterpret_cast<uint4 *>(hi_img + off) = hi;
+  *reinterpret_cast<uint4 *>(lo_img + off) = lo;
+}
+
+__global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int Ttot, Ws W) {
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  unsigned char *sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  unsigned char *KQH = sm + kOffKQH, *KQL = sm + kOffKQL;
+  unsigned char *B2H = sm + kOffB2H, *B2L = sm + kOffB2L;
+  float *AF = reinterpret_cast<float *>(sm + kOffAF);
+  unsigned char *TRH = sm + kOffAF, *TRL = sm + kOffTRL;
+  unsigned char *PTH = sm + kOffPTH, *PTL = sm + kOffPTL;
+  float *SCR = reinterpret_cast<float *>(sm + kOffSCR);
+  float *sg = reinterpret_cast<float *>(sm + kOffSm);  // g
+  float *sb = sg + 64;                                   // beta
+  float *sG = sb + 64;                                   // inclusive prefix of g
+  float *sgam = sG + 64;                                 // exp(G_j)
+  float *sec = sgam + 64;                                // exp(G_C - G_j)
+  uint64_t *bar_ld = reinterpret_cast<uint64_t *>(sec + 64);
+  uint64_t *bar_mma = bar_ld + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_mma + 1);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int s = blockIdx.x, h = blockIdx.y, kh = h / A.G;
+  int r, c;
+  R.locate(s, Ttot, r, c);
+  if (r < 0) return;
+  const int start = R.start(r), len = R.len(r);
+  const int nvalid = min(CH, len - c * CH);
+
+  if (tid == 0) {
+    mbar_init(bar_ld, 1);
+    mbar_init(bar_mma, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(tmem_slot, 256);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar_ld, 131072);
+    for (int part = 0; part < 2; ++part) {
+      const __half *ki = W.kimg + ((size_t)s * A.nk + kh) * 2 * kImg + part * kImg;
+      const __half *qi = W.qimg + ((size_t)s * A.nk + kh) * 2 * kImg + part * kImg;
+      unsigned char *dst = part ? KQL : KQH;
+      bulk_g2s(dst, ki, 8192, bar_ld);                 // K, column block 0
+      bulk_g2s(dst + 8192, qi, 8192, bar_ld);          // Q, column block 0
+      bulk_g2s(dst + 16384, ki + 4096, 8192, bar_ld);  // K, column block 1
+      bulk_g2s(dst + 24576, qi + 4096, 8192, bar_ld);  // Q, column block 1
+      unsigned char *b2 = part ? B2L : B2H;            // K^T rows 0-127, V^T rows 128-255
+      bulk_g2s(b2, W.ktimg + ((size_t)s * A.nk + kh) * 2 * kImg + part * kImg, 16384, bar_ld);
+      bulk_g2s(b2 + 16384, W.vtimg + ((size_t)s * A.nv + h) * 2 * kImg + part * kImg, 16384, bar_ld);
+    }
+  }
+  // gates of the chunk's tokens; padding and tokens past the row end get g = beta = 0
+  if (tid < CH) {
+    float g = 0.f, beta = 0.f;
+    if (tid < nvalid) {
+      const size_t p = (size_t)start + c * CH + tid;
+      if (!A.mask || A.mask[p] == 1.0f) {
+        // gdn_gates: g = -exp(A_log) softplus(a + dt_bias), beta = sigmoid(b)
+        g = __fmul_rn(-expf(A.A_log[h]), softplus_f(__fadd_rn(ldbf(A.a + p * A.nv + h), A.dt_bias[h])));
+        beta = sigmoid_f(ldbf(A.b + p * A.nv + h));
+      }
+    }
+    sg[tid] = g;
+    sb[tid] = beta;
+  }
+  __syncthreads();
+  if (warp == 0) {  // inclusive prefix over 64 values, two per lane
+    const float v0 = sg[2 * lane], v1 = v0 + sg[2 * lane + 1];
+    float run = v1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float t = __shfl_up_sync(0xffffffffu, run, o);
+      if (lane >= o) run += t;
+    }
+    const float excl = run - v1;
+    sG[2 * lane] = excl + v0;
+    sG[2 * lane + 1] = run;
+    __syncwarp();
+    const float GC = sG[CH - 1];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int j = 2 * lane + e;
+      sgam[j] = __expf(sG[j]);
+      sec[j] = __expf(GC - sG[j]);
+    }
+  }
+  if (!cta_wait(bar_ld, 0, A.status)) goto done;
+
+  // ---- [K; Q] K^T -> TMEM columns [0, 64)
+  if (tid == 0) {
+    tc_fence_after();
+    umma_tile_split(tmem, smem_u32(KQH), smem_u32(KQL), 128, smem_u32(KQH), smem_u32(KQL), 128, 128,
+                    umma_idesc_f16(128, 64));
+    umma_commit(bar_mma);
+  }
+  {
+    // while the tensor core runs: scale the K^T / V^T rows in place into
+    // (beta gamma K)^T and (beta V)^T, and write (K exp(G_C - G))^T (plain
+    // fp16) to the workspace
+    unsigned char *ktout = reinterpret_cast<unsigned char *>(W.kt + ((size_t)s * A.nv + h) * kImg);
+    for (int e = tid; e < 256 * 8; e += 256) {
+      const int n = e & 255, cj = e >> 8;  // row n, tokens 8cj .. 8cj+7
+      const uint32_t off = sw128_chunk(256, n, cj);
+      const uint4 hv = *reinterpret_cast<const uint4 *>(B2H + off), lv = *reinterpret_cast<const uint4 *>(B2L + off);
+      const uint32_t hs[4] = {hv.x, hv.y, hv.z, hv.w}, ls[4] = {lv.x, lv.y, lv.z, lv.w};
+      float x[8];
+#pragma unroll
+      for (int e2 = 0; e2 < 4; ++e2) {
+        const float2 f = join2(hs[e2], ls[e2]);
+        x[2 * e2] = f.x;
+        x[2 * e2 + 1] = f.y;
+      }
+      if (n < HD) {
+        float kt8[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const int j = 8 * cj + t;
+          kt8[t] = x[t] * sec[j];
+          x[t] = x[t] * (sb[j] * sgam[j]);
+        }
+        *reinterpret_cast<uint4 *>(ktout + sw128_chunk(128, n, cj)) =
+            make_uint4(pack_h2(kt8[0], kt8[1]), pack_h2(kt8[2], kt8[3]), pack_h2(kt8[4], kt8[5]),
+                       pack_h2(kt8[6], kt8[7]));
+      } else {
+#pragma unroll
+        for (int t = 0; t < 8; ++t) x[t] *= sb[8 * cj + t];
+      }
+      store_split8(B2H, B2L, off, x);
+    }
+    fence_proxy_async_smem();
+  }
+  if (!cta_wait(bar_mma, 0, A.status)) goto done;
+  tc_fence_after();
+  {
+    // A (rows 0-63: strictly lower, beta_i KK_ij Gamma_ij) in fp32; P (rows
+    // 64-127: QK_ij Gamma_ij for j <= i) as a split image
+    const int q = warp & 3, hh = warp >> 2, row = 32 * q + lane;
+    float v[32];
+    tmem_ld32(tmem_at(tmem, q, 32 * hh), v);
+    if (row < CH) {
+      const int i = row;
+      const float Gi = sG[i], bi = sb[i];
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) {
+        const int j = 32 * hh + jj;
+        AF[i * 64 + j] = j < i ? bi * v[jj] * __expf(Gi - sG[j]) : 0.0f;
+      }
+    } else {
+      const int i = row - CH;
+      const float Gi = sG[i];
+      float pv[32];
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) {
+        const int j = 32 * hh + jj;
+        pv[jj] = j <= i ? v[jj] * __expf(Gi - sG[j]) : 0.0f;
+      }
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) store_split8(PTH, PTL, sw128_chunk(128, i, 4 * hh + c4), pv + 8 * c4);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+
+  // ---- T = (I + A)^-1 in place, 16x16 blocks: diagonal blocks by forward
+  // substitution, then T_ab = -(sum_{b<c<=a} T_ac A_cb) T_bb column by column.
+  {
+    float x[16];
+    const int bb = tid >> 4, cc = tid & 15;
+    if (tid < 64) {
+      const float *Ab = AF + (16 * bb) * 64 + 16 * bb;
+#pragma unroll
+      for (int rr = 0; rr < 16; ++rr) {
+        float acc = rr == cc ? 1.0f : 0.0f;
+#pragma unroll
+        for (int l = 0; l < rr; ++l) acc = fmaf(-Ab[rr * 64 + l], x[l], acc);
+        x[rr] = acc;
+      }
+    }
+    __syncthreads();
+    if (tid < 64) {
+      float *Tb = AF + (16 * bb) * 64 + 16 * bb;
+#pragma unroll
+      for (int rr = 0; rr < 16; ++rr) Tb[rr * 64 + cc] = x[rr];
+    }
+    __syncthreads();
+    for (int b = 2; b >= 0; --b) {
+      const int nrows = 3 - b;
+      for (int e = tid; e < nrows * 256; e += 256) {
+        const int a = b + 1 + (e >> 8), rr = (e >> 4) & 15, m = e & 15;
+        float acc = 0.0f;
+        for (int cb = b + 1; cb <= a; ++cb) {
+          const float *Tac = AF + (16 * a + rr) * 64 + 16 * cb;
+          const float *Acb = AF + (16 * cb) * 64 + 16 * b + m;
+#pragma unroll
+          for (int k = 0; k < 16; ++k) acc = fmaf(Tac[k], Acb[k * 64], acc);
+        }
+        SCR[e] = acc;
+      }
+      __syncthreads();
+      float outv[3];
+      for (int e = tid, n = 0; e < nrows * 256; e += 256, ++n) {
+        const int rr = (e >> 4) & 15, m = e & 15;
+        const float *M = SCR + (e >> 8) * 256 + rr * 16;
+        const float *Tbb = AF + (16 * b) * 64 + 16 * b + m;
+        float acc = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) acc = fmaf(M[k], Tbb[k * 64], acc);
+        outv[n] = -acc;
+      }
+      __syncthreads();
+      for (int e = tid, n = 0; e < nrows * 256; e += 256, ++n) {
+        const int a = b + 1 + (e >> 8), rr = (e >> 4) & 15, m = e & 15;
+        AF[(16 * a + rr) * 64 + 16 * b + m] = outv[n];
+      }
+      __syncthreads();
+    }
+    // T (fp32, in AF) -> [T; R] split image rows 0-63 (hi aliases AF) and the
+    // split T^T image (rows 64-127 of the P tiles)
+    const int i = tid >> 2, q4 = tid & 3;
+    float t16[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) t16[k] = AF[i * 64 + 16 * q4 + k];
+    __syncthreads();
+#pragma unroll
+    for (int c2 = 0; c2 < 2; ++c2) store_split8(TRH, TRL, sw128_chunk(128, i, 2 * q4 + c2), t16 + 8 * c2);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const uint32_t off = sw128_off(128, CH + 16 * q4 + k, i);
+      const __half hv = __float2half_rn(t16[k]);
+      *reinterpret_cast<__half *>(PTH + off) = hv;
+      *reinterpret_cast<__half *>(PTL + off) = __float2half_rn(t16[k] - __half2float(hv));
+    }
+    fence_proxy_async_smem();
+  }
+  tc_fence_before();
+  __syncthreads();
+
+  // ---- R = P T -> TMEM columns [0, 64) (lanes 64-127 of this product are unused)
+  if (tid == 0) {
+    tc_fence_after();
+    umma_tile_split(tmem, smem_u32(PTH), smem_u32(PTL), 128, smem_u32(PTH) + CH * 128, smem_u32(PTL) + CH * 128,
+                    128, 64, umma_idesc_f16(128, 64));
+    umma_commit(bar_mma);
+  }
+  if (!cta_wait(bar_mma, 1, A.status)) goto done;
+  tc_fence_after();
+  if ((warp & 3) < 2) {
+    const int q = warp & 3, hh = warp >> 2, i = 32 * q + lane;
+    float v[32];
+    tmem_ld32(tmem_at(tmem, q, 32 * hh), v);
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) store_split8(TRH, TRL, sw128_chunk(128, CH + i, 4 * hh + c4), v + 8 * c4);
+    fence_proxy_async_smem();
+  }
+  tc_fence_before();
+  __syncthreads();
+
+  // ---- [T; R] [beta gamma K | beta V] -> TMEM columns [0, 256):
+  //   lanes 0-63: W (cols 0-127) | U (cols 128-255); lanes 64-127: P W | P U
+  if (tid == 0) {
+    tc_fence_after();
+    umma_tile_split(tmem, smem_u32(TRH), smem_u32(TRL), 128, smem_u32(B2H), smem_u32(B2L), 256, 64,
+                    umma_idesc_f16(128, 256));
+    umma_commit(bar_mma);
+  }
+  if (!cta_wait(bar_mma, 0, A.status)) goto done;
+  tc_fence_after();
+  {
+    const int q = warp & 3, hh = warp >> 2, row = 32 * q + lane, i = row & (CH - 1);
+    const bool upper = row >= CH;
+    const float gam = sgam[i];
+    float *ut = W.ut + ((size_t)s * A.nv + h) * kRowF;
+    float *ot = W.ot + ((size_t)s * A.nv + h) * kRowF;
+    for (int cb = 0; cb < 4; ++cb) {
+      float v[32];
+      tmem_ld32(tmem_at(tmem, q, 128 * hh + 32 * cb), v);
+      if (hh == 0) {
+        // W row i (dk columns 32cb..) or Q' = gamma Q - P W, plain fp16 for the state kernel
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          const uint32_t off = sw128_chunk(128, row, 4 * cb + c4);
+          uint4 *dst = reinterpret_cast<uint4 *>(KQH + off);
+          float y[8];
+          if (upper) {
+            const uint4 qh = *dst, ql = *reinterpret_cast<const uint4 *>(KQL + off);
+            const uint32_t hs[4] = {qh.x, qh.y, qh.z, qh.w}, ls[4] = {ql.x, ql.y, ql.z, ql.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = join2(hs[e], ls[e]);
+              y[2 * e] = gam * f.x - v[8 * c4 + 2 * e];
+              y[2 * e + 1] = gam * f.y - v[8 * c4 + 2 * e + 1];
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) y[e] = v[8 * c4 + e];
+          }
+          *dst = make_uint4(pack_h2(y[0], y[1]), pack_h2(y[2], y[3]), pack_h2(y[4], y[5]), pack_h2(y[6], y[7]));
+        }
+      } else {
+        // U or O_local, stored transposed: [v][i]
+        float *dst = upper ? ot : ut;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) dst[(32 * cb + e) * CH + i] = v[e];
+      }
+    }
+    if (tid == 0) W.gc[(size_t)s * A.nv + h] = sgam[CH - 1];
+    fence_proxy_async_smem();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    bulk_s2g(W.wq + ((size_t)s * A.nv + h) * kWQ, KQH, 32768);
+    bulk_commit();
+    bulk_wait_all();
+  }
+done:
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+// ------------------------------------------------------------ state pass
+
+constexpr int kSOffS = 0;         // S_math fp16 image [2 kb][128 rows][128 B]
+constexpr int kSOffWQ = 32768;    // 2 x W|Q' image (32 KiB each)
+constexpr int kSOffKT = 98304;    // 2 x K~^T image (16 KiB each)
+constexpr int kSOffUP = 131072;   // U'^T image [128 rows][128 B]
+constexpr int kSOffZ = 147456;    // 2 x output gate of the chunk, fp16 [64][128] (16 KiB each)
+constexpr int kSOffO = 180224;    // output rows of the chunk, bf16 [64][128]
+constexpr int kSOffRed = 196608;  // fp32 [4][64] RMS partials, [64] rstd, [128] norm weight
+constexpr int kSOffBar = kSOffRed + 4 * 64 * 4 + 64 * 4 + 128 * 4;
+constexpr int kStateSmem = kSOffBar + 64 + 1024;
+
+__device__ __forceinline__ void named_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// omap: out viewed as [Ttot][nv*dv] bf16, box [32 tokens][128 values].
+__global__ void __launch_bounds__(256, 1) state_kernel(LayerArgs A, Rows R, int Ttot, Ws W,
+                                                       const __grid_constant__ CUtensorMap omap) {
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  unsigned char *sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  unsigned char *SI = sm + kSOffS;
+  unsigned char *UP = sm + kSOffUP;
+  float *red = reinterpret_cast<float *>(sm + kSOffRed);  // [4][64]
+  float *rstd = red + 256;                                // [64]
+  float *fw = rstd + 64;                                  // [128]
+  uint64_t *bar_ld = reinterpret_cast<uint64_t *>(sm + kSOffBar);  // [2]
+  uint64_t *bar_mma = bar_ld + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_mma + 1);
+  __shared__ int s_min_zero, s_max_one, s_bad;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = blockIdx.x / A.nv, h = blockIdx.x % A.nv, kh = h / A.G;
+  const int kd = A.nk * HD, C = A.C;
+  const int start = R.start(b), len = R.len(b);
+  const int slot = row_slot(A, b);
+  if (slot < 0 || start < 0 || len < 0 || start + len > Ttot) {
+    if (tid == 0) set_status(A.status, GDN_ERR_INDEX);
+    return;
+  }
+  // real length: the mask row must be ones then zeros
+  if (tid == 0) {
+    s_min_zero = len;
+    s_max_one = -1;
+    s_bad = 0;
+  }
+  __syncthreads();
+  if (A.mask)
+    for (int i = tid; i < len; i += 256) {
+      const float m = A.mask[start + i];
+      if (m == 1.0f) atomicMax(&s_max_one, i);
+      else if (m == 0.0f) atomicMin(&s_min_zero, i);
+      else s_bad = 1;
+    }
+  __syncthreads();
+  const int Lr = s_min_zero;
+  if (s_bad || s_max_one >= Lr) {
+    if (tid == 0) set_status(A.status, GDN_ERR_MASK);
+    return;
+  }
+  // conv tail: xin rows Lr .. Lr+2 (old rows when Lr < 3), own channels only
+  {
+    bf16 *cs = A.conv_state + (size_t)slot * KC * C;
+    const bool qk = (h % A.G) == 0;
+    const int nch = qk ? 3 * HD : HD;
+    for (int e = tid; e < nch; e += 256) {
+      const int which = qk ? e / HD : 2, cc = e % HD;
+      const int ch = which == 0 ? kh * HD + cc : (which == 1 ? kd + kh * HD + cc : 2 * kd + h * HD + cc);
+      const bf16 *src = which == 0 ? A.q + kh * HD + cc : (which == 1 ? A.k + kh * HD + cc : A.v + h * HD + cc);
+      const size_t rstride = which == 2 ? (size_t)A.nv * HD : (size_t)kd;
+      bf16 nv3[KC];
+#pragma unroll
+      for (int rr = 0; rr < KC; ++rr) {
+        const int xi = Lr + rr;
+        nv3[rr] = xi < KC ? cs[(size_t)xi * C + ch] : src[(size_t)(start + xi - KC) * rstride];
+      }
+#pragma unroll
+      for (int rr = 0; rr < KC; ++rr) cs[(size_t)rr * C + ch] = nv3[rr];
+    }
+  }
+  for (int cc = tid; cc < HD; cc += 256) fw[cc] = ldbf(A.norm_w + cc);
+
+  const int n_chunks = (len + CH - 1) / CH;
+  const int s0 = R.slot0(b);
+  if (tid == 0) {
+    mbar_init(&bar_ld[0], 1);
+    mbar_init(&bar_ld[1], 1);
+    mbar_init(bar_mma, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(tmem_slot, 256);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // chunk ci's operand tiles and its output gate norm_w * silu(z)
+  auto issue_loads = [&](int ci) {  // thread 0
+    const int buf = ci & 1, s = s0 + ci;
+    mbar_arrive_expect_tx(&bar_ld[buf], 32768 + 16384 + 16384);
+    bulk_g2s(sm + kSOffWQ + buf * 32768, W.wq + ((size_t)s * A.nv + h) * kWQ, 32768, &bar_ld[buf]);
+    bulk_g2s(sm + kSOffKT + buf * 16384, W.kt + ((size_t)s * A.nv + h) * kImg, 16384, &bar_ld[buf]);
+    bulk_g2s(sm + kSOffZ + buf * 16384, W.gz + ((size_t)s * A.nv + h) * kImg, 16384, &bar_ld[buf]);
+  };
+  if (tid == 0 && n_chunks > 0) issue_loads(0);
+
+  // thread <-> (value row v = TMEM lane, key half hh)
+  const int q = warp & 3, hh = warp >> 2, v = 32 * q + lane;
+  float Sv[64];
+  float *gS = A.state + ((size_t)slot * A.nv + h) * HD * HD;
+#pragma unroll
+  for (int k = 0; k < 64; ++k) Sv[k] = gS[(size_t)(64 * hh + k) * HD + v];
+  auto write_simg = [&]() {
+#pragma unroll
+    for (int c8 = 0; c8 < 8; ++c8)
+      *reinterpret_cast<uint4 *>(SI + sw128_chunk(128, v, 8 * hh + c8)) =
+          make_uint4(pack_h2(Sv[8 * c8], Sv[8 * c8 + 1]), pack_h2(Sv[8 * c8 + 2], Sv[8 * c8 + 3]),
+                     pack_h2(Sv[8 * c8 + 4], Sv[8 * c8 + 5]), pack_h2(Sv[8 * c8 + 6], Sv[8 * c8 + 7]));
+    fence_proxy_async_smem();
+  };
+  write_simg();
+  tc_fence_before();
+  __syncthreads();
+
+  for (int ci = 0; ci < n_chunks; ++ci) {
+    const int buf = ci & 1, s = s0 + ci;
+    if (tid == 0 && ci + 1 < n_chunks) issue_loads(ci + 1);
+    if (!cta_wait(&bar_ld[buf], (uint32_t)((ci >> 1) & 1), A.status)) goto done;
+    if (tid == 0) {
+      tc_fence_after();
+      umma_tile(tmem, smem_u32(SI), 128, smem_u32(sm + kSOffWQ + buf * 32768), 128, 128, umma_idesc_f16(128, 128),
+                false);
+      umma_commit(bar_mma);
+    }
+    const float gC = __ldg(W.gc + (size_t)s * A.nv + h);
+    if (!cta_wait(bar_mma, 0, A.status)) goto done;
+    tc_fence_after();
+    if (hh == 0) {
+      // U' = U - W S  -> fp16 image row v
+      const float4 *urow = reinterpret_cast<const float4 *>(W.ut + ((size_t)s * A.nv + h) * kRowF + (size_t)v * CH);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float x[32];
+        tmem_ld32(tmem_at(tmem, q, 32 * half), x);
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          const float4 u0 = __ldg(urow + 8 * half + 2 * c4), u1 = __ldg(urow + 8 * half + 2 * c4 + 1);
+          const float *xx = x + 8 * c4;
+          *reinterpret_cast<uint4 *>(UP + sw128_chunk(128, v, 4 * half + c4)) =
+              make_uint4(pack_h2(u0.x - xx[0], u0.y - xx[1]), pack_h2(u0.z - xx[2], u0.w - xx[3]),
+                         pack_h2(u1.x - xx[4], u1.y - xx[5]), pack_h2(u1.z - xx[6], u1.w - xx[7]));
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_sync(1, 128);
+      if (tid == 0) {
+        tc_fence_after();
+        umma_tile(tmem + 128, smem_u32(UP), 128, smem_u32(sm + kSOffKT + buf * 16384), 128, 64,
+                  umma_idesc_f16(128, 128), false);
+        umma_commit(bar_mma);
+      }
+    }
+    {
+      // O = Q' S + O_local for tokens 32hh .. 32hh+31 (warp group hh), gated
+      // RMSNorm over v per token (the group's 4 warps hold all 128 v), then the
+      // group's 32 output rows leave through the TMA
+      const int bar_id = 1 + hh, issuer = 128 * hh;
+      const float4 *orow =
+          reinterpret_cast<const float4 *>(W.ot + ((size_t)s * A.nv + h) * kRowF + (size_t)v * CH) + 8 * hh;
+      float o[32];
+      tmem_ld32(tmem_at(tmem, q, 64 + 32 * hh), o);
+#pragma unroll
+      for (int c4 = 0; c4 < 8; ++c4) {
+        const float4 ol = __ldg(orow + c4);
+        o[4 * c4] += ol.x;
+        o[4 * c4 + 1] += ol.y;
+        o[4 * c4 + 2] += ol.z;
+        o[4 * c4 + 3] += ol.w;
+      }
+      // sum over the warp's 32 rows of o^2 for each of the 32 tokens: after the
+      // transposing butterfly lane l holds token l's partial
+      float sq[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) sq[e] = o[e] * o[e];
+#pragma unroll
+      for (int w = 16; w >= 1; w >>= 1) {
+        const bool up = (lane & w) != 0;
+#pragma unroll
+        for (int e = 0; e < w; ++e) {
+          const float send = up ? sq[e] : sq[e + w];
+          const float keep = up ? sq[e + w] : sq[e];
+          sq[e] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+        }
+      }
+      red[q * 64 + 32 * hh + lane] = sq[0];
+      if (tid == issuer) bulk_wait_read_all();  // this group's previous output rows have left shared memory
+      named_sync(bar_id, 128);
+      if (q == 0) {
+        const int t = 32 * hh + lane;
+        const float ss = red[t] + red[64 + t] + red[128 + t] + red[192 + t];
+        rstd[t] = rsqrtf(ss / (float)HD + A.rms_eps);
+      }
+      named_sync(bar_id, 128);
+      const __half *gzs = reinterpret_cast<const __half *>(sm + kSOffZ + buf * 16384);
+      bf16 *os = reinterpret_cast<bf16 *>(sm + kSOffO);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int i = 32 * hh + e;
+        os[i * HD + v] = __float2bfloat16_rn(o[e] * rstd[i] * __half2float(gzs[i * HD + v]));
+      }
+      fence_proxy_async_smem();
+      named_sync(bar_id, 128);
+      if (tid == issuer) {
+        const int nout = min(32, Lr - ci * CH - 32 * hh);  // real tokens of this half
+        if (nout == 32) {
+          tma_store_2d(&omap, h * HD, start + ci * CH + 32 * hh, os + 32 * hh * HD);
+        } else {
+          bf16 *dst = A.out + ((size_t)(start + ci * CH + 32 * hh) * A.nv + h) * HD;
+          for (int i = 0; i < nout; ++i) bulk_s2g(dst + (size_t)i * A.nv * HD, os + (32 * hh + i) * HD, HD * 2);
+        }
+        bulk_commit();
+      }
+    }
+    if (!cta_wait(bar_mma, 1, A.status)) goto done;
+    tc_fence_after();
+    // S = gamma_C S + dS
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      float d[32];
+      tmem_ld32(tmem_at(tmem, q, 128 + 64 * hh + 32 * half), d);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) Sv[32 * half + e] = fmaf(gC, Sv[32 * half + e], d[e]);
+    }
+    write_simg();
+    tc_fence_before();
+    __syncthreads();
+  }
+  if (tid == 0 || tid == 128) bulk_wait_all();
+#pragma unroll
+  for (int k = 0; k < 64; ++k) gS[(size_t)(64 * hh + k) * HD + v] = Sv[k];
+  for (int t = Lr + tid / 16; t < len; t += 16) {
+    if ((tid & 15) < HD / 8)
+      reinterpret_cast<uint4 *>(A.out + ((size_t)(start + t) * A.nv + h) * HD)[tid & 15] = make_uint4(0u, 0u, 0u, 0u);
+  }
+done:
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+// Tensor map of a bf16 [rows][cols] row-major tensor with [32][128] boxes.
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                 const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+gdn_status encode_rows_map(CUtensorMap *map, const void *base, int rows, int cols) {
+  static EncodeTiled encode = nullptr;
+  if (!encode) {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return fail(GDN_ERR_CUDA, "prefill: cuTensorMapEncodeTiled is unavailable");
+    encode = reinterpret_cast<EncodeTiled>(fn);
+  }
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)HD, (cuuint32_t)(CH / 2)};
+  const cuuint32_t estr[2] = {1, 1};
+  if (encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return fail(GDN_ERR_CUDA, "prefill: cannot encode a tensor map");
+  return GDN_OK;
+}
+
+}  // namespace tc
+
+size_t prefill_tc_workspace_bytes(int B, int T, int nk, int nv, bool packed) {
+  return tc::ws_bytes(B, T, nk, nv, packed);
+}
+
+gdn_status launch_prefill_tc(const LayerArgs &A, void *ws, cudaStream_t stream) {
+  const bool packed = A.cu_seqlens != nullptr;
+  const int Ttot = packed ? A.T : A.B * A.T;
+  const int S = (int)tc::slots_total(A.B, A.T, packed);
+  tc::Rows R{A.B, A.T, packed ? 0 : (A.T + tc::CH - 1) / tc::CH, A.cu_seqlens};
+  tc::Ws W = tc::carve(ws, A.B, A.T, A.nk, A.nv, packed);
+  const DeviceInfo &dev = device_info();
+  static bool attr_set[kMaxDevices] = {};
+  if (!attr_set[dev.id]) {
+    if (cudaFuncSetAttribute(tc::chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kChunkSmem) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(tc::state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kStateSmem) !=
+            cudaSuccess)
+      return fail(GDN_ERR_CUDA, "prefill: cannot reserve shared memory");
+    attr_set[dev.id] = true;
+  }
+  tc::front_kernel<<<dim3(S, 2 * A.nk + 2 * A.nv), 256, 0, stream>>>(A, R, Ttot, W);
+  if (gdn_status st = check_launch("prefill front")) return st;
+  tc::chunk_kernel<<<dim3(S, A.nv), 256, tc::kChunkSmem, stream>>>(A, R, Ttot, W);
+  if (gdn_status st = check_launch("prefill chunk")) return st;
+  CUtensorMap omap;
+  if (gdn_status st = tc::encode_rows_map(&omap, A.out, Ttot, A.nv * tc::HD)) return st;
+  tc::state_kernel<<<A.B * A.nv, 256, tc::kStateSmem, stream>>>(A, R, Ttot, W, omap);
+  return check_launch("prefill state");
+}
+
+}  // namespace gdn

@@ -40,6 +40,14 @@ __device__ __forceinline__ float conv4_silu(float w0, float w1, float w2, float 
   return silu_f(acc);
 }
 
+// Fast variants for the chunked prefill (no bit-exactness constraint there):
+// __expf and __fdividef, relative error ~2^-21.
+__device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
+__device__ __forceinline__ float conv4_silu_fast(float w0, float w1, float w2, float w3, float x0, float x1,
+                                                 float x2, float x3) {
+  return silu_fast(fmaf(w3, x3, fmaf(w2, x2, fmaf(w1, x1, w0 * x0))));
+}
+
 // L2-normalise a D-vector in shared memory in place and multiply by `scale`
 // (use_qk_l2norm_in_kernel: x / sqrt(sum x^2 + eps)). Called by one whole warp.
 template <int D>
