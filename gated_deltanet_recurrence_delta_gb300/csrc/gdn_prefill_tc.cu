@@ -172,7 +172,7 @@ __device__ __forceinline__ void umma_tile_split(uint32_t tmem_d, uint32_t a_hi, 
 
 // ------------------------------------------------------------ front end
 
-__global__ void __launch_bounds__(256) front_kernel(LayerArgs A, Rows R, int Ttot, Ws W) {
+__global__ void __launch_bounds__(256, 3) front_kernel(LayerArgs A, Rows R, int Ttot, Ws W) {
   __shared__ __align__(16) float Y[CH][HD];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int s = blockIdx.x, gi = blockIdx.y, kd = A.nk * HD;
@@ -297,7 +297,9 @@ constexpr int kOffKQH = 0;       // [2 kb][128 rows][128 B]: K rows 0-63 | Q row
 constexpr int kOffKQL = 32768;   // the same, lo parts
 constexpr int kOffB2H = 65536;   // [256 rows][128 B]: (beta gamma K)^T rows 0-127 | (beta V)^T rows 128-255 (hi)
 constexpr int kOffB2L = 98304;   // the same, lo parts
-constexpr int kOffAF = 131072;   // fp32 [64][64]: A, then T in place; later the [T; R] image (hi)
+constexpr int kOffAF = 131072;   // fp32 [64][kLD]: A, then T in place; later the [T; R] image (hi)
+constexpr int kLD = 65;          // padded row stride: column-wise accesses hit distinct banks
+                                 // (the 256 bytes past 16 KiB overlap the [T; R] lo image, unused until then)
 constexpr int kOffTRL = 147456;  // [T; R] image (lo)
 constexpr int kOffPTH = 163840;  // [128 rows][128 B]: P rows 0-63 | T^T rows 64-127 (hi)
 constexpr int kOffPTL = 180224;  // the same, lo parts
@@ -460,7 +462,7 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
 #pragma unroll
       for (int jj = 0; jj < 32; ++jj) {
         const int j = 32 * hh + jj;
-        AF[i * 64 + j] = j < i ? bi * v[jj] * __expf(Gi - sG[j]) : 0.0f;
+        AF[i * kLD + j] = j < i ? bi * v[jj] * __expf(Gi - sG[j]) : 0.0f;
       }
     } else {
       const int i = row - CH;
@@ -484,20 +486,20 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
     float x[16];
     const int bb = tid >> 4, cc = tid & 15;
     if (tid < 64) {
-      const float *Ab = AF + (16 * bb) * 64 + 16 * bb;
+      const float *Ab = AF + (16 * bb) * kLD + 16 * bb;
 #pragma unroll
       for (int rr = 0; rr < 16; ++rr) {
         float acc = rr == cc ? 1.0f : 0.0f;
 #pragma unroll
-        for (int l = 0; l < rr; ++l) acc = fmaf(-Ab[rr * 64 + l], x[l], acc);
+        for (int l = 0; l < rr; ++l) acc = fmaf(-Ab[rr * kLD + l], x[l], acc);
         x[rr] = acc;
       }
     }
     __syncthreads();
     if (tid < 64) {
-      float *Tb = AF + (16 * bb) * 64 + 16 * bb;
+      float *Tb = AF + (16 * bb) * kLD + 16 * bb;
 #pragma unroll
-      for (int rr = 0; rr < 16; ++rr) Tb[rr * 64 + cc] = x[rr];
+      for (int rr = 0; rr < 16; ++rr) Tb[rr * kLD + cc] = x[rr];
     }
     __syncthreads();
     for (int b = 2; b >= 0; --b) {
@@ -506,10 +508,10 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
         const int a = b + 1 + (e >> 8), rr = (e >> 4) & 15, m = e & 15;
         float acc = 0.0f;
         for (int cb = b + 1; cb <= a; ++cb) {
-          const float *Tac = AF + (16 * a + rr) * 64 + 16 * cb;
-          const float *Acb = AF + (16 * cb) * 64 + 16 * b + m;
+          const float *Tac = AF + (16 * a + rr) * kLD + 16 * cb;
+          const float *Acb = AF + (16 * cb) * kLD + 16 * b + m;
 #pragma unroll
-          for (int k = 0; k < 16; ++k) acc = fmaf(Tac[k], Acb[k * 64], acc);
+          for (int k = 0; k < 16; ++k) acc = fmaf(Tac[k], Acb[k * kLD], acc);
         }
         SCR[e] = acc;
       }
@@ -518,16 +520,16 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
       for (int e = tid, n = 0; e < nrows * 256; e += 256, ++n) {
         const int rr = (e >> 4) & 15, m = e & 15;
         const float *M = SCR + (e >> 8) * 256 + rr * 16;
-        const float *Tbb = AF + (16 * b) * 64 + 16 * b + m;
+        const float *Tbb = AF + (16 * b) * kLD + 16 * b + m;
         float acc = 0.0f;
 #pragma unroll
-        for (int k = 0; k < 16; ++k) acc = fmaf(M[k], Tbb[k * 64], acc);
+        for (int k = 0; k < 16; ++k) acc = fmaf(M[k], Tbb[k * kLD], acc);
         outv[n] = -acc;
       }
       __syncthreads();
       for (int e = tid, n = 0; e < nrows * 256; e += 256, ++n) {
         const int a = b + 1 + (e >> 8), rr = (e >> 4) & 15, m = e & 15;
-        AF[(16 * a + rr) * 64 + 16 * b + m] = outv[n];
+        AF[(16 * a + rr) * kLD + 16 * b + m] = outv[n];
       }
       __syncthreads();
     }
@@ -536,7 +538,7 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
     const int i = tid >> 2, q4 = tid & 3;
     float t16[16];
 #pragma unroll
-    for (int k = 0; k < 16; ++k) t16[k] = AF[i * 64 + 16 * q4 + k];
+    for (int k = 0; k < 16; ++k) t16[k] = AF[i * kLD + 16 * q4 + k];
     __syncthreads();
 #pragma unroll
     for (int c2 = 0; c2 < 2; ++c2) store_split8(TRH, TRL, sw128_chunk(128, i, 2 * q4 + c2), t16 + 8 * c2);
@@ -627,7 +629,7 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
   if (tid == 0) {
     bulk_s2g(W.wq + ((size_t)s * A.nv + h) * kWQ, KQH, 32768);
     bulk_commit();
-    bulk_wait_all();
+    bulk_wait_read_all();  // shared memory may be released; the writes land before the grid completes
   }
 done:
   tc_fence_before();
