@@ -24,7 +24,8 @@ struct StateLayout {
   static_assert(TPR <= 32 && NG * TPR == NT && RPT * NG == D, "unsupported head size");
 };
 
-__device__ __forceinline__ float sigmoid_f(float x) { return __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-x))); }
+// __frcp_rn is the correctly rounded 1/x, the same value as __fdiv_rn(1, x).
+__device__ __forceinline__ float sigmoid_f(float x) { return __frcp_rn(__fadd_rn(1.0f, expf(-x))); }
 __device__ __forceinline__ float silu_f(float x) { return __fmul_rn(x, sigmoid_f(x)); }
 // softplus(x) = log(1 + e^x); above 20 the correction is below 2.1e-9 and x is returned.
 __device__ __forceinline__ float softplus_f(float x) { return x > 20.0f ? x : log1pf(expf(x)); }
@@ -175,7 +176,8 @@ __device__ __forceinline__ void rmsnorm_store_smem(float4 o, int lane, const flo
     ss = __fmaf_rn(o.w, o.w, ss);
   }
   ss = warp_sum_bcast(ss);
-  const float r = __fdiv_rn(1.0f, sqrtf(__fadd_rn(__fdiv_rn(ss, (float)D), eps)));
+  // D is a power of two: ss * (1/D) is exactly ss / D
+  const float r = __frcp_rn(sqrtf(__fadd_rn(__fmul_rn(ss, 1.0f / D), eps)));
   if (lane < L::TPR) {
     const int c = 4 * lane;
     const float ov[4] = {o.x, o.y, o.z, o.w};
