@@ -131,6 +131,9 @@ class ClockSampler:
         return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+SPIN_HZ = 2.1e9  # cycles per second assumed when sizing the spin kernel (SM clock up to 2070 MHz)
+
+
 class Timer:
     """CUDA events on the launching stream; per-launch pairs for one kernel."""
 
@@ -181,14 +184,23 @@ def max_over_ranks(x: float, world: int) -> float:
 def timed(world, steps, warmup, step_fn, kernel_fn=None):
     """Run warmup steps, then `steps` timed steps bracketed by a barrier and a
     synchronize on both sides; returns (ms per step max over ranks, mean ms of
-    the dominant kernel per launch)."""
+    the dominant kernel per launch).
+
+    The device is kept busy by a bounded spin kernel (torch.cuda._sleep)
+    queued just before the start event, long enough to cover the host's
+    enqueue of all timed steps (measured on the warm-up steps): the start event
+    is then reached only once every step is queued behind it, so the events
+    time the device work and not the Python launch overhead between launches."""
+    t0 = time.perf_counter()
     for i in range(warmup):
         step_fn(i, None)
+    host_s = (time.perf_counter() - t0) / max(1, warmup)
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
     kt = Timer()
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(int(min(0.5, 2.0 * host_s * (steps + 1) + 2e-3) * SPIN_HZ))
     s.record()
     for i in range(steps):
         step_fn(warmup + i, kt)
@@ -343,7 +355,7 @@ def phase_prefill(gdn, world, steps, warmup, peak_tf):
     ms, kms = timed(world, steps, warmup, step)
     flops = prefill_flops_per_token(s) * T
     res = {"tokens_per_s": T * world / (ms * 1e-3), "ms_per_step": ms, "tokens_per_step": T,
-           "ms_per_512_call": ms / (T // call), "launches_per_step": 2 * (T // call),
+           "ms_per_512_call": ms / (T // call), "launches_per_step": 3 * (T // call),
            "roofline": {"bound": "tensor", "achieved": flops / (kms * 1e-3) / 1e12, "peak": peak_tf,
                         "unit": "TFLOP/s", "frac": flops / (kms * 1e-3) / 1e12 / peak_tf,
                         "traffic": None, "algorithmic_flops_per_token": prefill_flops_per_token(s)}}
@@ -377,7 +389,7 @@ def phase_varlen(gdn, world, steps, warmup, peak_tf, n_layers=24):
     flops = prefill_flops_per_token(s) * real * n_layers
     res = {"real_tokens_per_s": real * world / (ms * 1e-3),
            "layer_tokens_per_s": real * n_layers * world / (ms * 1e-3), "ms_per_step": ms,
-           "real_tokens": real, "padded_tokens": padded, "layers": n_layers, "launches_per_step": 2 * n_layers,
+           "real_tokens": real, "padded_tokens": padded, "layers": n_layers, "launches_per_step": 3 * n_layers,
            "roofline": {"bound": "tensor", "achieved": flops / (kms * 1e-3) / 1e12, "peak": peak_tf,
                         "unit": "TFLOP/s", "frac": flops / (kms * 1e-3) / 1e12 / peak_tf, "traffic": None}}
     del layers, ws
