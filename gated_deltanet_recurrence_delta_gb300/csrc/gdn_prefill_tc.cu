@@ -13,7 +13,7 @@
 //   S_C = gamma_C S_0 + (K * exp(G_C - G))^T U'
 // (S on the stored transpose St[k][v]). exp(-G) is never formed.
 //
-// Kernels (one call = front -> chunk -> state, stream ordered):
+// Kernels (one call = front -> chunk -> state -> output, stream ordered):
 //   front  conv + SiLU + q/k L2 norm per (chunk slot, head), written as split
 //          fp16 tiles (128B-swizzled K-major images): K and Q as [token][d],
 //          K^T and V^T as [d][token].
@@ -22,13 +22,16 @@
 //          blocked fp32 triangular inverse; R = P T (tcgen05); then one
 //          tcgen05 product [T; R] [beta gamma K | beta V] (M=128,N=256,K=64)
 //          yields W, U, P W (-> Q') and P U (= O_local). Writes W|Q' as one
-//          swizzled image, (K*exp(G_C-G))^T as another, U^T and O_local^T fp32.
+//          swizzled image, (K*exp(G_C-G))^T as another, U and O_local fp32.
 //   state  per (row, value head), sequential over its chunks with the state
 //          in registers (fp32) and an fp16 copy in shared memory:
-//          X = S_math [W;Q']^T (tcgen05 M=128,N=128,K=128) ->
-//          U' = U - X_W, O = X_Q + O_local (gated RMSNorm epilogue, bf16 out)
+//          X = S_math W^T (tcgen05 M=128,N=64,K=128) -> U' = U - X,
 //          dS = U'^T-image x (K~^T)-image (tcgen05 M=128,N=128,K=64) ->
-//          S = gamma_C S + dS.
+//          S = gamma_C S + dS; the fp16 state image at every chunk start
+//          is copied out.
+//   output per (chunk slot, value head), all chunks in parallel:
+//          O = Q' S + O_local from that image (tcgen05 M=128,N=64,K=128),
+//          gated RMSNorm epilogue, bf16 rows out through the TMA.
 // Operand tiles move between HBM and shared memory with bulk copies (TMA).
 // Precision: accumulators are fp32. The chunk kernel runs every product in
 // split fp16 (x = hi + lo, hi = fp16(x), lo = fp16(x - hi); a*b ~ hi*hi +
@@ -55,14 +58,16 @@ struct Ws {
   __half *vtimg;        // [S][nv][2 hi|lo][128][64]    V^T as a swizzled [dv][token] image
   __half *wq;           // [S][nv][2][128][64]  W (rows 0-63) | Q' (rows 64-127) image (32 KiB)
   __half *kt;           // [S][nv][128][64]     (K * exp(G_C - G))^T image (16 KiB)
-  float *ut, *ot;       // [S][nv][128][64]     U^T and O_local^T (32 KiB each)
+  float *ut, *ot;       // [S][nv][64][128]     U and O_local, token-major fp32 (32 KiB each)
   __half *gz;           // [S][nv][64][128]     norm_w * silu(z), row-major (16 KiB)
   float *gc;            // [S][nv]              gamma_C
+  __half *simg;         // [S][nv][2][128][64]  fp16 image of the state at the chunk's start (32 KiB)
+  int *lr;              // [B]                  real length of each row, -1 = row rejected
 };
 
 constexpr size_t kImg = 64 * 128;    // halves in a 64x128 image
 constexpr size_t kWQ = 128 * 128;    // halves in the W|Q' image
-constexpr size_t kRowF = 128 * 64;   // floats in U^T / O_local^T
+constexpr size_t kRowF = 128 * 64;   // floats in U / O_local
 
 size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -73,7 +78,8 @@ size_t slots_total(int B, int T, bool packed) {
 size_t ws_bytes(int B, int T, int nk, int nv, bool packed) {
   const size_t S = slots_total(B, T, packed);
   return 3 * a256(S * nk * kImg * 4) + a256(S * nv * kImg * 4) + a256(S * nv * kWQ * 2) +
-         a256(S * nv * kImg * 2) + 2 * a256(S * nv * kRowF * 4) + a256(S * nv * 4) + a256(S * nv * kImg * 2);
+         a256(S * nv * kImg * 2) + 2 * a256(S * nv * kRowF * 4) + a256(S * nv * 4) + a256(S * nv * kImg * 2) +
+         a256(S * nv * kWQ * 2) + a256((size_t)B * 4);
 }
 
 Ws carve(void *ws, int B, int T, int nk, int nv, bool packed) {
@@ -99,6 +105,10 @@ Ws carve(void *ws, int B, int T, int nk, int nv, bool packed) {
   w.gc = reinterpret_cast<float *>(p);
   p += a256(S * nv * 4);
   w.gz = reinterpret_cast<__half *>(p);
+  p += a256(S * nv * kImg * 2);
+  w.simg = reinterpret_cast<__half *>(p);
+  p += a256(S * nv * kWQ * 2);
+  w.lr = reinterpret_cast<int *>(p);
   return w;
 }
 
@@ -616,10 +626,10 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
           *dst = make_uint4(pack_h2(y[0], y[1]), pack_h2(y[2], y[3]), pack_h2(y[4], y[5]), pack_h2(y[6], y[7]));
         }
       } else {
-        // U or O_local, stored transposed: [v][i]
-        float *dst = upper ? ot : ut;
+        // U or O_local row i (token-major)
+        float4 *dst = reinterpret_cast<float4 *>((upper ? ot : ut) + (size_t)i * HD + 32 * cb);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) dst[(32 * cb + e) * CH + i] = v[e];
+        for (int c4 = 0; c4 < 8; ++c4) dst[c4] = make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
       }
     }
     if (tid == 0) W.gc[(size_t)s * A.nv + h] = sgam[CH - 1];
@@ -638,44 +648,47 @@ done:
 }
 
 // ------------------------------------------------------------ state pass
+//
+// The sequential part only: per (row, value head), over its chunks,
+//   X = S_math W^T (tcgen05 M=128 v, N=64 tokens, K=128) -> U' = U - X,
+//   dS = U'^T-image x (K~^T)-image (M=128, N=128, K=64) -> S = gamma_C S + dS,
+// with the state in registers (fp32) and an fp16 copy in shared memory. The
+// fp16 image of the state at the start of every chunk is copied out (bulk
+// store) for the output kernel, which does O = Q' S + O_local off this path.
 
-constexpr int kSOffS = 0;         // S_math fp16 image [2 kb][128 rows][128 B]
-constexpr int kSOffWQ = 32768;    // 2 x W|Q' image (32 KiB each)
-constexpr int kSOffKT = 98304;    // 2 x K~^T image (16 KiB each)
-constexpr int kSOffUP = 131072;   // U'^T image [128 rows][128 B]
-constexpr int kSOffZ = 147456;    // 2 x output gate of the chunk, fp16 [64][128] (16 KiB each)
-constexpr int kSOffO = 180224;    // output rows of the chunk, bf16 [64][128]
-constexpr int kSOffRed = 196608;  // fp32 [4][64] RMS partials, [64] rstd, [128] norm weight
-constexpr int kSOffBar = kSOffRed + 4 * 64 * 4 + 64 * 4 + 128 * 4;
+constexpr int kSOffS = 0;         // S_math fp16 image [2 kb][128 rows][128 B] (32 KiB)
+constexpr int kSOffW = 32768;     // 2 x W image [2 kb][64 rows][128 B] (16 KiB each)
+constexpr int kSOffKT = 65536;    // 2 x K~^T image [128 rows][128 B] (16 KiB each)
+constexpr int kSOffUT = 98304;    // 2 x U fp32 [64 tokens][128 v] (32 KiB each)
+constexpr int kSOffUP = 163840;   // U'^T image [128 rows][128 B] (16 KiB)
+constexpr int kSOffBar = 180224;  // barriers, TMEM base
 constexpr int kStateSmem = kSOffBar + 64 + 1024;
 
 __device__ __forceinline__ void named_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-// omap: out viewed as [Ttot][nv*dv] bf16, box [32 tokens][128 values].
-__global__ void __launch_bounds__(256, 1) state_kernel(LayerArgs A, Rows R, int Ttot, Ws W,
-                                                       const __grid_constant__ CUtensorMap omap) {
+__global__ void __launch_bounds__(256, 1) state_kernel(LayerArgs A, Rows R, int Ttot, Ws W) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   unsigned char *sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   unsigned char *SI = sm + kSOffS;
   unsigned char *UP = sm + kSOffUP;
-  float *red = reinterpret_cast<float *>(sm + kSOffRed);  // [4][64]
-  float *rstd = red + 256;                                // [64]
-  float *fw = rstd + 64;                                  // [128]
   uint64_t *bar_ld = reinterpret_cast<uint64_t *>(sm + kSOffBar);  // [2]
   uint64_t *bar_mma = bar_ld + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_mma + 1);
   __shared__ int s_min_zero, s_max_one, s_bad;
 
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.x / A.nv, h = blockIdx.x % A.nv, kh = h / A.G;
   const int kd = A.nk * HD, C = A.C;
   const int start = R.start(b), len = R.len(b);
   const int slot = row_slot(A, b);
   if (slot < 0 || start < 0 || len < 0 || start + len > Ttot) {
-    if (tid == 0) set_status(A.status, GDN_ERR_INDEX);
+    if (tid == 0) {
+      set_status(A.status, GDN_ERR_INDEX);
+      if (h == 0) W.lr[b] = -1;
+    }
     return;
   }
   // real length: the mask row must be ones then zeros
@@ -695,9 +708,13 @@ __global__ void __launch_bounds__(256, 1) state_kernel(LayerArgs A, Rows R, int 
   __syncthreads();
   const int Lr = s_min_zero;
   if (s_bad || s_max_one >= Lr) {
-    if (tid == 0) set_status(A.status, GDN_ERR_MASK);
+    if (tid == 0) {
+      set_status(A.status, GDN_ERR_MASK);
+      if (h == 0) W.lr[b] = -1;
+    }
     return;
   }
+  if (tid == 0 && h == 0) W.lr[b] = Lr;  // read by the output kernel
   // conv tail: xin rows Lr .. Lr+2 (old rows when Lr < 3), own channels only
   {
     bf16 *cs = A.conv_state + (size_t)slot * KC * C;
@@ -718,7 +735,6 @@ __global__ void __launch_bounds__(256, 1) state_kernel(LayerArgs A, Rows R, int 
       for (int rr = 0; rr < KC; ++rr) cs[(size_t)rr * C + ch] = nv3[rr];
     }
   }
-  for (int cc = tid; cc < HD; cc += 256) fw[cc] = ldbf(A.norm_w + cc);
 
   const int n_chunks = (len + CH - 1) / CH;
   const int s0 = R.slot0(b);
@@ -734,17 +750,21 @@ __global__ void __launch_bounds__(256, 1) state_kernel(LayerArgs A, Rows R, int 
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // chunk ci's operand tiles and its output gate norm_w * silu(z)
+  // chunk ci's W rows (rows 0-63 of each column block of the W|Q' image),
+  // (K exp(G_C - G))^T and U
   auto issue_loads = [&](int ci) {  // thread 0
     const int buf = ci & 1, s = s0 + ci;
-    mbar_arrive_expect_tx(&bar_ld[buf], 32768 + 16384 + 16384);
-    bulk_g2s(sm + kSOffWQ + buf * 32768, W.wq + ((size_t)s * A.nv + h) * kWQ, 32768, &bar_ld[buf]);
+    const unsigned char *wq = reinterpret_cast<const unsigned char *>(W.wq + ((size_t)s * A.nv + h) * kWQ);
+    unsigned char *wdst = sm + kSOffW + buf * 16384;
+    mbar_arrive_expect_tx(&bar_ld[buf], 16384 + 16384 + 32768);
+    bulk_g2s(wdst, wq, 8192, &bar_ld[buf]);
+    bulk_g2s(wdst + 8192, wq + 16384, 8192, &bar_ld[buf]);
     bulk_g2s(sm + kSOffKT + buf * 16384, W.kt + ((size_t)s * A.nv + h) * kImg, 16384, &bar_ld[buf]);
-    bulk_g2s(sm + kSOffZ + buf * 16384, W.gz + ((size_t)s * A.nv + h) * kImg, 16384, &bar_ld[buf]);
+    bulk_g2s(sm + kSOffUT + buf * 32768, W.ut + ((size_t)s * A.nv + h) * kRowF, 32768, &bar_ld[buf]);
   };
   if (tid == 0 && n_chunks > 0) issue_loads(0);
 
-  // thread <-> (value row v = TMEM lane, key half hh)
+  // thread <-> (value row v = TMEM lane, key half / token half hh)
   const int q = warp & 3, hh = warp >> 2, v = 32 * q + lane;
   float Sv[64];
   float *gS = A.state + ((size_t)slot * A.nv + h) * HD * HD;
@@ -761,106 +781,47 @@ __global__ void __launch_bounds__(256, 1) state_kernel(LayerArgs A, Rows R, int 
   write_simg();
   tc_fence_before();
   __syncthreads();
+  if (tid == 0 && n_chunks > 0) {  // the state image at the start of chunk 0
+    bulk_s2g(W.simg + ((size_t)s0 * A.nv + h) * kWQ, SI, 32768);
+    bulk_commit();
+  }
 
   for (int ci = 0; ci < n_chunks; ++ci) {
     const int buf = ci & 1, s = s0 + ci;
     if (tid == 0 && ci + 1 < n_chunks) issue_loads(ci + 1);
+    const float gC = __ldg(W.gc + (size_t)s * A.nv + h);
     if (!cta_wait(&bar_ld[buf], (uint32_t)((ci >> 1) & 1), A.status)) goto done;
     if (tid == 0) {
       tc_fence_after();
-      umma_tile(tmem, smem_u32(SI), 128, smem_u32(sm + kSOffWQ + buf * 32768), 128, 128, umma_idesc_f16(128, 128),
+      umma_tile(tmem, smem_u32(SI), 128, smem_u32(sm + kSOffW + buf * 16384), 64, 128, umma_idesc_f16(128, 64),
                 false);
       umma_commit(bar_mma);
     }
-    const float gC = __ldg(W.gc + (size_t)s * A.nv + h);
     if (!cta_wait(bar_mma, 0, A.status)) goto done;
     tc_fence_after();
-    if (hh == 0) {
-      // U' = U - W S  -> fp16 image row v
-      const float4 *urow = reinterpret_cast<const float4 *>(W.ut + ((size_t)s * A.nv + h) * kRowF + (size_t)v * CH);
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        float x[32];
-        tmem_ld32(tmem_at(tmem, q, 32 * half), x);
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          const float4 u0 = __ldg(urow + 8 * half + 2 * c4), u1 = __ldg(urow + 8 * half + 2 * c4 + 1);
-          const float *xx = x + 8 * c4;
-          *reinterpret_cast<uint4 *>(UP + sw128_chunk(128, v, 4 * half + c4)) =
-              make_uint4(pack_h2(u0.x - xx[0], u0.y - xx[1]), pack_h2(u0.z - xx[2], u0.w - xx[3]),
-                         pack_h2(u1.x - xx[4], u1.y - xx[5]), pack_h2(u1.z - xx[6], u1.w - xx[7]));
-        }
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      named_sync(1, 128);
-      if (tid == 0) {
-        tc_fence_after();
-        umma_tile(tmem + 128, smem_u32(UP), 128, smem_u32(sm + kSOffKT + buf * 16384), 128, 64,
-                  umma_idesc_f16(128, 128), false);
-        umma_commit(bar_mma);
-      }
-    }
     {
-      // O = Q' S + O_local for tokens 32hh .. 32hh+31 (warp group hh), gated
-      // RMSNorm over v per token (the group's 4 warps hold all 128 v), then the
-      // group's 32 output rows leave through the TMA
-      const int bar_id = 1 + hh, issuer = 128 * hh;
-      const float4 *orow =
-          reinterpret_cast<const float4 *>(W.ot + ((size_t)s * A.nv + h) * kRowF + (size_t)v * CH) + 8 * hh;
-      float o[32];
-      tmem_ld32(tmem_at(tmem, q, 64 + 32 * hh), o);
+      // U' = U - W S for tokens 32hh .. 32hh+31 of value row v -> fp16 image row v
+      const float *ut = reinterpret_cast<const float *>(sm + kSOffUT + buf * 32768) + (size_t)(32 * hh) * HD + v;
+      float x[32];
+      tmem_ld32(tmem_at(tmem, q, 32 * hh), x);
 #pragma unroll
-      for (int c4 = 0; c4 < 8; ++c4) {
-        const float4 ol = __ldg(orow + c4);
-        o[4 * c4] += ol.x;
-        o[4 * c4 + 1] += ol.y;
-        o[4 * c4 + 2] += ol.z;
-        o[4 * c4 + 3] += ol.w;
-      }
-      // sum over the warp's 32 rows of o^2 for each of the 32 tokens: after the
-      // transposing butterfly lane l holds token l's partial
-      float sq[32];
+      for (int c4 = 0; c4 < 4; ++c4) {
+        float y[8];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) sq[e] = o[e] * o[e];
-#pragma unroll
-      for (int w = 16; w >= 1; w >>= 1) {
-        const bool up = (lane & w) != 0;
-#pragma unroll
-        for (int e = 0; e < w; ++e) {
-          const float send = up ? sq[e] : sq[e + w];
-          const float keep = up ? sq[e + w] : sq[e];
-          sq[e] = keep + __shfl_xor_sync(0xffffffffu, send, w);
-        }
-      }
-      red[q * 64 + 32 * hh + lane] = sq[0];
-      if (tid == issuer) bulk_wait_read_all();  // this group's previous output rows have left shared memory
-      named_sync(bar_id, 128);
-      if (q == 0) {
-        const int t = 32 * hh + lane;
-        const float ss = red[t] + red[64 + t] + red[128 + t] + red[192 + t];
-        rstd[t] = rsqrtf(ss / (float)HD + A.rms_eps);
-      }
-      named_sync(bar_id, 128);
-      const __half *gzs = reinterpret_cast<const __half *>(sm + kSOffZ + buf * 16384);
-      bf16 *os = reinterpret_cast<bf16 *>(sm + kSOffO);
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int i = 32 * hh + e;
-        os[i * HD + v] = __float2bfloat16_rn(o[e] * rstd[i] * __half2float(gzs[i * HD + v]));
+        for (int e = 0; e < 8; ++e) y[e] = ut[(size_t)(8 * c4 + e) * HD] - x[8 * c4 + e];
+        *reinterpret_cast<uint4 *>(UP + sw128_chunk(128, v, 4 * hh + c4)) =
+            make_uint4(pack_h2(y[0], y[1]), pack_h2(y[2], y[3]), pack_h2(y[4], y[5]), pack_h2(y[6], y[7]));
       }
       fence_proxy_async_smem();
-      named_sync(bar_id, 128);
-      if (tid == issuer) {
-        const int nout = min(32, Lr - ci * CH - 32 * hh);  // real tokens of this half
-        if (nout == 32) {
-          tma_store_2d(&omap, h * HD, start + ci * CH + 32 * hh, os + 32 * hh * HD);
-        } else {
-          bf16 *dst = A.out + ((size_t)(start + ci * CH + 32 * hh) * A.nv + h) * HD;
-          for (int i = 0; i < nout; ++i) bulk_s2g(dst + (size_t)i * A.nv * HD, os + (32 * hh + i) * HD, HD * 2);
-        }
-        bulk_commit();
-      }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+      umma_tile(tmem + 128, smem_u32(UP), 128, smem_u32(sm + kSOffKT + buf * 16384), 128, 64,
+                umma_idesc_f16(128, 128), false);
+      umma_commit(bar_mma);
+      bulk_wait_read_all();  // the copy of the previous state image has left shared memory
     }
     if (!cta_wait(bar_mma, 1, A.status)) goto done;
     tc_fence_after();
@@ -875,18 +836,148 @@ __global__ void __launch_bounds__(256, 1) state_kernel(LayerArgs A, Rows R, int 
     write_simg();
     tc_fence_before();
     __syncthreads();
+    if (tid == 0 && ci + 1 < n_chunks) {  // the state image at the start of chunk ci + 1
+      bulk_s2g(W.simg + ((size_t)(s + 1) * A.nv + h) * kWQ, SI, 32768);
+      bulk_commit();
+    }
   }
-  if (tid == 0 || tid == 128) bulk_wait_all();
+  if (tid == 0) bulk_wait_read_all();
 #pragma unroll
   for (int k = 0; k < 64; ++k) gS[(size_t)(64 * hh + k) * HD + v] = Sv[k];
-  for (int t = Lr + tid / 16; t < len; t += 16) {
-    if ((tid & 15) < HD / 8)
-      reinterpret_cast<uint4 *>(A.out + ((size_t)(start + t) * A.nv + h) * HD)[tid & 15] = make_uint4(0u, 0u, 0u, 0u);
+done:
+  if (tid == 0) bulk_wait_read_all();  // no bulk store may still read this CTA's shared memory
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+// ------------------------------------------------------------ outputs
+//
+// Per (chunk slot, value head), all chunks in parallel: O^T = S_img Q'^T
+// (tcgen05 M=128 v, N=64 tokens, K=128) from the state image at the chunk's
+// start, + O_local, then the gated RMSNorm (statecache.py, gated_rmsnorm)
+// and bf16 rows out through the TMA. Padded tokens of the row get zeros.
+
+constexpr int kOOffS = 0;         // state image (32 KiB)
+constexpr int kOOffQ = 32768;     // Q' image [2 kb][64 rows][128 B] (16 KiB)
+constexpr int kOOffOT = 49152;    // O_local fp32 [64 tokens][128 v] (32 KiB)
+constexpr int kOOffZ = 81920;     // norm_w * silu(z) fp16 [64][128], overwritten in place by the bf16 rows
+constexpr int kOOffRed = 98304;   // fp32 [4][64] RMS partials, [64] rstd
+constexpr int kOOffBar = kOOffRed + 4 * 64 * 4 + 64 * 4;
+constexpr int kOutSmem = kOOffBar + 64 + 1024;
+
+// omap: out viewed as [Ttot][nv*dv] bf16, box [32 tokens][128 values].
+__global__ void __launch_bounds__(256, 2) output_kernel(LayerArgs A, Rows R, int Ttot, Ws W,
+                                                        const __grid_constant__ CUtensorMap omap) {
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  unsigned char *sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  float *red = reinterpret_cast<float *>(sm + kOOffRed);  // [4][64]
+  float *rstd = red + 256;                                // [64]
+  uint64_t *bar_ld = reinterpret_cast<uint64_t *>(sm + kOOffBar);
+  uint64_t *bar_mma = bar_ld + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_mma + 1);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int s = blockIdx.x, h = blockIdx.y;
+  int r, c;
+  R.locate(s, Ttot, r, c);
+  if (r < 0) return;
+  const int Lr = W.lr[r];
+  if (Lr < 0) return;  // the row was rejected (its status is set)
+  const int start = R.start(r), len = R.len(r), t0 = c * CH;
+  const int ntok = min(CH, len - t0), nreal = max(0, min(CH, Lr - t0));
+  // padded tokens of this chunk: zeros
+  for (int e = nreal * 16 + tid; e < ntok * 16; e += 256)
+    reinterpret_cast<uint4 *>(A.out + ((size_t)(start + t0 + e / 16) * A.nv + h) * HD)[e % 16] =
+        make_uint4(0u, 0u, 0u, 0u);
+  if (nreal == 0) return;
+
+  if (tid == 0) {
+    mbar_init(bar_ld, 1);
+    mbar_init(bar_mma, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(tmem_slot, 64);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (tid == 0) {
+    const size_t sh = (size_t)s * A.nv + h;
+    const unsigned char *wq = reinterpret_cast<const unsigned char *>(W.wq + sh * kWQ);
+    mbar_arrive_expect_tx(bar_ld, 32768 + 16384 + 32768 + 16384);
+    bulk_g2s(sm + kOOffS, W.simg + sh * kWQ, 32768, bar_ld);
+    bulk_g2s(sm + kOOffQ, wq + 8192, 8192, bar_ld);           // Q' rows, column block 0
+    bulk_g2s(sm + kOOffQ + 8192, wq + 24576, 8192, bar_ld);   // Q' rows, column block 1
+    bulk_g2s(sm + kOOffOT, W.ot + sh * kRowF, 32768, bar_ld);
+    bulk_g2s(sm + kOOffZ, W.gz + sh * kImg, 16384, bar_ld);
+  }
+  if (!cta_wait(bar_ld, 0, A.status)) goto done;
+  if (tid == 0) {
+    tc_fence_after();
+    umma_tile(tmem, smem_u32(sm + kOOffS), 128, smem_u32(sm + kOOffQ), 64, 128, umma_idesc_f16(128, 64), false);
+    umma_commit(bar_mma);
+  }
+  if (!cta_wait(bar_mma, 0, A.status)) goto done;
+  tc_fence_after();
+  {
+    // value row v = TMEM lane, tokens 32hh .. 32hh+31 (warp group hh); the
+    // group's 4 warps hold all 128 v of its tokens
+    const int q = warp & 3, hh = warp >> 2, v = 32 * q + lane, bar_id = 1 + hh, issuer = 128 * hh;
+    float o[32];
+    tmem_ld32(tmem_at(tmem, q, 32 * hh), o);
+    const float *ol = reinterpret_cast<const float *>(sm + kOOffOT) + (size_t)(32 * hh) * HD + v;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) o[e] += ol[(size_t)e * HD];
+    // sum over the warp's 32 rows of o^2 for each of the 32 tokens: after the
+    // transposing butterfly lane l holds token l's partial
+    float sq[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) sq[e] = o[e] * o[e];
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1) {
+      const bool up = (lane & w) != 0;
+#pragma unroll
+      for (int e = 0; e < w; ++e) {
+        const float send = up ? sq[e] : sq[e + w];
+        const float keep = up ? sq[e + w] : sq[e];
+        sq[e] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+      }
+    }
+    red[q * 64 + 32 * hh + lane] = sq[0];
+    named_sync(bar_id, 128);
+    if (q == 0) {
+      const int t = 32 * hh + lane;
+      const float ss = red[t] + red[64 + t] + red[128 + t] + red[192 + t];
+      rstd[t] = rsqrtf(ss / (float)HD + A.rms_eps);
+    }
+    named_sync(bar_id, 128);
+    const __half *gzs = reinterpret_cast<const __half *>(sm + kOOffZ);
+    bf16 *os = reinterpret_cast<bf16 *>(sm + kOOffZ);  // each element is read, then overwritten, by one thread
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const int i = 32 * hh + e;
+      os[i * HD + v] = __float2bfloat16_rn(o[e] * rstd[i] * __half2float(gzs[i * HD + v]));
+    }
+    fence_proxy_async_smem();
+    named_sync(bar_id, 128);
+    if (tid == issuer) {
+      const int nout = min(32, nreal - 32 * hh);  // real tokens of this half
+      if (nout == 32) {
+        tma_store_2d(&omap, h * HD, start + t0 + 32 * hh, os + 32 * hh * HD);
+      } else {
+        bf16 *dst = A.out + ((size_t)(start + t0 + 32 * hh) * A.nv + h) * HD;
+        for (int i = 0; i < nout; ++i) bulk_s2g(dst + (size_t)i * A.nv * HD, os + (32 * hh + i) * HD, HD * 2);
+      }
+      bulk_commit();
+      bulk_wait_read_all();
+    }
   }
 done:
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 256);
+  if (warp == 0) tmem_dealloc(tmem, 64);
 }
 
 // Tensor map of a bf16 [rows][cols] row-major tensor with [32][128] boxes.
@@ -934,6 +1025,8 @@ gdn_status launch_prefill_tc(const LayerArgs &A, void *ws, cudaStream_t stream) 
     if (cudaFuncSetAttribute(tc::chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kChunkSmem) !=
             cudaSuccess ||
         cudaFuncSetAttribute(tc::state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kStateSmem) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(tc::output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kOutSmem) !=
             cudaSuccess)
       return fail(GDN_ERR_CUDA, "prefill: cannot reserve shared memory");
     attr_set[dev.id] = true;
@@ -942,10 +1035,12 @@ gdn_status launch_prefill_tc(const LayerArgs &A, void *ws, cudaStream_t stream) 
   if (gdn_status st = check_launch("prefill front")) return st;
   tc::chunk_kernel<<<dim3(S, A.nv), 256, tc::kChunkSmem, stream>>>(A, R, Ttot, W);
   if (gdn_status st = check_launch("prefill chunk")) return st;
+  tc::state_kernel<<<A.B * A.nv, 256, tc::kStateSmem, stream>>>(A, R, Ttot, W);
+  if (gdn_status st = check_launch("prefill state")) return st;
   CUtensorMap omap;
   if (gdn_status st = tc::encode_rows_map(&omap, A.out, Ttot, A.nv * tc::HD)) return st;
-  tc::state_kernel<<<A.B * A.nv, 256, tc::kStateSmem, stream>>>(A, R, Ttot, W, omap);
-  return check_launch("prefill state");
+  tc::output_kernel<<<dim3(S, A.nv), 256, tc::kOutSmem, stream>>>(A, R, Ttot, W, omap);
+  return check_launch("prefill output");
 }
 
 }  // namespace gdn
