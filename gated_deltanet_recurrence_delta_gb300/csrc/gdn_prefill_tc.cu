@@ -19,14 +19,16 @@
 //          K^T and V^T as [d][token].
 //   chunk  per (chunk slot, value head), all chunks in parallel: [K;Q] K^T on
 //          tcgen05 (M=128,N=64,K=128); A and P in fp32 from TMEM; T by a
-//          blocked fp32 triangular inverse; R = P T (tcgen05); then one
-//          tcgen05 product [T; R] [beta gamma K | beta V] (M=128,N=256,K=64)
-//          yields W, U, P W (-> Q') and P U (= O_local). Writes W|Q' as one
-//          swizzled image, (K*exp(G_C-G))^T as another, U and O_local fp32.
+//          blocked fp32 triangular inverse; R = P T (tcgen05); then the
+//          tcgen05 products [T; R] diag(beta gamma) K and [T; R] diag(beta) V
+//          (M=128,N=128,K=64 each; the factors ride on the columns of two
+//          [T; R] images) yield W, P W (-> Q'), U and P U (= O_local). Writes
+//          W|Q' as one swizzled image, U and O_local fp32, exp(G_C - G).
 //   state  per (row, value head), sequential over its chunks with the state
 //          in registers (fp32) and an fp16 copy in shared memory:
 //          X = S_math W^T (tcgen05 M=128,N=64,K=128) -> U' = U - X,
-//          dS = U'^T-image x (K~^T)-image (tcgen05 M=128,N=128,K=64) ->
+//          dS = (U' exp(G_C - G))^T-image x K^T-image (tcgen05 M=128,N=128,
+//          K=64) ->
 //          S = gamma_C S + dS; the fp16 state image at every chunk start
 //          is copied out.
 //   output per (chunk slot, value head), all chunks in parallel:
@@ -40,6 +42,8 @@
 // operands (10-bit mantissa; bf16 would leave the final state ~3e-3 off in
 // relative Frobenius norm). With every product in plain fp16 the normalised
 // outputs of badly conditioned tokens drift by ~1e-2.
+#include <utility>
+
 #include "gdn_launch.h"
 #include "gdn_token.cuh"
 #include "gdn_umma.cuh"
@@ -57,8 +61,9 @@ struct Ws {
   __half *ktimg;        // [S][nk][2 hi|lo][128][64]    K^T as a swizzled [dk][token] image
   __half *vtimg;        // [S][nv][2 hi|lo][128][64]    V^T as a swizzled [dv][token] image
   __half *wq;           // [S][nv][2][128][64]  W (rows 0-63) | Q' (rows 64-127) image (32 KiB)
-  __half *kt;           // [S][nv][128][64]     (K * exp(G_C - G))^T image (16 KiB)
-  float *ut, *ot;       // [S][nv][64][128]     U and O_local, token-major fp32 (32 KiB each)
+  float *sec;           // [S][nv][64]          exp(G_C - G_j) per token
+  float *ut, *ot;       // [S][nv][64][128]     U and O_local, token-major fp32, 16-byte chunk c of
+                        //                      row i stored at c ^ (i % 8) (32 KiB each)
   __half *gz;           // [S][nv][64][128]     norm_w * silu(z), row-major (16 KiB)
   float *gc;            // [S][nv]              gamma_C
   __half *simg;         // [S][nv][2][128][64]  fp16 image of the state at the chunk's start (32 KiB)
@@ -78,7 +83,7 @@ size_t slots_total(int B, int T, bool packed) {
 size_t ws_bytes(int B, int T, int nk, int nv, bool packed) {
   const size_t S = slots_total(B, T, packed);
   return 3 * a256(S * nk * kImg * 4) + a256(S * nv * kImg * 4) + a256(S * nv * kWQ * 2) +
-         a256(S * nv * kImg * 2) + 2 * a256(S * nv * kRowF * 4) + a256(S * nv * 4) + a256(S * nv * kImg * 2) +
+         a256(S * nv * CH * 4) + 2 * a256(S * nv * kRowF * 4) + a256(S * nv * 4) + a256(S * nv * kImg * 2) +
          a256(S * nv * kWQ * 2) + a256((size_t)B * 4);
 }
 
@@ -96,8 +101,8 @@ Ws carve(void *ws, int B, int T, int nk, int nv, bool packed) {
   p += a256(S * nv * kImg * 4);
   w.wq = reinterpret_cast<__half *>(p);
   p += a256(S * nv * kWQ * 2);
-  w.kt = reinterpret_cast<__half *>(p);
-  p += a256(S * nv * kImg * 2);
+  w.sec = reinterpret_cast<float *>(p);
+  p += a256(S * nv * CH * 4);
   w.ut = reinterpret_cast<float *>(p);
   p += a256(S * nv * kRowF * 4);
   w.ot = reinterpret_cast<float *>(p);
@@ -184,6 +189,7 @@ __device__ __forceinline__ void umma_tile_split(uint32_t tmem_d, uint32_t a_hi, 
 
 __global__ void __launch_bounds__(256, 3) front_kernel(LayerArgs A, Rows R, int Ttot, Ws W) {
   __shared__ __align__(16) float Y[CH][HD];
+  griddep_trigger();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int s = blockIdx.x, gi = blockIdx.y, kd = A.nk * HD;
   int r, c;
@@ -363,6 +369,8 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  griddep_wait();  // the front kernel's images are complete
+  griddep_trigger();
   if (tid == 0) {
     mbar_arrive_expect_tx(bar_ld, 131072);
     for (int part = 0; part < 2; ++part) {
@@ -422,41 +430,9 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
                     umma_idesc_f16(128, 64));
     umma_commit(bar_mma);
   }
-  {
-    // while the tensor core runs: scale the K^T / V^T rows in place into
-    // (beta gamma K)^T and (beta V)^T, and write (K exp(G_C - G))^T (plain
-    // fp16) to the workspace
-    unsigned char *ktout = reinterpret_cast<unsigned char *>(W.kt + ((size_t)s * A.nv + h) * kImg);
-    for (int e = tid; e < 256 * 8; e += 256) {
-      const int n = e & 255, cj = e >> 8;  // row n, tokens 8cj .. 8cj+7
-      const uint32_t off = sw128_chunk(256, n, cj);
-      const uint4 hv = *reinterpret_cast<const uint4 *>(B2H + off), lv = *reinterpret_cast<const uint4 *>(B2L + off);
-      const uint32_t hs[4] = {hv.x, hv.y, hv.z, hv.w}, ls[4] = {lv.x, lv.y, lv.z, lv.w};
-      float x[8];
-#pragma unroll
-      for (int e2 = 0; e2 < 4; ++e2) {
-        const float2 f = join2(hs[e2], ls[e2]);
-        x[2 * e2] = f.x;
-        x[2 * e2 + 1] = f.y;
-      }
-      if (n < HD) {
-        float kt8[8];
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          const int j = 8 * cj + t;
-          kt8[t] = x[t] * sec[j];
-          x[t] = x[t] * (sb[j] * sgam[j]);
-        }
-        *reinterpret_cast<uint4 *>(ktout + sw128_chunk(128, n, cj)) =
-            make_uint4(pack_h2(kt8[0], kt8[1]), pack_h2(kt8[2], kt8[3]), pack_h2(kt8[4], kt8[5]),
-                       pack_h2(kt8[6], kt8[7]));
-      } else {
-#pragma unroll
-        for (int t = 0; t < 8; ++t) x[t] *= sb[8 * cj + t];
-      }
-      store_split8(B2H, B2L, off, x);
-    }
-    fence_proxy_async_smem();
+  if (tid < CH) {  // per-token factors for the state pass: exp(G_C - G_j)
+    W.sec[((size_t)s * A.nv + h) * CH + tid] = sec[tid];
+    if (tid == 0) W.gc[(size_t)s * A.nv + h] = sgam[CH - 1];
   }
   if (!cta_wait(bar_mma, 0, A.status)) goto done;
   tc_fence_after();
@@ -492,6 +468,7 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
 
   // ---- T = (I + A)^-1 in place, 16x16 blocks: diagonal blocks by forward
   // substitution, then T_ab = -(sum_{b<c<=a} T_ac A_cb) T_bb column by column.
+  float t16[16];  // T row i = tid / 4, columns 16 (tid % 4) .. +15 (kept for the second image)
   {
     float x[16];
     const int bb = tid >> 4, cc = tid & 15;
@@ -543,15 +520,17 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
       }
       __syncthreads();
     }
-    // T (fp32, in AF) -> [T; R] split image rows 0-63 (hi aliases AF) and the
-    // split T^T image (rows 64-127 of the P tiles)
+    // T (fp32, in AF) -> rows 0-63 of the split image [T; R] diag(beta gamma)
+    // (hi aliases AF) and the split T^T image (rows 64-127 of the P tiles)
     const int i = tid >> 2, q4 = tid & 3;
-    float t16[16];
 #pragma unroll
     for (int k = 0; k < 16; ++k) t16[k] = AF[i * kLD + 16 * q4 + k];
     __syncthreads();
+    float y16[16];
 #pragma unroll
-    for (int c2 = 0; c2 < 2; ++c2) store_split8(TRH, TRL, sw128_chunk(128, i, 2 * q4 + c2), t16 + 8 * c2);
+    for (int k = 0; k < 16; ++k) y16[k] = t16[k] * (sb[16 * q4 + k] * sgam[16 * q4 + k]);
+#pragma unroll
+    for (int c2 = 0; c2 < 2; ++c2) store_split8(TRH, TRL, sw128_chunk(128, i, 2 * q4 + c2), y16 + 8 * c2);
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
       const uint32_t off = sw128_off(128, CH + 16 * q4 + k, i);
@@ -573,38 +552,56 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
   }
   if (!cta_wait(bar_mma, 1, A.status)) goto done;
   tc_fence_after();
+  // the P tiles are free: they take the second image [T; R] diag(beta)
+  {
+    const int i = tid >> 2, q4 = tid & 3;
+    float y16[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) y16[k] = t16[k] * sb[16 * q4 + k];
+#pragma unroll
+    for (int c2 = 0; c2 < 2; ++c2) store_split8(PTH, PTL, sw128_chunk(128, i, 2 * q4 + c2), y16 + 8 * c2);
+  }
   if ((warp & 3) < 2) {
     const int q = warp & 3, hh = warp >> 2, i = 32 * q + lane;
-    float v[32];
+    float v[32], y[32];
     tmem_ld32(tmem_at(tmem, q, 32 * hh), v);
 #pragma unroll
-    for (int c4 = 0; c4 < 4; ++c4) store_split8(TRH, TRL, sw128_chunk(128, CH + i, 4 * hh + c4), v + 8 * c4);
-    fence_proxy_async_smem();
+    for (int jj = 0; jj < 32; ++jj) y[jj] = v[jj] * (sb[32 * hh + jj] * sgam[32 * hh + jj]);
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) store_split8(TRH, TRL, sw128_chunk(128, CH + i, 4 * hh + c4), y + 8 * c4);
+#pragma unroll
+    for (int jj = 0; jj < 32; ++jj) y[jj] = v[jj] * sb[32 * hh + jj];
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) store_split8(PTH, PTL, sw128_chunk(128, CH + i, 4 * hh + c4), y + 8 * c4);
   }
+  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
 
-  // ---- [T; R] [beta gamma K | beta V] -> TMEM columns [0, 256):
-  //   lanes 0-63: W (cols 0-127) | U (cols 128-255); lanes 64-127: P W | P U
+  // ---- [T; R] diag(beta gamma) K -> TMEM columns [0, 128) (W | P W) and
+  //      [T; R] diag(beta) V -> columns [128, 256) (U | P U)
   if (tid == 0) {
     tc_fence_after();
     umma_tile_split(tmem, smem_u32(TRH), smem_u32(TRL), 128, smem_u32(B2H), smem_u32(B2L), 256, 64,
-                    umma_idesc_f16(128, 256));
+                    umma_idesc_f16(128, 128));
+    umma_tile_split(tmem + 128, smem_u32(PTH), smem_u32(PTL), 128, smem_u32(B2H) + HD * 128,
+                    smem_u32(B2L) + HD * 128, 256, 64, umma_idesc_f16(128, 128));
     umma_commit(bar_mma);
   }
   if (!cta_wait(bar_mma, 0, A.status)) goto done;
   tc_fence_after();
   {
+    // W / Q' into the K|Q image (plain fp16); U / O_local rows, fp32, staged in
+    // the free B2 tiles in the row-swizzled layout of the workspace (16-byte
+    // chunk c of row i at c ^ (i % 8)), then bulk-stored
     const int q = warp & 3, hh = warp >> 2, row = 32 * q + lane, i = row & (CH - 1);
     const bool upper = row >= CH;
     const float gam = sgam[i];
-    float *ut = W.ut + ((size_t)s * A.nv + h) * kRowF;
-    float *ot = W.ot + ((size_t)s * A.nv + h) * kRowF;
+    float4 *stage = reinterpret_cast<float4 *>(sm + kOffB2H + (upper ? 32768 : 0)) + (size_t)i * 32;
     for (int cb = 0; cb < 4; ++cb) {
       float v[32];
       tmem_ld32(tmem_at(tmem, q, 128 * hh + 32 * cb), v);
       if (hh == 0) {
-        // W row i (dk columns 32cb..) or Q' = gamma Q - P W, plain fp16 for the state kernel
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
           const uint32_t off = sw128_chunk(128, row, 4 * cb + c4);
@@ -626,18 +623,19 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
           *dst = make_uint4(pack_h2(y[0], y[1]), pack_h2(y[2], y[3]), pack_h2(y[4], y[5]), pack_h2(y[6], y[7]));
         }
       } else {
-        // U or O_local row i (token-major)
-        float4 *dst = reinterpret_cast<float4 *>((upper ? ot : ut) + (size_t)i * HD + 32 * cb);
 #pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) dst[c4] = make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
+        for (int c4 = 0; c4 < 8; ++c4)
+          stage[(8 * cb + c4) ^ (i & 7)] = make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
       }
     }
-    if (tid == 0) W.gc[(size_t)s * A.nv + h] = sgam[CH - 1];
     fence_proxy_async_smem();
   }
   __syncthreads();
   if (tid == 0) {
-    bulk_s2g(W.wq + ((size_t)s * A.nv + h) * kWQ, KQH, 32768);
+    const size_t sh = (size_t)s * A.nv + h;
+    bulk_s2g(W.wq + sh * kWQ, KQH, 32768);
+    bulk_s2g(W.ut + sh * kRowF, sm + kOffB2H, 32768);
+    bulk_s2g(W.ot + sh * kRowF, sm + kOffB2H + 32768, 32768);
     bulk_commit();
     bulk_wait_read_all();  // shared memory may be released; the writes land before the grid completes
   }
@@ -651,7 +649,8 @@ done:
 //
 // The sequential part only: per (row, value head), over its chunks,
 //   X = S_math W^T (tcgen05 M=128 v, N=64 tokens, K=128) -> U' = U - X,
-//   dS = U'^T-image x (K~^T)-image (M=128, N=128, K=64) -> S = gamma_C S + dS,
+//   dS = (U' * exp(G_C - G))^T-image x K^T-image (M=128, N=128, K=64) ->
+//   S = gamma_C S + dS,
 // with the state in registers (fp32) and an fp16 copy in shared memory. The
 // fp16 image of the state at the start of every chunk is copied out (bulk
 // store) for the output kernel, which does O = Q' S + O_local off this path.
@@ -661,7 +660,8 @@ constexpr int kSOffW = 32768;     // 2 x W image [2 kb][64 rows][128 B] (16 KiB 
 constexpr int kSOffKT = 65536;    // 2 x K~^T image [128 rows][128 B] (16 KiB each)
 constexpr int kSOffUT = 98304;    // 2 x U fp32 [64 tokens][128 v] (32 KiB each)
 constexpr int kSOffUP = 163840;   // U'^T image [128 rows][128 B] (16 KiB)
-constexpr int kSOffBar = 180224;  // barriers, TMEM base
+constexpr int kSOffSec = 180224;  // 2 x exp(G_C - G_j), fp32 [64]
+constexpr int kSOffBar = 180736;  // barriers, TMEM base
 constexpr int kStateSmem = kSOffBar + 64 + 1024;
 
 __device__ __forceinline__ void named_sync(int id, int n) {
@@ -751,19 +751,19 @@ __global__ void __launch_bounds__(256, 1) state_kernel(LayerArgs A, Rows R, int 
   const uint32_t tmem = *tmem_slot;
 
   // chunk ci's W rows (rows 0-63 of each column block of the W|Q' image),
-  // (K exp(G_C - G))^T and U
+  // the fp16 K^T image of the key head, U and exp(G_C - G)
   auto issue_loads = [&](int ci) {  // thread 0
     const int buf = ci & 1, s = s0 + ci;
-    const unsigned char *wq = reinterpret_cast<const unsigned char *>(W.wq + ((size_t)s * A.nv + h) * kWQ);
+    const size_t sh = (size_t)s * A.nv + h;
+    const unsigned char *wq = reinterpret_cast<const unsigned char *>(W.wq + sh * kWQ);
     unsigned char *wdst = sm + kSOffW + buf * 16384;
-    mbar_arrive_expect_tx(&bar_ld[buf], 16384 + 16384 + 32768);
+    mbar_arrive_expect_tx(&bar_ld[buf], 16384 + 16384 + 32768 + CH * 4);
     bulk_g2s(wdst, wq, 8192, &bar_ld[buf]);
     bulk_g2s(wdst + 8192, wq + 16384, 8192, &bar_ld[buf]);
-    bulk_g2s(sm + kSOffKT + buf * 16384, W.kt + ((size_t)s * A.nv + h) * kImg, 16384, &bar_ld[buf]);
-    bulk_g2s(sm + kSOffUT + buf * 32768, W.ut + ((size_t)s * A.nv + h) * kRowF, 32768, &bar_ld[buf]);
+    bulk_g2s(sm + kSOffKT + buf * 16384, W.ktimg + ((size_t)s * A.nk + kh) * 2 * kImg, 16384, &bar_ld[buf]);
+    bulk_g2s(sm + kSOffUT + buf * 32768, W.ut + sh * kRowF, 32768, &bar_ld[buf]);
+    bulk_g2s(sm + kSOffSec + buf * CH * 4, W.sec + sh * CH, CH * 4, &bar_ld[buf]);
   };
-  if (tid == 0 && n_chunks > 0) issue_loads(0);
-
   // thread <-> (value row v = TMEM lane, key half / token half hh)
   const int q = warp & 3, hh = warp >> 2, v = 32 * q + lane;
   float Sv[64];
@@ -779,6 +779,9 @@ __global__ void __launch_bounds__(256, 1) state_kernel(LayerArgs A, Rows R, int 
     fence_proxy_async_smem();
   };
   write_simg();
+  griddep_wait();  // the chunk kernel's outputs are complete
+  griddep_trigger();
+  if (tid == 0 && n_chunks > 0) issue_loads(0);
   tc_fence_before();
   __syncthreads();
   if (tid == 0 && n_chunks > 0) {  // the state image at the start of chunk 0
@@ -800,15 +803,19 @@ __global__ void __launch_bounds__(256, 1) state_kernel(LayerArgs A, Rows R, int 
     if (!cta_wait(bar_mma, 0, A.status)) goto done;
     tc_fence_after();
     {
-      // U' = U - W S for tokens 32hh .. 32hh+31 of value row v -> fp16 image row v
-      const float *ut = reinterpret_cast<const float *>(sm + kSOffUT + buf * 32768) + (size_t)(32 * hh) * HD + v;
+      // (U - W S) * exp(G_C - G) for tokens 32hh .. 32hh+31 of value row v -> fp16 image row v
+      const float *ut = reinterpret_cast<const float *>(sm + kSOffUT + buf * 32768);
+      const float *sec = reinterpret_cast<const float *>(sm + kSOffSec + buf * CH * 4) + 32 * hh;
       float x[32];
       tmem_ld32(tmem_at(tmem, q, 32 * hh), x);
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {
         float y[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) y[e] = ut[(size_t)(8 * c4 + e) * HD] - x[8 * c4 + e];
+        for (int e = 0; e < 8; ++e) {
+          const int i = 32 * hh + 8 * c4 + e;  // token; element (i, v) sits in chunk (v / 4) ^ (i % 8) of row i
+          y[e] = (ut[i * HD + ((((v >> 2) ^ (i & 7))) << 2) + (v & 3)] - x[8 * c4 + e]) * sec[8 * c4 + e];
+        }
         *reinterpret_cast<uint4 *>(UP + sw128_chunk(128, v, 4 * hh + c4)) =
             make_uint4(pack_h2(y[0], y[1]), pack_h2(y[2], y[3]), pack_h2(y[4], y[5]), pack_h2(y[6], y[7]));
       }
@@ -882,6 +889,8 @@ __global__ void __launch_bounds__(256, 2) output_kernel(LayerArgs A, Rows R, int
   const int s = blockIdx.x, h = blockIdx.y;
   int r, c;
   R.locate(s, Ttot, r, c);
+  griddep_wait();  // the state kernel's images and row lengths are complete
+  griddep_trigger();
   if (r < 0) return;
   const int Lr = W.lr[r];
   if (Lr < 0) return;  // the row was rejected (its status is set)
@@ -927,9 +936,12 @@ __global__ void __launch_bounds__(256, 2) output_kernel(LayerArgs A, Rows R, int
     const int q = warp & 3, hh = warp >> 2, v = 32 * q + lane, bar_id = 1 + hh, issuer = 128 * hh;
     float o[32];
     tmem_ld32(tmem_at(tmem, q, 32 * hh), o);
-    const float *ol = reinterpret_cast<const float *>(sm + kOOffOT) + (size_t)(32 * hh) * HD + v;
+    const float *ol = reinterpret_cast<const float *>(sm + kOOffOT);
 #pragma unroll
-    for (int e = 0; e < 32; ++e) o[e] += ol[(size_t)e * HD];
+    for (int e = 0; e < 32; ++e) {
+      const int i = 32 * hh + e;  // element (i, v) sits in chunk (v / 4) ^ (i % 8) of row i
+      o[e] += ol[i * HD + ((((v >> 2) ^ (i & 7))) << 2) + (v & 3)];
+    }
     // sum over the warp's 32 rows of o^2 for each of the 32 tokens: after the
     // transposing butterfly lane l holds token l's partial
     float sq[32];
@@ -1007,6 +1019,22 @@ gdn_status encode_rows_map(CUtensorMap *map, const void *base, int rows, int col
   return GDN_OK;
 }
 
+// Launch with programmatic stream serialization (256 threads per CTA).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, size_t smem, cudaStream_t stream, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 }  // namespace tc
 
 size_t prefill_tc_workspace_bytes(int B, int T, int nk, int nv, bool packed) {
@@ -1033,13 +1061,17 @@ gdn_status launch_prefill_tc(const LayerArgs &A, void *ws, cudaStream_t stream) 
   }
   tc::front_kernel<<<dim3(S, 2 * A.nk + 2 * A.nv), 256, 0, stream>>>(A, R, Ttot, W);
   if (gdn_status st = check_launch("prefill front")) return st;
-  tc::chunk_kernel<<<dim3(S, A.nv), 256, tc::kChunkSmem, stream>>>(A, R, Ttot, W);
-  if (gdn_status st = check_launch("prefill chunk")) return st;
-  tc::state_kernel<<<A.B * A.nv, 256, tc::kStateSmem, stream>>>(A, R, Ttot, W);
-  if (gdn_status st = check_launch("prefill state")) return st;
+  // chunk, state and output start early (programmatic dependent launch) and
+  // wait for their predecessor inside the kernel
   CUtensorMap omap;
   if (gdn_status st = tc::encode_rows_map(&omap, A.out, Ttot, A.nv * tc::HD)) return st;
-  tc::output_kernel<<<dim3(S, A.nv), 256, tc::kOutSmem, stream>>>(A, R, Ttot, W, omap);
+  if (tc::launch_dependent(tc::chunk_kernel, dim3(S, A.nv), tc::kChunkSmem, stream, A, R, Ttot, W) != cudaSuccess)
+    return check_launch("prefill chunk");
+  if (tc::launch_dependent(tc::state_kernel, dim3(A.B * A.nv), tc::kStateSmem, stream, A, R, Ttot, W) != cudaSuccess)
+    return check_launch("prefill state");
+  if (tc::launch_dependent(tc::output_kernel, dim3(S, A.nv), tc::kOutSmem, stream, A, R, Ttot, W, omap) !=
+      cudaSuccess)
+    return check_launch("prefill output");
   return check_launch("prefill output");
 }
 
