@@ -156,6 +156,11 @@ __device__ __forceinline__ bool cta_wait(uint64_t *bar, uint32_t parity, unsigne
   return ok;
 }
 
+// Named barrier `id` over `n` threads (whole warps).
+__device__ __forceinline__ void named_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 // ------------------------------------------------------------ split fp16
 
 __device__ __forceinline__ void split2(float a, float b, uint32_t &hi, uint32_t &lo) {
@@ -319,8 +324,8 @@ constexpr int kLD = 65;          // padded row stride: column-wise accesses hit 
 constexpr int kOffTRL = 147456;  // [T; R] image (lo)
 constexpr int kOffPTH = 163840;  // [128 rows][128 B]: P rows 0-63 | T^T rows 64-127 (hi)
 constexpr int kOffPTL = 180224;  // the same, lo parts
-constexpr int kOffSCR = 196608;  // fp32 [3][16][16] solve scratch
-constexpr int kOffSm = 199680;   // g, beta, G, exp(G), exp(G_C - G): fp32 [5][64]; barriers; tmem base
+constexpr int kOffSCR = 196608;  // fp32 [1024] solve scratch
+constexpr int kOffSm = 200704;   // g, beta, G, exp(G), exp(G_C - G): fp32 [5][64]; barriers; tmem base
 constexpr int kChunkSmem = kOffSm + 2048 + 1024;  // + alignment slack
 
 __device__ __forceinline__ void store_split8(unsigned char *hi_img, unsigned char *lo_img, uint32_t off,
@@ -466,13 +471,16 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
   tc_fence_before();
   __syncthreads();
 
-  // ---- T = (I + A)^-1 in place, 16x16 blocks: diagonal blocks by forward
-  // substitution, then T_ab = -(sum_{b<c<=a} T_ac A_cb) T_bb column by column.
+  // ---- T = (I + A)^-1 in place by recursive doubling on the 2x2 block form
+  //      inv([[X, 0], [Y, Z]]) = [[X^-1, 0], [-Z^-1 Y X^-1, Z^-1]]:
+  //      the four diagonal 16x16 blocks by forward substitution, then the two
+  //      16x16 off-diagonal blocks of the 32x32 diagonal blocks, then the
+  //      lower-left 32x32 block. Each product runs over all 256 threads.
   float t16[16];  // T row i = tid / 4, columns 16 (tid % 4) .. +15 (kept for the second image)
   {
-    float x[16];
-    const int bb = tid >> 4, cc = tid & 15;
     if (tid < 64) {
+      const int bb = tid >> 4, cc = tid & 15;
+      float x[16];
       const float *Ab = AF + (16 * bb) * kLD + 16 * bb;
 #pragma unroll
       for (int rr = 0; rr < 16; ++rr) {
@@ -481,50 +489,71 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
         for (int l = 0; l < rr; ++l) acc = fmaf(-Ab[rr * kLD + l], x[l], acc);
         x[rr] = acc;
       }
-    }
-    __syncthreads();
-    if (tid < 64) {
+      named_sync(1, 64);  // every diagonal block has been read
       float *Tb = AF + (16 * bb) * kLD + 16 * bb;
 #pragma unroll
       for (int rr = 0; rr < 16; ++rr) Tb[rr * kLD + cc] = x[rr];
     }
     __syncthreads();
-    for (int b = 2; b >= 0; --b) {
-      const int nrows = 3 - b;
-      for (int e = tid; e < nrows * 256; e += 256) {
-        const int a = b + 1 + (e >> 8), rr = (e >> 4) & 15, m = e & 15;
-        float acc = 0.0f;
-        for (int cb = b + 1; cb <= a; ++cb) {
-          const float *Tac = AF + (16 * a + rr) * kLD + 16 * cb;
-          const float *Acb = AF + (16 * cb) * kLD + 16 * b + m;
+    {
+      // level 1: blocks (1,0) and (3,2): X = A_rc T_cc, then T_rc = -T_rr X
+      const int pr = tid >> 7, rem = tid & 127, rr = rem >> 3, m0 = (rem & 7) * 2;
+      const int r0 = 16 + 32 * pr, c0 = 32 * pr;
+      float x0 = 0.0f, x1 = 0.0f;
 #pragma unroll
-          for (int k = 0; k < 16; ++k) acc = fmaf(Tac[k], Acb[k * kLD], acc);
-        }
-        SCR[e] = acc;
+      for (int k = 0; k < 16; ++k) {
+        const float a = AF[(r0 + rr) * kLD + c0 + k];
+        x0 = fmaf(a, AF[(c0 + k) * kLD + c0 + m0], x0);
+        x1 = fmaf(a, AF[(c0 + k) * kLD + c0 + m0 + 1], x1);
       }
+      SCR[pr * 256 + rr * 16 + m0] = x0;
+      SCR[pr * 256 + rr * 16 + m0 + 1] = x1;
       __syncthreads();
-      float outv[3];
-      for (int e = tid, n = 0; e < nrows * 256; e += 256, ++n) {
-        const int rr = (e >> 4) & 15, m = e & 15;
-        const float *M = SCR + (e >> 8) * 256 + rr * 16;
-        const float *Tbb = AF + (16 * b) * kLD + 16 * b + m;
-        float acc = 0.0f;
+      float y0 = 0.0f, y1 = 0.0f;
 #pragma unroll
-        for (int k = 0; k < 16; ++k) acc = fmaf(M[k], Tbb[k * kLD], acc);
-        outv[n] = -acc;
+      for (int k = 0; k < 16; ++k) {
+        const float t = AF[(r0 + rr) * kLD + r0 + k];
+        y0 = fmaf(t, SCR[pr * 256 + k * 16 + m0], y0);
+        y1 = fmaf(t, SCR[pr * 256 + k * 16 + m0 + 1], y1);
       }
-      __syncthreads();
-      for (int e = tid, n = 0; e < nrows * 256; e += 256, ++n) {
-        const int a = b + 1 + (e >> 8), rr = (e >> 4) & 15, m = e & 15;
-        AF[(16 * a + rr) * kLD + 16 * b + m] = outv[n];
-      }
-      __syncthreads();
+      AF[(r0 + rr) * kLD + c0 + m0] = -y0;
+      AF[(r0 + rr) * kLD + c0 + m0 + 1] = -y1;
     }
+    __syncthreads();
+    {
+      // level 2: block rows 32-63, columns 0-31: Y = A_BA T_A, then T_BA = -T_B Y
+      const int r = tid >> 3, m0 = (tid & 7) * 4;
+      float y[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const float a = AF[(32 + r) * kLD + k];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) y[e] = fmaf(a, AF[k * kLD + m0 + e], y[e]);
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) SCR[r * 32 + m0 + e] = y[e];
+      __syncthreads();
+      float z[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const float t = AF[(32 + r) * kLD + 32 + k];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) z[e] = fmaf(t, SCR[k * 32 + m0 + e], z[e]);
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) AF[(32 + r) * kLD + m0 + e] = -z[e];
+    }
+    __syncthreads();
     // T (fp32, in AF) -> rows 0-63 of the split image [T; R] diag(beta gamma)
-    // (hi aliases AF) and the split T^T image (rows 64-127 of the P tiles)
+    // (hi aliases AF) and the split T^T image (rows 64-127 of the P tiles,
+    // row j = column j of T, gathered by column)
     const int i = tid >> 2, q4 = tid & 3;
 #pragma unroll
     for (int k = 0; k < 16; ++k) t16[k] = AF[i * kLD + 16 * q4 + k];
+    const int jc = tid & 63, ip = tid >> 6;  // T^T row jc, tokens 16 ip .. +15
+    float tc16[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) tc16[k] = AF[(16 * ip + k) * kLD + jc];
     __syncthreads();
     float y16[16];
 #pragma unroll
@@ -532,12 +561,7 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
 #pragma unroll
     for (int c2 = 0; c2 < 2; ++c2) store_split8(TRH, TRL, sw128_chunk(128, i, 2 * q4 + c2), y16 + 8 * c2);
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const uint32_t off = sw128_off(128, CH + 16 * q4 + k, i);
-      const __half hv = __float2half_rn(t16[k]);
-      *reinterpret_cast<__half *>(PTH + off) = hv;
-      *reinterpret_cast<__half *>(PTL + off) = __float2half_rn(t16[k] - __half2float(hv));
-    }
+    for (int c2 = 0; c2 < 2; ++c2) store_split8(PTH, PTL, sw128_chunk(128, CH + jc, 2 * ip + c2), tc16 + 8 * c2);
     fence_proxy_async_smem();
   }
   tc_fence_before();
@@ -663,10 +687,6 @@ constexpr int kSOffUP = 163840;   // U'^T image [128 rows][128 B] (16 KiB)
 constexpr int kSOffSec = 180224;  // 2 x exp(G_C - G_j), fp32 [64]
 constexpr int kSOffBar = 180736;  // barriers, TMEM base
 constexpr int kStateSmem = kSOffBar + 64 + 1024;
-
-__device__ __forceinline__ void named_sync(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
 
 __global__ void __launch_bounds__(256, 1) state_kernel(LayerArgs A, Rows R, int Ttot, Ws W) {
   extern __shared__ unsigned char smem_raw[];
