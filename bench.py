@@ -317,9 +317,9 @@ def phase_verify(gdn, world, steps, warmup, peak_hbm):
     res = {"tokens_per_s": P * K * world / (ms * 1e-3), "ms_per_step": ms, "tokens_per_step": P * K,
            "kernel_ms": kms, "launches_per_step": 2, "algorithmic_bytes_per_step": nbytes,
            "step_hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peak_hbm,
-           "roofline": {"bound": "hbm", "kernel": "verify_kernel", "achieved": vbytes / (kms * 1e-3) / 1e9,
+           "roofline": {"bound": "hbm", "kernel": "verify_split_kernel", "achieved": vbytes / (kms * 1e-3) / 1e9,
                         "peak": peak_hbm, "unit": "GB/s", "frac": vbytes / (kms * 1e-3) / 1e9 / peak_hbm,
-                        "traffic": dram_traffic("verify_kernel")}}
+                        "traffic": dram_traffic("verify_split_kernel")}}
     del sets
     torch.cuda.empty_cache()
     return res
