@@ -444,28 +444,28 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
   {
     // A (rows 0-63: strictly lower, beta_i KK_ij Gamma_ij) in fp32; P (rows
     // 64-127: QK_ij Gamma_ij for j <= i) as a split image
+    // rolled over 8-column groups: this code runs once per CTA, so a compact
+    // loop fetches far fewer instructions than a fully unrolled one
     const int q = warp & 3, hh = warp >> 2, row = 32 * q + lane;
-    float v[32];
-    tmem_ld32(tmem_at(tmem, q, 32 * hh), v);
-    if (row < CH) {
-      const int i = row;
-      const float Gi = sG[i], bi = sb[i];
+    const bool arow = row < CH;
+    const int i = row & (CH - 1);
+    const float Gi = sG[i], bi = sb[i];
+#pragma unroll 1
+    for (int g8 = 0; g8 < 4; ++g8) {
+      float v[8], y[8];
+      tmem_ld8(tmem_at(tmem, q, 32 * hh + 8 * g8), v);
 #pragma unroll
-      for (int jj = 0; jj < 32; ++jj) {
-        const int j = 32 * hh + jj;
-        AF[i * kLD + j] = j < i ? bi * v[jj] * __expf(Gi - sG[j]) : 0.0f;
+      for (int e = 0; e < 8; ++e) {
+        const int j = 32 * hh + 8 * g8 + e;
+        const float gam = __expf(Gi - sG[j]);
+        y[e] = arow ? (j < i ? bi * v[e] * gam : 0.0f) : (j <= i ? v[e] * gam : 0.0f);
       }
-    } else {
-      const int i = row - CH;
-      const float Gi = sG[i];
-      float pv[32];
+      if (arow) {
 #pragma unroll
-      for (int jj = 0; jj < 32; ++jj) {
-        const int j = 32 * hh + jj;
-        pv[jj] = j <= i ? v[jj] * __expf(Gi - sG[j]) : 0.0f;
+        for (int e = 0; e < 8; ++e) AF[i * kLD + 32 * hh + 8 * g8 + e] = y[e];
+      } else {
+        store_split8(PTH, PTL, sw128_chunk(128, i, 4 * hh + g8), y);
       }
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) store_split8(PTH, PTL, sw128_chunk(128, i, 4 * hh + c4), pv + 8 * c4);
     }
   }
   tc_fence_before();
@@ -587,16 +587,18 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
   }
   if ((warp & 3) < 2) {
     const int q = warp & 3, hh = warp >> 2, i = 32 * q + lane;
-    float v[32], y[32];
-    tmem_ld32(tmem_at(tmem, q, 32 * hh), v);
+#pragma unroll 1
+    for (int g8 = 0; g8 < 4; ++g8) {
+      float v[8], y[8];
+      tmem_ld8(tmem_at(tmem, q, 32 * hh + 8 * g8), v);
+      const int j0 = 32 * hh + 8 * g8;
 #pragma unroll
-    for (int jj = 0; jj < 32; ++jj) y[jj] = v[jj] * (sb[32 * hh + jj] * sgam[32 * hh + jj]);
+      for (int e = 0; e < 8; ++e) y[e] = v[e] * (sb[j0 + e] * sgam[j0 + e]);
+      store_split8(TRH, TRL, sw128_chunk(128, CH + i, 4 * hh + g8), y);
 #pragma unroll
-    for (int c4 = 0; c4 < 4; ++c4) store_split8(TRH, TRL, sw128_chunk(128, CH + i, 4 * hh + c4), y + 8 * c4);
-#pragma unroll
-    for (int jj = 0; jj < 32; ++jj) y[jj] = v[jj] * sb[32 * hh + jj];
-#pragma unroll
-    for (int c4 = 0; c4 < 4; ++c4) store_split8(PTH, PTL, sw128_chunk(128, CH + i, 4 * hh + c4), y + 8 * c4);
+      for (int e = 0; e < 8; ++e) y[e] = v[e] * sb[j0 + e];
+      store_split8(PTH, PTL, sw128_chunk(128, CH + i, 4 * hh + g8), y);
+    }
   }
   fence_proxy_async_smem();
   tc_fence_before();
@@ -622,6 +624,7 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
     const bool upper = row >= CH;
     const float gam = sgam[i];
     float4 *stage = reinterpret_cast<float4 *>(sm + kOffB2H + (upper ? 32768 : 0)) + (size_t)i * 32;
+#pragma unroll 1
     for (int cb = 0; cb < 4; ++cb) {
       float v[32];
       tmem_ld32(tmem_at(tmem, q, 128 * hh + 32 * cb), v);
