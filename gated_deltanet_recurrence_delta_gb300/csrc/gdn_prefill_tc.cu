@@ -14,9 +14,9 @@
 // (S on the stored transpose St[k][v]). exp(-G) is never formed.
 //
 // Kernels (one call = front -> chunk -> state -> output, stream ordered):
-//   front  conv + SiLU + q/k L2 norm per (chunk slot, head), written as split
-//          fp16 tiles (128B-swizzled K-major images): K and Q as [token][d],
-//          K^T and V^T as [d][token].
+//   front  conv + SiLU + q/k L2 norm per (chunk slot, q/k/v head), written
+//          as split fp16 tiles (128B-swizzled K-major images): K and Q as
+//          [token][d], K^T and V^T as [d][token].
 //   chunk  per (chunk slot, value head), all chunks in parallel: [K;Q] K^T on
 //          tcgen05 (M=128,N=64,K=128); A and P in fp32 from TMEM; T by a
 //          blocked fp32 triangular inverse; R = P T (tcgen05); then the
@@ -33,7 +33,8 @@
 //          is copied out.
 //   output per (chunk slot, value head), all chunks in parallel:
 //          O = Q' S + O_local from that image (tcgen05 M=128,N=64,K=128),
-//          gated RMSNorm epilogue, bf16 rows out through the TMA.
+//          gated RMSNorm epilogue with z loaded by the TMA, bf16 rows out
+//          through the TMA.
 // Operand tiles move between HBM and shared memory with bulk copies (TMA).
 // Precision: accumulators are fp32. The chunk kernel runs every product in
 // split fp16 (x = hi + lo, hi = fp16(x), lo = fp16(x - hi); a*b ~ hi*hi +
@@ -64,7 +65,6 @@ struct Ws {
   float *sec;           // [S][nv][64]          exp(G_C - G_j) per token
   float *ut, *ot;       // [S][nv][64][128]     U and O_local, token-major fp32, 16-byte chunk c of
                         //                      row i stored at c ^ (i % 8) (32 KiB each)
-  __half *gz;           // [S][nv][64][128]     norm_w * silu(z), row-major (16 KiB)
   float *gc;            // [S][nv]              gamma_C
   __half *simg;         // [S][nv][2][128][64]  fp16 image of the state at the chunk's start (32 KiB)
   int *lr;              // [B]                  real length of each row, -1 = row rejected
@@ -83,7 +83,7 @@ size_t slots_total(int B, int T, bool packed) {
 size_t ws_bytes(int B, int T, int nk, int nv, bool packed) {
   const size_t S = slots_total(B, T, packed);
   return 3 * a256(S * nk * kImg * 4) + a256(S * nv * kImg * 4) + a256(S * nv * kWQ * 2) +
-         a256(S * nv * CH * 4) + 2 * a256(S * nv * kRowF * 4) + a256(S * nv * 4) + a256(S * nv * kImg * 2) +
+         a256(S * nv * CH * 4) + 2 * a256(S * nv * kRowF * 4) + a256(S * nv * 4) +
          a256(S * nv * kWQ * 2) + a256((size_t)B * 4);
 }
 
@@ -109,8 +109,6 @@ Ws carve(void *ws, int B, int T, int nk, int nv, bool packed) {
   p += a256(S * nv * kRowF * 4);
   w.gc = reinterpret_cast<float *>(p);
   p += a256(S * nv * 4);
-  w.gz = reinterpret_cast<__half *>(p);
-  p += a256(S * nv * kImg * 2);
   w.simg = reinterpret_cast<__half *>(p);
   p += a256(S * nv * kWQ * 2);
   w.lr = reinterpret_cast<int *>(p);
@@ -201,33 +199,11 @@ __global__ void __launch_bounds__(256, 3) front_kernel(LayerArgs A, Rows R, int 
   R.locate(s, Ttot, r, c);
   if (r < 0) return;
   const int start = R.start(r), len = R.len(r);
-  const int which = gi < A.nk ? 0 : (gi < 2 * A.nk ? 1 : (gi < 2 * A.nk + A.nv ? 2 : 3));
-  const int head = which == 0 ? gi : (which == 1 ? gi - A.nk : (which == 2 ? gi - 2 * A.nk : gi - 2 * A.nk - A.nv));
+  const int which = gi < A.nk ? 0 : (gi < 2 * A.nk ? 1 : 2);
+  const int head = which == 0 ? gi : (which == 1 ? gi - A.nk : gi - 2 * A.nk);
   const int slot = row_slot(A, r);
   // thread -> 8 channels (cb) x 4 tokens (tb): 16-byte loads of 7 input rows
   const int cb = tid & 15, tb = tid >> 4, pos0 = c * CH + 4 * tb;
-  if (which == 3) {
-    // output gate of value head `head`: norm_w * silu(z), fp16 [token][v]
-    const uint4 wv = __ldg(reinterpret_cast<const uint4 *>(A.norm_w) + cb);
-    const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
-    __half *gz = W.gz + ((size_t)s * A.nv + head) * kImg;
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const int pos = pos0 + t;
-      uint4 zv = make_uint4(0u, 0u, 0u, 0u);
-      if (pos < len) zv = __ldg(reinterpret_cast<const uint4 *>(A.z + ((size_t)(start + pos) * A.nv + head) * HD) + cb);
-      const uint32_t zs[4] = {zv.x, zv.y, zv.z, zv.w};
-      float y[8];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        y[2 * e] = __uint_as_float(ws[e] << 16) * silu_fast(__uint_as_float(zs[e] << 16));
-        y[2 * e + 1] = __uint_as_float(ws[e] & 0xffff0000u) * silu_fast(__uint_as_float(zs[e] & 0xffff0000u));
-      }
-      reinterpret_cast<uint4 *>(gz)[(4 * tb + t) * 16 + cb] =
-          make_uint4(pack_h2(y[0], y[1]), pack_h2(y[2], y[3]), pack_h2(y[4], y[5]), pack_h2(y[6], y[7]));
-    }
-    return;
-  }
   const int ch0 = which == 0 ? head * HD : (which == 1 ? kd + head * HD : 2 * kd + head * HD);
   const bf16 *src = which == 0 ? A.q + head * HD : (which == 1 ? A.k + head * HD : A.v + head * HD);
   const size_t rstride = which == 2 ? (size_t)A.nv * HD : (size_t)kd;
@@ -891,14 +867,16 @@ done:
 constexpr int kOOffS = 0;         // state image (32 KiB)
 constexpr int kOOffQ = 32768;     // Q' image [2 kb][64 rows][128 B] (16 KiB)
 constexpr int kOOffOT = 49152;    // O_local fp32 [64 tokens][128 v] (32 KiB)
-constexpr int kOOffZ = 81920;     // norm_w * silu(z) fp16 [64][128], overwritten in place by the bf16 rows
+constexpr int kOOffZ = 81920;     // z bf16 [64 tokens][128], overwritten in place by the bf16 output rows
 constexpr int kOOffRed = 98304;   // fp32 [4][64] RMS partials, [64] rstd
 constexpr int kOOffBar = kOOffRed + 4 * 64 * 4 + 64 * 4;
 constexpr int kOutSmem = kOOffBar + 64 + 1024;
 
-// omap: out viewed as [Ttot][nv*dv] bf16, box [32 tokens][128 values].
+// omap: out viewed as [Ttot][nv*dv] bf16, box [32 tokens][128 values];
+// zmap: z viewed the same way, box [64 tokens][128 values].
 __global__ void __launch_bounds__(256, 2) output_kernel(LayerArgs A, Rows R, int Ttot, Ws W,
-                                                        const __grid_constant__ CUtensorMap omap) {
+                                                        const __grid_constant__ CUtensorMap omap,
+                                                        const __grid_constant__ CUtensorMap zmap) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   unsigned char *sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -943,7 +921,7 @@ __global__ void __launch_bounds__(256, 2) output_kernel(LayerArgs A, Rows R, int
     bulk_g2s(sm + kOOffQ, wq + 8192, 8192, bar_ld);           // Q' rows, column block 0
     bulk_g2s(sm + kOOffQ + 8192, wq + 24576, 8192, bar_ld);   // Q' rows, column block 1
     bulk_g2s(sm + kOOffOT, W.ot + sh * kRowF, 32768, bar_ld);
-    bulk_g2s(sm + kOOffZ, W.gz + sh * kImg, 16384, bar_ld);
+    tma_load_2d(sm + kOOffZ, &zmap, h * HD, start + t0, bar_ld);  // rows past the tensor read as zeros
   }
   if (!cta_wait(bar_ld, 0, A.status)) goto done;
   if (tid == 0) {
@@ -988,12 +966,13 @@ __global__ void __launch_bounds__(256, 2) output_kernel(LayerArgs A, Rows R, int
       rstd[t] = rsqrtf(ss / (float)HD + A.rms_eps);
     }
     named_sync(bar_id, 128);
-    const __half *gzs = reinterpret_cast<const __half *>(sm + kOOffZ);
-    bf16 *os = reinterpret_cast<bf16 *>(sm + kOOffZ);  // each element is read, then overwritten, by one thread
+    bf16 *os = reinterpret_cast<bf16 *>(sm + kOOffZ);  // each z is read, then overwritten, by one thread
+    const float wv = ldbf(A.norm_w + v);
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
       const int i = 32 * hh + e;
-      os[i * HD + v] = __float2bfloat16_rn(o[e] * rstd[i] * __half2float(gzs[i * HD + v]));
+      const float gz = wv * silu_fast(__bfloat162float(os[i * HD + v]));
+      os[i * HD + v] = __float2bfloat16_rn(o[e] * rstd[i] * gz);
     }
     fence_proxy_async_smem();
     named_sync(bar_id, 128);
@@ -1015,12 +994,12 @@ done:
   if (warp == 0) tmem_dealloc(tmem, 64);
 }
 
-// Tensor map of a bf16 [rows][cols] row-major tensor with [32][128] boxes.
+// Tensor map of a bf16 [rows][cols] row-major tensor with [box_rows][128] boxes.
 using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-gdn_status encode_rows_map(CUtensorMap *map, const void *base, int rows, int cols) {
+gdn_status encode_rows_map(CUtensorMap *map, const void *base, int rows, int cols, int box_rows) {
   static EncodeTiled encode = nullptr;
   if (!encode) {
     void *fn = nullptr;
@@ -1033,7 +1012,7 @@ gdn_status encode_rows_map(CUtensorMap *map, const void *base, int rows, int col
   }
   const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)HD, (cuuint32_t)(CH / 2)};
+  const cuuint32_t box[2] = {(cuuint32_t)HD, (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
   if (encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1082,17 +1061,18 @@ gdn_status launch_prefill_tc(const LayerArgs &A, void *ws, cudaStream_t stream) 
       return fail(GDN_ERR_CUDA, "prefill: cannot reserve shared memory");
     attr_set[dev.id] = true;
   }
-  tc::front_kernel<<<dim3(S, 2 * A.nk + 2 * A.nv), 256, 0, stream>>>(A, R, Ttot, W);
+  tc::front_kernel<<<dim3(S, 2 * A.nk + A.nv), 256, 0, stream>>>(A, R, Ttot, W);
   if (gdn_status st = check_launch("prefill front")) return st;
   // chunk, state and output start early (programmatic dependent launch) and
   // wait for their predecessor inside the kernel
-  CUtensorMap omap;
-  if (gdn_status st = tc::encode_rows_map(&omap, A.out, Ttot, A.nv * tc::HD)) return st;
+  CUtensorMap omap, zmap;
+  if (gdn_status st = tc::encode_rows_map(&omap, A.out, Ttot, A.nv * tc::HD, tc::CH / 2)) return st;
+  if (gdn_status st = tc::encode_rows_map(&zmap, A.z, Ttot, A.nv * tc::HD, tc::CH)) return st;
   if (tc::launch_dependent(tc::chunk_kernel, dim3(S, A.nv), tc::kChunkSmem, stream, A, R, Ttot, W) != cudaSuccess)
     return check_launch("prefill chunk");
   if (tc::launch_dependent(tc::state_kernel, dim3(A.B * A.nv), tc::kStateSmem, stream, A, R, Ttot, W) != cudaSuccess)
     return check_launch("prefill state");
-  if (tc::launch_dependent(tc::output_kernel, dim3(S, A.nv), tc::kOutSmem, stream, A, R, Ttot, W, omap) !=
+  if (tc::launch_dependent(tc::output_kernel, dim3(S, A.nv), tc::kOutSmem, stream, A, R, Ttot, W, omap, zmap) !=
       cudaSuccess)
     return check_launch("prefill output");
   return check_launch("prefill output");
