@@ -133,3 +133,43 @@ def test_split_call_equals_whole_call(oracle_mod):
     assert torch.equal(c1, c2)
     assert_state(S2, S1.cpu().double().numpy())
     assert_out(torch.cat(parts, 1), whole.cpu().double().numpy())
+
+
+@pytest.mark.parametrize("T", [1, 3, 64, 130])
+def test_tensor_core_path_short_and_ragged(oracle_mod, T):
+    """Head size 128 (the tcgen05 chunked path): rows shorter than the conv
+    width, exactly one chunk, and a ragged last chunk."""
+    shape = I.Shape(nk=2, nv=4, dk=128, dv=128)
+    d = I.decode_batch(seed=70 + T, B=3, shape=shape)
+    acts = I.activations(shape, 3, T, torch.Generator().manual_seed(71 + T))
+    w = _wd(d)
+    conv, S = dev(d["conv_state"]).clone(), dev(d["state"]).clone()
+    out = _prefill(shape, w, {n: dev(a) for n, a in acts.items()}, conv, S)
+    gdn.check_status()
+    ref = oracle_layer(oracle_mod, shape, d, acts, d["conv_state"], d["state"])
+    assert_out(out, ref["out"])
+    assert_state(S, ref["state"])
+    assert torch.equal(conv.cpu().double(), torch.from_numpy(ref["conv_state"]))
+
+
+@pytest.mark.parametrize("nk,nv", [(2, 2), (1, 4)])
+def test_tensor_core_path_gqa_groups(oracle_mod, nk, nv):
+    """Head size 128 with one value head per key head (G=1) and four (G=4):
+    the key-head mapping, the per-key-head K^T image and the conv-tail update
+    of the shared q|k channels."""
+    shape = I.Shape(nk=nk, nv=nv, dk=128, dv=128)
+    d = I.decode_batch(seed=80 + nv, B=2, shape=shape)
+    T = 100
+    acts = I.activations(shape, 2, T, torch.Generator().manual_seed(81 + nv))
+    mask = torch.ones((2, T))
+    mask[1, 61:] = 0
+    w = _wd(d)
+    conv, S = dev(d["conv_state"]).clone(), dev(d["state"]).clone()
+    out = _prefill(shape, w, {n: dev(a) for n, a in acts.items()}, conv, S, mask=dev(mask))
+    gdn.check_status()
+    ref = oracle_layer(oracle_mod, shape, d, acts, d["conv_state"], d["state"], mask=mask)
+    assert_out(out[0], ref["out"][0])
+    assert_out(out[1, :61], ref["out"][1, :61])
+    assert torch.count_nonzero(out[1, 61:].float()) == 0
+    assert_state(S, ref["state"])
+    assert torch.equal(conv.cpu().double(), torch.from_numpy(ref["conv_state"]))
