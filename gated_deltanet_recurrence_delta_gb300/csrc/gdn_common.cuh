@@ -126,4 +126,14 @@ __device__ __forceinline__ void bulk_g2s(void *smem_dst, const void *gmem_src, u
 // Streaming (evict-first) 16-byte store.
 __device__ __forceinline__ void st_cs(float4 *p, float4 v) { __stcs(p, v); }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start before its predecessor in the stream completes;
+// griddep_wait() blocks until the predecessor grid has completed and its memory
+// is visible (a no-op for an ordinary launch). griddep_trigger() lets this
+// grid's own dependent start once every CTA of this grid has issued it or
+// exited. Each kernel here triggers only after its own wait, so a dependent's
+// pre-wait code may rely on everything before this grid's predecessor.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 }  // namespace gdn

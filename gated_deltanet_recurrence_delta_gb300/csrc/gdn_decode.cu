@@ -163,9 +163,6 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(LayerArgs A) {
     }
   };
 
-  for (int i = tid; i < my_units && i < kSlotTable; i += blockDim.x) slot_tab[i] = resolve(i, true);
-  for (int i = kSlotTable + tid; i < my_units; i += blockDim.x) (void)resolve(i, true);
-  for (int c = tid; c < D; c += blockDim.x) fw[c] = ldbf(A.norm_w + c);
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
@@ -173,6 +170,11 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(LayerArgs A) {
     }
     fence_mbar_init();
   }
+  griddep_wait();  // the kernel before this call (e.g. the previous layer's) is complete
+  griddep_trigger();
+  for (int i = tid; i < my_units && i < kSlotTable; i += blockDim.x) slot_tab[i] = resolve(i, true);
+  for (int i = kSlotTable + tid; i < my_units; i += blockDim.x) (void)resolve(i, true);
+  for (int c = tid; c < D; c += blockDim.x) fw[c] = ldbf(A.norm_w + c);
   __syncthreads();
 
   if (warp == 8) {
@@ -311,7 +313,8 @@ static gdn_status launch_decode_t(const LayerArgs &A, cudaStream_t stream) {
     return fail(GDN_ERR_CUDA, "decode: kernel does not fit on an SM");
   const int n_units = A.B * A.nk;
   const int grid = n_units < dev.sms * per_sm ? n_units : dev.sms * per_sm;
-  decode_kernel<D, NS><<<grid, 288, S::kBytes, stream>>>(A);
+  if (launch_pdl(decode_kernel<D, NS>, dim3(grid), dim3(288), S::kBytes, stream, A) != cudaSuccess)
+    return check_launch("decode");
   return check_launch("decode");
 }
 

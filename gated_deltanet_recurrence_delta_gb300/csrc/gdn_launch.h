@@ -1,6 +1,8 @@
 // Host-side plumbing shared by the launchers of libgdn (not part of the C-ABI).
 #pragma once
 
+#include <utility>
+
 #include "gdn_common.cuh"
 
 namespace gdn {
@@ -23,6 +25,25 @@ const DeviceInfo &device_info();
 gdn_status fail(gdn_status code, const char *msg);
 // GDN_OK, or GDN_ERR_CUDA with the launch error of `what`.
 gdn_status check_launch(const char *what);
+
+// Launch with programmatic stream serialization: the kernel may start before
+// its predecessor in the stream completes and calls griddep_wait() before it
+// touches global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 gdn_status launch_decode(const LayerArgs &A, cudaStream_t stream);
 gdn_status launch_verify(const LayerArgs &A, float *ckpt_state, bf16 *ckpt_conv, cudaStream_t stream);

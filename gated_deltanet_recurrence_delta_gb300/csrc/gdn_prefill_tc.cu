@@ -43,8 +43,6 @@
 // operands (10-bit mantissa; bf16 would leave the final state ~3e-3 off in
 // relative Frobenius norm). With every product in plain fp16 the normalised
 // outputs of badly conditioned tokens drift by ~1e-2.
-#include <utility>
-
 #include "gdn_launch.h"
 #include "gdn_token.cuh"
 #include "gdn_umma.cuh"
@@ -192,6 +190,7 @@ __device__ __forceinline__ void umma_tile_split(uint32_t tmem_d, uint32_t a_hi, 
 
 __global__ void __launch_bounds__(256, 3) front_kernel(LayerArgs A, Rows R, int Ttot, Ws W) {
   __shared__ __align__(16) float Y[CH][HD];
+  griddep_wait();  // the kernel before this call (a previous layer call) is complete
   griddep_trigger();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int s = blockIdx.x, gi = blockIdx.y, kd = A.nk * HD;
@@ -1021,22 +1020,6 @@ gdn_status encode_rows_map(CUtensorMap *map, const void *base, int rows, int col
   return GDN_OK;
 }
 
-// Launch with programmatic stream serialization (256 threads per CTA).
-template <typename... KArgs, typename... Args>
-cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, size_t smem, cudaStream_t stream, Args &&...args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
-}
-
 }  // namespace tc
 
 size_t prefill_tc_workspace_bytes(int B, int T, int nk, int nv, bool packed) {
@@ -1061,18 +1044,18 @@ gdn_status launch_prefill_tc(const LayerArgs &A, void *ws, cudaStream_t stream) 
       return fail(GDN_ERR_CUDA, "prefill: cannot reserve shared memory");
     attr_set[dev.id] = true;
   }
-  tc::front_kernel<<<dim3(S, 2 * A.nk + A.nv), 256, 0, stream>>>(A, R, Ttot, W);
-  if (gdn_status st = check_launch("prefill front")) return st;
-  // chunk, state and output start early (programmatic dependent launch) and
-  // wait for their predecessor inside the kernel
+  if (launch_pdl(tc::front_kernel, dim3(S, 2 * A.nk + A.nv), dim3(256), 0, stream, A, R, Ttot, W) != cudaSuccess)
+    return check_launch("prefill front");
+  // every kernel starts early (programmatic dependent launch) and waits for
+  // its predecessor inside the kernel
   CUtensorMap omap, zmap;
   if (gdn_status st = tc::encode_rows_map(&omap, A.out, Ttot, A.nv * tc::HD, tc::CH / 2)) return st;
   if (gdn_status st = tc::encode_rows_map(&zmap, A.z, Ttot, A.nv * tc::HD, tc::CH)) return st;
-  if (tc::launch_dependent(tc::chunk_kernel, dim3(S, A.nv), tc::kChunkSmem, stream, A, R, Ttot, W) != cudaSuccess)
+  if (launch_pdl(tc::chunk_kernel, dim3(S, A.nv), dim3(256), tc::kChunkSmem, stream, A, R, Ttot, W) != cudaSuccess)
     return check_launch("prefill chunk");
-  if (tc::launch_dependent(tc::state_kernel, dim3(A.B * A.nv), tc::kStateSmem, stream, A, R, Ttot, W) != cudaSuccess)
+  if (launch_pdl(tc::state_kernel, dim3(A.B * A.nv), dim3(256), tc::kStateSmem, stream, A, R, Ttot, W) != cudaSuccess)
     return check_launch("prefill state");
-  if (tc::launch_dependent(tc::output_kernel, dim3(S, A.nv), tc::kOutSmem, stream, A, R, Ttot, W, omap, zmap) !=
+  if (launch_pdl(tc::output_kernel, dim3(S, A.nv), dim3(256), tc::kOutSmem, stream, A, R, Ttot, W, omap, zmap) !=
       cudaSuccess)
     return check_launch("prefill output");
   return check_launch("prefill output");

@@ -15,6 +15,8 @@ __global__ void __launch_bounds__(256) state_copy_kernel(const float4 *__restric
                                                          const int32_t *src_slot, const int32_t *dst_slot, int n_src,
                                                          int n_dst, size_t state_vec, size_t conv_vec,
                                                          unsigned int *status) {
+  griddep_wait();  // the kernel before this call (e.g. the verify that wrote the checkpoints) is complete
+  griddep_trigger();
   const int i = blockIdx.y;
   const int ss = src_slot[i], ds = dst_slot[i];
   if (ss == -1) return;  // nothing to commit for this pair
@@ -56,10 +58,11 @@ gdn_status launch_state_copy(const float *src_state, const bf16 *src_conv, float
   if (want > cap) want = cap;
   if (want < 1) want = 1;
   dim3 grid((unsigned)want, (unsigned)n);
-  state_copy_kernel<<<grid, 256, 0, stream>>>(
-      reinterpret_cast<const float4 *>(src_state), reinterpret_cast<const uint4 *>(src_conv),
-      reinterpret_cast<float4 *>(dst_state), reinterpret_cast<uint4 *>(dst_conv), src_slot, dst_slot, n_src, n_dst,
-      state_vec, conv_vec, dev.status);
+  if (launch_pdl(state_copy_kernel, grid, dim3(256), 0, stream, reinterpret_cast<const float4 *>(src_state),
+                 reinterpret_cast<const uint4 *>(src_conv), reinterpret_cast<float4 *>(dst_state),
+                 reinterpret_cast<uint4 *>(dst_conv), src_slot, dst_slot, n_src, n_dst, state_vec, conv_vec,
+                 dev.status) != cudaSuccess)
+    return check_launch("state_copy");
   return check_launch("state_copy");
 }
 

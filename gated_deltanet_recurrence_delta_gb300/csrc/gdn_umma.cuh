@@ -138,16 +138,6 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int x, int 
                : "memory");
 }
 
-// Programmatic dependent launch: a kernel launched with programmatic stream
-// serialization may start before its predecessor in the stream completes;
-// griddep_wait() blocks until the predecessor grid has completed and its memory
-// is visible (a no-op for an ordinary launch). griddep_trigger() lets this
-// grid's own dependent start once every CTA of this grid has issued it or
-// exited. Each kernel here triggers only after its own wait, so a dependent's
-// pre-wait code may rely on everything before this grid's predecessor.
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void griddep_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-
 __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
   const __half2 h = __floats2half2_rn(a, b);
   return *reinterpret_cast<const uint32_t *>(&h);

@@ -217,6 +217,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 4)
   // tokens (half 0: the q block, half 1: the k block, plus its own 64 value
   // channels), taps, output gate, norm weight, mask, gates; then the slot and
   // the state slice and conv tail it selects.
+  griddep_wait();  // the kernel before this call (e.g. the previous commit) is complete
+  griddep_trigger();
   const int slot_raw = A.state_idx ? __ldg(A.state_idx + b) : b;  // used only after the loads below
   const int cq = tid % NQ, grp = tid / NQ;
   const int NR = T + KC;
@@ -489,7 +491,9 @@ static gdn_status launch_verify_t(const LayerArgs &A, float *ckpt_state, bf16 *c
 gdn_status launch_verify(const LayerArgs &A, float *ckpt_state, bf16 *ckpt_conv, cudaStream_t stream) {
   switch (A.D) {
     case 128:
-      verify_split_kernel<<<2 * A.B * A.nv, 128, 0, stream>>>(A, ckpt_state, ckpt_conv);
+      if (launch_pdl(verify_split_kernel, dim3(2 * A.B * A.nv), dim3(128), 0, stream, A, ckpt_state, ckpt_conv) !=
+          cudaSuccess)
+        return check_launch("verify");
       return check_launch("verify");
     case 64: return launch_verify_t<64>(A, ckpt_state, ckpt_conv, stream);
     case 32: return launch_verify_t<32>(A, ckpt_state, ckpt_conv, stream);
