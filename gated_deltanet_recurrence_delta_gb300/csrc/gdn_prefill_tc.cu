@@ -882,28 +882,19 @@ __global__ void __launch_bounds__(256, 2) output_kernel(LayerArgs A, Rows R, int
   float *red = reinterpret_cast<float *>(sm + kOOffRed);  // [4][64]
   float *rstd = red + 256;                                // [64]
   uint64_t *bar_ld = reinterpret_cast<uint64_t *>(sm + kOOffBar);
-  uint64_t *bar_mma = bar_ld + 1;
+  uint64_t *bar_s = bar_ld + 1;
+  uint64_t *bar_mma = bar_ld + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_mma + 1);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int s = blockIdx.x, h = blockIdx.y;
   int r, c;
   R.locate(s, Ttot, r, c);
-  griddep_wait();  // the state kernel's images and row lengths are complete
-  griddep_trigger();
   if (r < 0) return;
-  const int Lr = W.lr[r];
-  if (Lr < 0) return;  // the row was rejected (its status is set)
   const int start = R.start(r), len = R.len(r), t0 = c * CH;
-  const int ntok = min(CH, len - t0), nreal = max(0, min(CH, Lr - t0));
-  // padded tokens of this chunk: zeros
-  for (int e = nreal * 16 + tid; e < ntok * 16; e += 256)
-    reinterpret_cast<uint4 *>(A.out + ((size_t)(start + t0 + e / 16) * A.nv + h) * HD)[e % 16] =
-        make_uint4(0u, 0u, 0u, 0u);
-  if (nreal == 0) return;
-
   if (tid == 0) {
     mbar_init(bar_ld, 1);
+    mbar_init(bar_s, 1);
     mbar_init(bar_mma, 1);
     fence_mbar_init();
   }
@@ -912,17 +903,36 @@ __global__ void __launch_bounds__(256, 2) output_kernel(LayerArgs A, Rows R, int
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const size_t sh = (size_t)s * A.nv + h;
+  // before the wait: what the chunk kernel (complete before the state kernel
+  // started) and the caller produced -- Q', O_local, z
   if (tid == 0) {
-    const size_t sh = (size_t)s * A.nv + h;
     const unsigned char *wq = reinterpret_cast<const unsigned char *>(W.wq + sh * kWQ);
-    mbar_arrive_expect_tx(bar_ld, 32768 + 16384 + 32768 + 16384);
-    bulk_g2s(sm + kOOffS, W.simg + sh * kWQ, 32768, bar_ld);
+    mbar_arrive_expect_tx(bar_ld, 16384 + 32768 + 16384);
     bulk_g2s(sm + kOOffQ, wq + 8192, 8192, bar_ld);           // Q' rows, column block 0
     bulk_g2s(sm + kOOffQ + 8192, wq + 24576, 8192, bar_ld);   // Q' rows, column block 1
     bulk_g2s(sm + kOOffOT, W.ot + sh * kRowF, 32768, bar_ld);
     tma_load_2d(sm + kOOffZ, &zmap, h * HD, start + t0, bar_ld);  // rows past the tensor read as zeros
   }
+  griddep_wait();  // the state kernel's images and row lengths are complete
+  griddep_trigger();
+  const int Lr = W.lr[r];  // < 0: the row was rejected (its status is set)
+  const int ntok = min(CH, len - t0), nreal = Lr < 0 ? 0 : max(0, min(CH, Lr - t0));
+  // padded tokens of this chunk: zeros
+  if (Lr >= 0)
+    for (int e = nreal * 16 + tid; e < ntok * 16; e += 256)
+      reinterpret_cast<uint4 *>(A.out + ((size_t)(start + t0 + e / 16) * A.nv + h) * HD)[e % 16] =
+          make_uint4(0u, 0u, 0u, 0u);
+  if (nreal == 0) {  // nothing to compute: let the loads in flight land, then leave
+    (void)cta_wait(bar_ld, 0, A.status);
+    goto done;
+  }
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar_s, 32768);
+    bulk_g2s(sm + kOOffS, W.simg + sh * kWQ, 32768, bar_s);
+  }
   if (!cta_wait(bar_ld, 0, A.status)) goto done;
+  if (!cta_wait(bar_s, 0, A.status)) goto done;
   if (tid == 0) {
     tc_fence_after();
     umma_tile(tmem, smem_u32(sm + kOOffS), 128, smem_u32(sm + kOOffQ), 64, 128, umma_idesc_f16(128, 64), false);
