@@ -326,8 +326,8 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
   float *sG = sb + 64;                                   // inclusive prefix of g
   float *sgam = sG + 64;                                 // exp(G_j)
   float *sec = sgam + 64;                                // exp(G_C - G_j)
-  uint64_t *bar_ld = reinterpret_cast<uint64_t *>(sec + 64);
-  uint64_t *bar_mma = bar_ld + 1;
+  uint64_t *bar_ld = reinterpret_cast<uint64_t *>(sec + 64);  // [0]: K|Q tiles, [1]: K^T|V^T tiles
+  uint64_t *bar_mma = bar_ld + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_mma + 1);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -339,7 +339,8 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
   const int nvalid = min(CH, len - c * CH);
 
   if (tid == 0) {
-    mbar_init(bar_ld, 1);
+    mbar_init(&bar_ld[0], 1);
+    mbar_init(&bar_ld[1], 1);
     mbar_init(bar_mma, 1);
     fence_mbar_init();
   }
@@ -351,19 +352,22 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
 
   griddep_wait();  // the front kernel's images are complete
   griddep_trigger();
-  if (tid == 0) {
-    mbar_arrive_expect_tx(bar_ld, 131072);
+  if (tid == 0) {  // the K|Q tiles first (the first product needs them), then K^T|V^T
+    mbar_arrive_expect_tx(&bar_ld[0], 65536);
     for (int part = 0; part < 2; ++part) {
       const __half *ki = W.kimg + ((size_t)s * A.nk + kh) * 2 * kImg + part * kImg;
       const __half *qi = W.qimg + ((size_t)s * A.nk + kh) * 2 * kImg + part * kImg;
       unsigned char *dst = part ? KQL : KQH;
-      bulk_g2s(dst, ki, 8192, bar_ld);                 // K, column block 0
-      bulk_g2s(dst + 8192, qi, 8192, bar_ld);          // Q, column block 0
-      bulk_g2s(dst + 16384, ki + 4096, 8192, bar_ld);  // K, column block 1
-      bulk_g2s(dst + 24576, qi + 4096, 8192, bar_ld);  // Q, column block 1
-      unsigned char *b2 = part ? B2L : B2H;            // K^T rows 0-127, V^T rows 128-255
-      bulk_g2s(b2, W.ktimg + ((size_t)s * A.nk + kh) * 2 * kImg + part * kImg, 16384, bar_ld);
-      bulk_g2s(b2 + 16384, W.vtimg + ((size_t)s * A.nv + h) * 2 * kImg + part * kImg, 16384, bar_ld);
+      bulk_g2s(dst, ki, 8192, &bar_ld[0]);                 // K, column block 0
+      bulk_g2s(dst + 8192, qi, 8192, &bar_ld[0]);          // Q, column block 0
+      bulk_g2s(dst + 16384, ki + 4096, 8192, &bar_ld[0]);  // K, column block 1
+      bulk_g2s(dst + 24576, qi + 4096, 8192, &bar_ld[0]);  // Q, column block 1
+    }
+    mbar_arrive_expect_tx(&bar_ld[1], 65536);
+    for (int part = 0; part < 2; ++part) {
+      unsigned char *b2 = part ? B2L : B2H;  // K^T rows 0-127, V^T rows 128-255
+      bulk_g2s(b2, W.ktimg + ((size_t)s * A.nk + kh) * 2 * kImg + part * kImg, 16384, &bar_ld[1]);
+      bulk_g2s(b2 + 16384, W.vtimg + ((size_t)s * A.nv + h) * 2 * kImg + part * kImg, 16384, &bar_ld[1]);
     }
   }
   // gates of the chunk's tokens; padding and tokens past the row end get g = beta = 0
@@ -401,7 +405,7 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
       sec[j] = __expf(GC - sG[j]);
     }
   }
-  if (!cta_wait(bar_ld, 0, A.status)) goto done;
+  if (!cta_wait(&bar_ld[0], 0, A.status)) goto done;
 
   // ---- [K; Q] K^T -> TMEM columns [0, 64)
   if (tid == 0) {
@@ -581,6 +585,7 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
 
   // ---- [T; R] diag(beta gamma) K -> TMEM columns [0, 128) (W | P W) and
   //      [T; R] diag(beta) V -> columns [128, 256) (U | P U)
+  if (!cta_wait(&bar_ld[1], 0, A.status)) goto done;  // long landed: loaded during the steps above
   if (tid == 0) {
     tc_fence_after();
     umma_tile_split(tmem, smem_u32(TRH), smem_u32(TRL), 128, smem_u32(B2H), smem_u32(B2L), 256, 64,
@@ -631,15 +636,20 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
       }
     }
     fence_proxy_async_smem();
-  }
-  __syncthreads();
-  if (tid == 0) {
-    const size_t sh = (size_t)s * A.nv + h;
-    bulk_s2g(W.wq + sh * kWQ, KQH, 32768);
-    bulk_s2g(W.ut + sh * kRowF, sm + kOffB2H, 32768);
-    bulk_s2g(W.ot + sh * kRowF, sm + kOffB2H + 32768, 32768);
-    bulk_commit();
-    bulk_wait_read_all();  // shared memory may be released; the writes land before the grid completes
+    // each warp group stores its own tiles as soon as its 4 warps are done:
+    // group 0 the W|Q' image, group 1 the U and O_local rows
+    named_sync(1 + hh, 128);
+    if (tid == 128 * hh) {
+      const size_t sh = (size_t)s * A.nv + h;
+      if (hh == 0) {
+        bulk_s2g(W.wq + sh * kWQ, KQH, 32768);
+      } else {
+        bulk_s2g(W.ut + sh * kRowF, sm + kOffB2H, 32768);
+        bulk_s2g(W.ot + sh * kRowF, sm + kOffB2H + 32768, 32768);
+      }
+      bulk_commit();
+      bulk_wait_read_all();  // shared memory may be released; the writes land before the grid completes
+    }
   }
 done:
   tc_fence_before();
