@@ -90,7 +90,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
         except OSError:
@@ -214,7 +214,7 @@ def decode_bytes(s, B):
     return state + B * per_row + weights
 
 
-def phase_decode(gdn, world, steps, warmup, peak_hbm, e2e=True):
+def phase_decode(gdn, world, steps, warmup, peak_hbm, local=0, e2e=True):
     s, B = I.QWEN35_9B, 64
     per_set = B * s.nv * s.dk * s.dv * 4
     n_sets = max(4, math.ceil(3 * L2_BYTES / per_set))
@@ -230,7 +230,8 @@ def phase_decode(gdn, world, steps, warmup, peak_hbm, e2e=True):
         d = sets[i % n_sets]
         gdn.decode_step(d["dims"], d["inp"], d["conv_state"], d["state"], d["out"])
 
-    ms = timed(world, steps, warmup, step)
+    with ClockSampler(local) as clk:  # around the warm-up and the timed region only
+        ms = timed(world, steps, warmup, step)
     kms = ms  # one launch per step and nothing else: the step time is the kernel's average launch duration
     nbytes = decode_bytes(s, B)
     res = {"tokens_per_s": B * world / (ms * 1e-3), "ms_per_step": ms, "tokens_per_step": B,
@@ -238,7 +239,8 @@ def phase_decode(gdn, world, steps, warmup, peak_hbm, e2e=True):
            "roofline": {"bound": "hbm", "achieved": nbytes / (kms * 1e-3) / 1e9, "peak": peak_hbm,
                         "unit": "GB/s", "frac": nbytes / (kms * 1e-3) / 1e9 / peak_hbm,
                         "traffic": dram_traffic("decode_kernel"), "algorithmic_bytes": nbytes},
-           "l2": f"inputs larger than L2: {n_sets} rotating layer buffer sets of {per_set / 2**20:.0f} MiB state"}
+           "l2": f"inputs larger than L2: {n_sets} rotating layer buffer sets of {per_set / 2**20:.0f} MiB state",
+           "clocks": clk.summary()}
     if e2e:
         # end to end through the C-ABI: the step's activations (q, k, v, z, a,
         # b) sit in one pinned host buffer and go to the device in one copy,
@@ -432,7 +434,7 @@ def oracle_decode_rate(seconds=10.0, max_steps=None):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
     ap.add_argument("--phases", default="decode,verify,prefill,varlen")
@@ -466,15 +468,14 @@ def main():
     peak_hbm, peak_tf, peak_tf_sus, peak_src = peaks()
     phases = [p for p in args.phases.split(",") if p]
     results = {}
-    with ClockSampler(local) as clk:
-        results["decode"] = phase_decode(gdn, world, steps, warmup, peak_hbm)
-    clocks = clk.summary()
+    results["decode"] = phase_decode(gdn, world, steps, warmup, peak_hbm, local=local)
+    clocks = results["decode"].pop("clocks")
     if "verify" in phases:
         results["verify"] = phase_verify(gdn, world, steps, warmup, peak_hbm)
     if "prefill" in phases:
-        results["prefill"] = phase_prefill(gdn, world, max(3, steps // 4), warmup, peak_tf_sus)
+        results["prefill"] = phase_prefill(gdn, world, max(3, steps // 400), warmup, peak_tf_sus)
     if "varlen" in phases:
-        results["varlen"] = phase_varlen(gdn, world, max(2, steps // 10), 3, peak_tf_sus)
+        results["varlen"] = phase_varlen(gdn, world, max(2, steps // 1000), 3, peak_tf_sus)
     gdn.check_status()
 
     dec = results["decode"]

@@ -51,7 +51,8 @@ def test_decode_batch_qwen_layout(oracle_mod):
     assert torch.equal(conv.cpu().double(), torch.from_numpy(ref["conv_state"]))
 
 
-@pytest.mark.parametrize("shape", [I.TINY, I.Shape(nk=4, nv=8, dk=64, dv=64), I.Shape(nk=2, nv=2, dk=128, dv=128)])
+@pytest.mark.parametrize("shape", [I.TINY, I.Shape(nk=4, nv=8, dk=64, dv=64), I.Shape(nk=2, nv=2, dk=128, dv=128),
+                                   I.Shape(nk=1, nv=4, dk=128, dv=128)])
 def test_decode_head_sizes(oracle_mod, shape):
     d = I.decode_batch(seed=11, B=5, shape=shape)
     w, acts = _wd(d), _acts(d)
@@ -91,7 +92,7 @@ def test_decode_mask_and_state_pool(oracle_mod):
         assert torch.equal(S[slot].cpu(), S0[slot]) and torch.equal(conv[slot].cpu(), conv0[slot])
 
 
-@pytest.mark.parametrize("shape", [I.TINY, I.QWEN35_9B])
+@pytest.mark.parametrize("shape", [I.TINY, I.QWEN35_9B, I.Shape(nk=1, nv=4, dk=128, dv=128)])
 def test_verify_checkpoints_equal_decode_steps_bitwise(shape):
     """Verify checkpoint t == the state after t+1 decode steps, bit for bit; the
     conv checkpoint == the decoded conv tail; the outputs are identical."""
