@@ -8,16 +8,17 @@
 //     alone (no cross-CTA hazard on the in-place tail);
 //   * each value head's state (one contiguous D*D fp32 block) is streamed into
 //     a ring of NS shared-memory stages by one bulk copy (cp.async.bulk, TMA
-//     engine) completing on a "full" mbarrier; a dedicated producer warp
-//     refills a stage as soon as the 8 compute warps have taken their slices
-//     into registers ("empty" mbarrier), so NS-1 heads are in flight while one
-//     is computed; the compute warps synchronise among themselves only
-//     (barrier 1), never with the producer;
+//     engine) completing on a "full" mbarrier; the 8 compute warps write the
+//     updated state back into the same stage and arrive on its "empty"
+//     mbarrier; a dedicated producer warp then bulk-stores the stage to the
+//     state slot and, once that copy has read it, refills the stage, so NS-1
+//     heads are in flight while one is computed and the compute warps never
+//     issue the 64 KiB of global stores themselves; the compute warps
+//     synchronise among themselves only (barrier 1), never with the producer;
 //   * the small per-unit inputs (token channels, conv tail, conv taps, z,
 //     gates) are loaded into registers one unit ahead, so their latency hides
 //     behind the current unit's state stream; row slots are resolved once
-//     into a shared table;
-//   * the new state goes straight from registers to HBM with streaming stores.
+//     into a shared table.
 // The per-token arithmetic is the shared code of gdn_token.cuh.
 #include "gdn_launch.h"
 #include "gdn_token.cuh"
@@ -180,13 +181,29 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(LayerArgs A) {
   if (warp == 8) {
     // ---- producer: stream every task's state into the stage ring
     if (lane == 0) {
-      for (int n = 0; n < n_tasks; ++n) {
-        if (n >= NS && !mbar_wait_bounded(&empty[n % NS], (uint32_t)(((n / NS) - 1) & 1))) {
-          set_status(A.status, GDN_ERR_TIMEOUT);
-          break;
+      // task m's updated state is back in its stage: bulk-store it to the slot
+      auto store_back = [&](int m) -> bool {
+        if (!mbar_wait_bounded(&empty[m % NS], (uint32_t)((m / NS) & 1))) return false;
+        const int u = (int)blockIdx.x + (m / G) * (int)gridDim.x;
+        const int h = (u % A.nk) * G + m % G;
+        const int slot = unit_slot(m / G);
+        if (slot >= 0) {
+          bulk_s2g(A.state + ((size_t)slot * A.nv + h) * D * D, stage + (m % NS) * S::kStage, D * D * 4);
+          bulk_commit();
         }
-        issue(n);
+        return true;
+      };
+      bool ok = true;
+      for (int n = 0; n < n_tasks && ok; ++n) {
+        if (n >= NS) {
+          ok = store_back(n - NS);
+          bulk_wait_read_all();  // the stage may be refilled
+        }
+        if (ok) issue(n);
       }
+      for (int m = n_tasks - NS < 0 ? 0 : n_tasks - NS; m < n_tasks && ok; ++m) ok = store_back(m);
+      if (!ok) set_status(A.status, GDN_ERR_TIMEOUT);
+      bulk_wait_read_all();  // shared memory stays valid until every store has read it
     }
     return;
   }
@@ -281,13 +298,15 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(LayerArgs A) {
       float4 s[L::RPT];
 #pragma unroll
       for (int r = 0; r < L::RPT; ++r) s[r] = st[(grp + r * L::NG) * L::TPR + cq];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[n % NS]);  // this warp's slice is in registers
       float4 o;
       state_step<D>(s, fq, fk, fv + j * D, fdecay[j], fbeta[j], fbkq[j], red, tid, o, csync);
-      float4 *gs = reinterpret_cast<float4 *>(A.state + ((size_t)slot * A.nv + h) * D * D);
+      // the updated slice back into the stage; the producer stores the stage
+      float4 *sw = reinterpret_cast<float4 *>(stage + (n % NS) * S::kStage);
 #pragma unroll
-      for (int r = 0; r < L::RPT; ++r) st_cs(gs + (grp + r * L::NG) * L::TPR + cq, s[r]);
+      for (int r = 0; r < L::RPT; ++r) sw[(grp + r * L::NG) * L::TPR + cq] = s[r];
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[n % NS]);
       if (warp == 7) rmsnorm_store_smem<D>(o, lane, fz + j * D, fw, A.rms_eps, out);
     } else {
       if (lane == 0) mbar_arrive(&empty[n % NS]);

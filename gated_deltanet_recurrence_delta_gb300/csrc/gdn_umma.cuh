@@ -110,18 +110,6 @@ __device__ __forceinline__ uint32_t tmem_at(uint32_t base, int q, int col) {
   return base + ((uint32_t)(32 * q) << 16) + (uint32_t)col;
 }
 
-// Bulk shared -> global copy (16-byte aligned, size % 16 == 0), tracked as a bulk group.
-__device__ __forceinline__ void bulk_s2g(void *gmem_dst, const void *smem_src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gmem_dst),
-               "r"(smem_u32(smem_src)), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-// The shared-memory sources of this thread's bulk stores may be overwritten.
-__device__ __forceinline__ void bulk_wait_read_all() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
 
 // 2-D tensor-map (TMA) tile load / store; coordinates in elements (x inner).
 __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
