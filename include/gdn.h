@@ -21,6 +21,14 @@
  *     stream) and is asynchronous: no entry point synchronises, except
  *     gdn_check_status. No entry point reads device memory on the host, so
  *     each call can be captured in a CUDA graph.
+ *   - Kernels are launched with programmatic stream serialization: a kernel
+ *     may start while the kernel before it in the stream is finishing, and it
+ *     waits (griddepcontrol.wait) for that kernel to complete before it reads
+ *     or writes any tensor; it then lets the next kernel in the stream start
+ *     early (griddepcontrol.launch_dependents). Stream order is preserved for
+ *     ordinary kernels; a caller's kernel that itself opts into programmatic
+ *     launch after a libgdn call must wait before reading libgdn's outputs, as
+ *     with any programmatic dependent.
  *   - Arguments are validated on the host before anything is launched; an
  *     invalid call returns an error status, launches nothing and leaves every
  *     buffer untouched. gdn_last_error() then describes it.
