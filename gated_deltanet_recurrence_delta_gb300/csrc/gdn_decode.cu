@@ -319,12 +319,13 @@ template <int D, int NS>
 static gdn_status launch_decode_t(const LayerArgs &A, cudaStream_t stream) {
   using S = DecodeSmem<D, NS>;
   const DeviceInfo &dev = device_info();
-  static bool attr_set[kMaxDevices] = {};
-  if (!attr_set[dev.id]) {
+  // set once per device; concurrent first calls may both set it (idempotent)
+  static std::atomic<bool> attr_set[kMaxDevices];
+  if (!attr_set[dev.id].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(decode_kernel<D, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::kBytes) !=
         cudaSuccess)
       return fail(GDN_ERR_CUDA, "decode: cannot reserve shared memory");
-    attr_set[dev.id] = true;
+    attr_set[dev.id].store(true, std::memory_order_release);
   }
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<D, NS>, 288, S::kBytes) != cudaSuccess ||

@@ -1,6 +1,7 @@
 // Host-side plumbing shared by the launchers of libgdn (not part of the C-ABI).
 #pragma once
 
+#include <atomic>
 #include <utility>
 
 #include "gdn_common.cuh"

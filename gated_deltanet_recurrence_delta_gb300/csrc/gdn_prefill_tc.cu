@@ -1019,16 +1019,17 @@ using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t,
                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 gdn_status encode_rows_map(CUtensorMap *map, const void *base, int rows, int cols, int box_rows) {
-  static EncodeTiled encode = nullptr;
-  if (!encode) {
+  // the driver entry point, looked up once (thread-safe static initialisation)
+  static const EncodeTiled encode = []() -> EncodeTiled {
     void *fn = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
             cudaSuccess ||
-        q != cudaDriverEntryPointSuccess || !fn)
-      return fail(GDN_ERR_CUDA, "prefill: cuTensorMapEncodeTiled is unavailable");
-    encode = reinterpret_cast<EncodeTiled>(fn);
-  }
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiled>(fn);
+  }();
+  if (!encode) return fail(GDN_ERR_CUDA, "prefill: cuTensorMapEncodeTiled is unavailable");
   const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
   const cuuint32_t box[2] = {(cuuint32_t)HD, (cuuint32_t)box_rows};
@@ -1053,8 +1054,9 @@ gdn_status launch_prefill_tc(const LayerArgs &A, void *ws, cudaStream_t stream) 
   tc::Rows R{A.B, A.T, packed ? 0 : (A.T + tc::CH - 1) / tc::CH, A.cu_seqlens};
   tc::Ws W = tc::carve(ws, A.B, A.T, A.nk, A.nv, packed);
   const DeviceInfo &dev = device_info();
-  static bool attr_set[kMaxDevices] = {};
-  if (!attr_set[dev.id]) {
+  // set once per device; concurrent first calls may both set it (idempotent)
+  static std::atomic<bool> attr_set[kMaxDevices];
+  if (!attr_set[dev.id].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(tc::chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kChunkSmem) !=
             cudaSuccess ||
         cudaFuncSetAttribute(tc::state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kStateSmem) !=
@@ -1062,7 +1064,7 @@ gdn_status launch_prefill_tc(const LayerArgs &A, void *ws, cudaStream_t stream) 
         cudaFuncSetAttribute(tc::output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kOutSmem) !=
             cudaSuccess)
       return fail(GDN_ERR_CUDA, "prefill: cannot reserve shared memory");
-    attr_set[dev.id] = true;
+    attr_set[dev.id].store(true, std::memory_order_release);
   }
   if (launch_pdl(tc::front_kernel, dim3(S, 2 * A.nk + A.nv), dim3(256), 0, stream, A, R, Ttot, W) != cudaSuccess)
     return check_launch("prefill front");

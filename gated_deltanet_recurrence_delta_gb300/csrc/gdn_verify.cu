@@ -477,12 +477,13 @@ template <int D>
 static gdn_status launch_verify_t(const LayerArgs &A, float *ckpt_state, bf16 *ckpt_conv, cudaStream_t stream) {
   using S = VerifySmem<D>;
   const DeviceInfo &dev = device_info();
-  static bool attr_set[kMaxDevices] = {};
-  if (!attr_set[dev.id]) {
+  // set once per device; concurrent first calls may both set it (idempotent)
+  static std::atomic<bool> attr_set[kMaxDevices];
+  if (!attr_set[dev.id].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(verify_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::kBytes) !=
         cudaSuccess)
       return fail(GDN_ERR_CUDA, "verify: cannot reserve shared memory");
-    attr_set[dev.id] = true;
+    attr_set[dev.id].store(true, std::memory_order_release);
   }
   verify_kernel<D><<<A.B * A.nv, 256, S::kBytes, stream>>>(A, ckpt_state, ckpt_conv);
   return check_launch("verify");
