@@ -9,7 +9,7 @@ import torch
 
 from gated_deltanet_recurrence_delta_gb300 import gdn
 from gated_deltanet_recurrence_delta_gb300 import inputs as I
-from tests.gpu_cases import ACTS, WEIGHTS, assert_out, assert_state, dev, dims, inputs
+from tests.gpu_cases import ACTS, WEIGHTS, dev, dims, inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -23,8 +23,10 @@ def _built():
     gdn.load_library()
 
 
-def test_static_scratch_matches_workspace_path():
-    shape = I.TINY
+@pytest.mark.parametrize("shape", [I.TINY, I.Shape(nk=2, nv=4, dk=128, dv=128)])
+def test_static_scratch_matches_workspace_path(shape):
+    """Both prefill paths (head size 32: CUDA cores; 128: tensor cores): the
+    static scratch gives the results of a caller workspace, bit for bit."""
     d = I.decode_batch(seed=60, B=3, shape=shape)
     g = torch.Generator().manual_seed(61)
     calls = [I.activations(shape, 3, T, g) for T in (100, 37)]
@@ -43,8 +45,8 @@ def test_static_scratch_matches_workspace_path():
         gdn.prefill_chunked(dm, inputs(w, a, mask=m), ref_conv, ref_S, out_ref, gdn.workspace(dm))
         gdn.prefill_chunked_static_scratch(dm, inputs(w, a, mask=m), new_conv, new_S, out_new)
         gdn.check_status()
-        assert_out(out_new, out_ref.double().cpu().numpy())
-        assert_state(new_S, ref_S.double().cpu().numpy())
+        assert torch.equal(out_new, out_ref)
+        assert torch.equal(new_S, ref_S)
         assert torch.equal(new_conv, ref_conv)
 
 
