@@ -488,7 +488,8 @@ def main():
     line = {
         "metric": METRIC, "value": dec["tokens_per_s"], "unit": "tokens/s", "n_gpus": world, "steps": steps,
         "warmup": warmup, "ms_per_step": dec["ms_per_step"], "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32 state, bf16 activations", "data": "synthetic",
+        "vs_baseline": None, "dtype": "f32",
+        "dtype_note": "fp32 state and arithmetic; bf16 activations, conv tail and outputs", "data": "synthetic",
         "config": {"workload": "decode step: B=64 rows, T=1, 16 key / 32 value heads, d=128, fp32 state "
                                "(Qwen3.5-9B-like GDN layer)",
                    "global_batch": 64 * world, "seq_len": 1, "parallelism": f"dp{world} (rows, no collective)",
