@@ -104,9 +104,13 @@ def make_dims(B, T, nk, nv, dk, dv, n_slots, conv_k=4, scale=None, l2_eps=1e-6, 
 
 def make_inputs(q, k, v, z, a, b, A_log, dt_bias, conv_w, norm_w, mask=None, cu_seqlens=None,
                 state_idx=None) -> Inputs:
-    return Inputs(q=_ptr(q), k=_ptr(k), v=_ptr(v), z=_ptr(z), a=_ptr(a), b=_ptr(b), A_log=_ptr(A_log),
-                  dt_bias=_ptr(dt_bias), conv_w=_ptr(conv_w), norm_w=_ptr(norm_w), mask=_ptr(mask),
-                  cu_seqlens=_ptr(cu_seqlens), state_idx=_ptr(state_idx))
+    """The inputs struct of raw device pointers. It keeps references to the
+    tensors, so they (and their device memory) live as long as the struct."""
+    inp = Inputs(q=_ptr(q), k=_ptr(k), v=_ptr(v), z=_ptr(z), a=_ptr(a), b=_ptr(b), A_log=_ptr(A_log),
+                 dt_bias=_ptr(dt_bias), conv_w=_ptr(conv_w), norm_w=_ptr(norm_w), mask=_ptr(mask),
+                 cu_seqlens=_ptr(cu_seqlens), state_idx=_ptr(state_idx))
+    inp._tensors = (q, k, v, z, a, b, A_log, dt_bias, conv_w, norm_w, mask, cu_seqlens, state_idx)
+    return inp
 
 
 def decode_step(dims: Dims, inputs: Inputs, conv_state, recurrent_state, out, stream=None):
