@@ -368,7 +368,8 @@ def phase_prefill(gdn, world, steps, warmup, peak_tf):
            "ms_per_512_call": ms / (T // call), "launches_per_step": 4 * (T // call),
            "roofline": {"bound": "tensor", "kernel": "front+chunk+state+output", "achieved": flops / (kms * 1e-3) / 1e12, "peak": peak_tf,
                         "unit": "TFLOP/s", "frac": flops / (kms * 1e-3) / 1e12 / peak_tf,
-                        "traffic": None, "algorithmic_flops_per_token": prefill_flops_per_token(s)}}
+                        "traffic": dram_traffic("prefill_call_512"), "traffic_scope": "one 512-token call (four kernels)",
+                        "algorithmic_flops_per_token": prefill_flops_per_token(s)}}
     del d, calls, ws
     torch.cuda.empty_cache()
     return res
