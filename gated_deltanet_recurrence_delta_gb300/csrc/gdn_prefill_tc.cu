@@ -188,11 +188,15 @@ __device__ __forceinline__ void umma_tile_split(uint32_t tmem_d, uint32_t a_hi, 
 
 // ------------------------------------------------------------ front end
 
-__global__ void __launch_bounds__(256, 3) front_kernel(LayerArgs A, Rows R, int Ttot, Ws W) {
-  __shared__ __align__(16) float Y[CH][HD];
+// One CTA per (chunk slot, q/k/v head): 256 threads, thread = 8 channels (cb)
+// x 4 tokens (tb), all in registers. A token's 128 channels sit in one
+// half-warp, so its L2 norm is a 16-lane butterfly; warp w holds tokens
+// 8w .. 8w+7, which is one 16-byte chunk column of the transposed images, so
+// they are built by one exchange between the two half-warps.
+__global__ void __launch_bounds__(256, 4) front_kernel(LayerArgs A, Rows R, int Ttot, Ws W) {
   griddep_wait();  // the kernel before this call (a previous layer call) is complete
   griddep_trigger();
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, half = lane >> 4;
   const int s = blockIdx.x, gi = blockIdx.y, kd = A.nk * HD;
   int r, c;
   R.locate(s, Ttot, r, c);
@@ -201,86 +205,88 @@ __global__ void __launch_bounds__(256, 3) front_kernel(LayerArgs A, Rows R, int 
   const int which = gi < A.nk ? 0 : (gi < 2 * A.nk ? 1 : 2);
   const int head = which == 0 ? gi : (which == 1 ? gi - A.nk : gi - 2 * A.nk);
   const int slot = row_slot(A, r);
-  // thread -> 8 channels (cb) x 4 tokens (tb): 16-byte loads of 7 input rows
   const int cb = tid & 15, tb = tid >> 4, pos0 = c * CH + 4 * tb;
   const int ch0 = which == 0 ? head * HD : (which == 1 ? kd + head * HD : 2 * kd + head * HD);
   const bf16 *src = which == 0 ? A.q + head * HD : (which == 1 ? A.k + head * HD : A.v + head * HD);
   const size_t rstride = which == 2 ? (size_t)A.nv * HD : (size_t)kd;
-  {
-    float wt[4][8];  // [tap][channel]
+  // 16-byte loads of the 7 input rows pos0-3 .. pos0+3 (8 channels each) and of the weights
+  uint4 xv[7];
 #pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {  // 8 channels x 4 taps = 64 bytes
-      const uint4 wq = __ldg(reinterpret_cast<const uint4 *>(A.conv_w + (size_t)(ch0 + 8 * cb) * 4) + q4);
-      const uint32_t wr[4] = {wq.x, wq.y, wq.z, wq.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {  // channel 2*q4 + e/2, taps 2*(e%2), 2*(e%2)+1
-        const int chl = 2 * q4 + (e >> 1), tap = 2 * (e & 1);
-        wt[tap][chl] = __uint_as_float(wr[e] << 16);
-        wt[tap + 1][chl] = __uint_as_float(wr[e] & 0xffff0000u);
-      }
-    }
-    float xr[7][8];  // input rows pos0-3 .. pos0+3, 8 channels
-#pragma unroll
-    for (int j = 0; j < 7; ++j) {
-      const int ip = pos0 - KC + j;
-      uint4 xv = make_uint4(0u, 0u, 0u, 0u);
-      if (slot >= 0 && ip < len) {
-        if (ip >= 0)
-          xv = __ldg(reinterpret_cast<const uint4 *>(src + (size_t)(start + ip) * rstride) + cb);
-        else
-          xv = *reinterpret_cast<const uint4 *>(A.conv_state + (size_t)slot * KC * A.C + (size_t)(KC + ip) * A.C + ch0 +
-                                                8 * cb);
-      }
-      const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        xr[j][2 * e] = __uint_as_float(xs[e] << 16);
-        xr[j][2 * e + 1] = __uint_as_float(xs[e] & 0xffff0000u);
-      }
-    }
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const bool ok = slot >= 0 && pos0 + t < len;
-      float y[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e)
-        y[e] = ok ? conv4_silu_fast(wt[0][e], wt[1][e], wt[2][e], wt[3][e], xr[t][e], xr[t + 1][e], xr[t + 2][e],
-                                    xr[t + 3][e])
-                  : 0.0f;
-      float4 *yr = reinterpret_cast<float4 *>(&Y[4 * tb + t][8 * cb]);
-      yr[0] = make_float4(y[0], y[1], y[2], y[3]);
-      yr[1] = make_float4(y[4], y[5], y[6], y[7]);
+  for (int j = 0; j < 7; ++j) {
+    const int ip = pos0 - KC + j;
+    xv[j] = make_uint4(0u, 0u, 0u, 0u);
+    if (slot >= 0 && ip < len) {
+      if (ip >= 0)
+        xv[j] = __ldg(reinterpret_cast<const uint4 *>(src + (size_t)(start + ip) * rstride) + cb);
+      else
+        xv[j] = *reinterpret_cast<const uint4 *>(A.conv_state + (size_t)slot * KC * A.C + (size_t)(KC + ip) * A.C +
+                                                 ch0 + 8 * cb);
     }
   }
-  __syncthreads();
-  if (which < 2)
-    for (int i = warp; i < CH; i += 8) warp_l2norm<HD>(Y[i], A.l2_eps, which == 0 ? A.scale : 1.0f, lane);
-  __syncthreads();
-  // fp16 hi part and fp16 remainder (lo) of every value
+  uint4 wv[4];  // channel 8cb + 2q + (e>>1): taps in bf16 pairs
+#pragma unroll
+  for (int q4 = 0; q4 < 4; ++q4) wv[q4] = __ldg(reinterpret_cast<const uint4 *>(A.conv_w + (size_t)(ch0 + 8 * cb) * 4) + q4);
+  float y[4][8];  // [token][channel]
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const uint32_t wp[4] = {wv[e >> 1].x, wv[e >> 1].y, wv[e >> 1].z, wv[e >> 1].w};
+    const uint32_t w01 = wp[2 * (e & 1)], w23 = wp[2 * (e & 1) + 1];
+    const float w0 = __uint_as_float(w01 << 16), w1 = __uint_as_float(w01 & 0xffff0000u);
+    const float w2 = __uint_as_float(w23 << 16), w3 = __uint_as_float(w23 & 0xffff0000u);
+    float x[7];
+#pragma unroll
+    for (int j = 0; j < 7; ++j) {
+      const uint32_t xp[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
+      x[j] = (e & 1) ? __uint_as_float(xp[e >> 1] & 0xffff0000u) : __uint_as_float(xp[e >> 1] << 16);
+    }
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+      y[t][e] = (slot >= 0 && pos0 + t < len) ? conv4_silu_fast(w0, w1, w2, w3, x[t], x[t + 1], x[t + 2], x[t + 3])
+                                              : 0.0f;
+  }
   if (which < 2) {
+    // L2 norm per token over the 16 lanes of the half-warp, then the [token][d] image
+    const float sc = which == 0 ? A.scale : 1.0f;
     unsigned char *img = reinterpret_cast<unsigned char *>((which == 0 ? W.qimg : W.kimg) +
                                                            ((size_t)s * A.nk + head) * 2 * kImg);
-    for (int e = tid; e < CH * 16; e += 256) {
-      const int i = e >> 4, c8 = e & 15;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      float ss = 0.0f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ss = __fmaf_rn(y[t][e], y[t][e], ss);
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+      const float rn = __fdiv_rn(sc, sqrtf(__fadd_rn(ss, A.l2_eps)));
+#pragma unroll
+      for (int e = 0; e < 8; ++e) y[t][e] = __fmul_rn(y[t][e], rn);
       uint4 hi, lo;
-      split8(&Y[i][c8 * 8], hi, lo);
-      *reinterpret_cast<uint4 *>(img + sw128_chunk(CH, i, c8)) = hi;
-      *reinterpret_cast<uint4 *>(img + kImg * 2 + sw128_chunk(CH, i, c8)) = lo;
+      split8(y[t], hi, lo);
+      const uint32_t off = sw128_chunk(CH, 4 * tb + t, cb);
+      *reinterpret_cast<uint4 *>(img + off) = hi;
+      *reinterpret_cast<uint4 *>(img + kImg * 2 + off) = lo;
     }
   }
   if (which > 0) {
-    // transposed [channel][token] image: chunk (n, cj) holds tokens 8cj .. 8cj+7
+    // transposed [channel][token] image: chunk (n, w) holds tokens 8w .. 8w+7 of
+    // channel n. Half 0 keeps channels 8cb+0..3, half 1 channels 8cb+4..7; the
+    // other four tokens of each come from the partner lane (lane ^ 16).
     unsigned char *img = reinterpret_cast<unsigned char *>(
         which == 1 ? W.ktimg + ((size_t)s * A.nk + head) * 2 * kImg : W.vtimg + ((size_t)s * A.nv + head) * 2 * kImg);
-    for (int e = tid; e < HD * 8; e += 256) {
-      const int n = e & (HD - 1), cj = e >> 7;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
       float x[8];
 #pragma unroll
-      for (int t = 0; t < 8; ++t) x[t] = Y[8 * cj + t][n];
+      for (int t = 0; t < 4; ++t) {
+        const float mine = half ? y[t][4 + j] : y[t][j];
+        const float other = __shfl_xor_sync(0xffffffffu, half ? y[t][j] : y[t][4 + j], 16);
+        x[t] = half ? other : mine;
+        x[t + 4] = half ? mine : other;
+      }
       uint4 hi, lo;
       split8(x, hi, lo);
-      *reinterpret_cast<uint4 *>(img + sw128_chunk(HD, n, cj)) = hi;
-      *reinterpret_cast<uint4 *>(img + kImg * 2 + sw128_chunk(HD, n, cj)) = lo;
+      const uint32_t off = sw128_chunk(HD, 8 * cb + 4 * half + j, warp);
+      *reinterpret_cast<uint4 *>(img + off) = hi;
+      *reinterpret_cast<uint4 *>(img + kImg * 2 + off) = lo;
     }
   }
 }
