@@ -365,10 +365,10 @@ def phase_prefill(gdn, world, steps, warmup, peak_tf):
     kms = ms  # the roofline covers the whole call (front, chunk, state and output kernels)
     flops = prefill_flops_per_token(s) * T
     res = {"tokens_per_s": T * world / (ms * 1e-3), "ms_per_step": ms, "tokens_per_step": T,
-           "ms_per_512_call": ms / (T // call), "launches_per_step": 4 * (T // call),
-           "roofline": {"bound": "tensor", "kernel": "front+chunk+state+output", "achieved": flops / (kms * 1e-3) / 1e12, "peak": peak_tf,
+           "ms_per_512_call": ms / (T // call), "launches_per_step": 3 * (T // call),
+           "roofline": {"bound": "tensor", "kernel": "front+chunk_state+output", "achieved": flops / (kms * 1e-3) / 1e12, "peak": peak_tf,
                         "unit": "TFLOP/s", "frac": flops / (kms * 1e-3) / 1e12 / peak_tf,
-                        "traffic": dram_traffic("prefill_call_512"), "traffic_scope": "one 512-token call (four kernels)",
+                        "traffic": dram_traffic("prefill_call_512"), "traffic_scope": "one 512-token call (three kernels)",
                         "algorithmic_flops_per_token": prefill_flops_per_token(s)}}
     del d, calls, ws
     torch.cuda.empty_cache()

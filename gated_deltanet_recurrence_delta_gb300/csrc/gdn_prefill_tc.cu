@@ -60,17 +60,18 @@ struct Ws {
   __half *ktimg;        // [S][nk][2 hi|lo][128][64]    K^T as a swizzled [dk][token] image
   __half *vtimg;        // [S][nv][2 hi|lo][128][64]    V^T as a swizzled [dv][token] image
   __half *wq;           // [S][nv][2][128][64]  W (rows 0-63) | Q' (rows 64-127) image (32 KiB)
-  float *sec;           // [S][nv][64]          exp(G_C - G_j) per token
+  float *sec;           // [S][nv][68]          exp(G_C - G_j) per token j < 64, then gamma_C (and 3 pad)
   float *ut, *ot;       // [S][nv][64][128]     U and O_local, token-major fp32, 16-byte chunk c of
                         //                      row i stored at c ^ (i % 8) (32 KiB each)
-  float *gc;            // [S][nv]              gamma_C
   __half *simg;         // [S][nv][2][128][64]  fp16 image of the state at the chunk's start (32 KiB)
   int *lr;              // [B]                  real length of each row, -1 = row rejected
+  int *flag;            // [S][nv]              chunk unit published (chunk + state in one grid)
 };
 
 constexpr size_t kImg = 64 * 128;    // halves in a 64x128 image
 constexpr size_t kWQ = 128 * 128;    // halves in the W|Q' image
 constexpr size_t kRowF = 128 * 64;   // floats in U / O_local
+constexpr int kSecRec = 68;          // floats in one exp(G_C - G) | gamma_C record (a multiple of 16 bytes)
 
 size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -81,8 +82,8 @@ size_t slots_total(int B, int T, bool packed) {
 size_t ws_bytes(int B, int T, int nk, int nv, bool packed) {
   const size_t S = slots_total(B, T, packed);
   return 3 * a256(S * nk * kImg * 4) + a256(S * nv * kImg * 4) + a256(S * nv * kWQ * 2) +
-         a256(S * nv * CH * 4) + 2 * a256(S * nv * kRowF * 4) + a256(S * nv * 4) +
-         a256(S * nv * kWQ * 2) + a256((size_t)B * 4);
+         a256(S * nv * kSecRec * 4) + 2 * a256(S * nv * kRowF * 4) +
+         a256(S * nv * kWQ * 2) + a256((size_t)B * 4) + a256(S * nv * 4);
 }
 
 Ws carve(void *ws, int B, int T, int nk, int nv, bool packed) {
@@ -100,16 +101,16 @@ Ws carve(void *ws, int B, int T, int nk, int nv, bool packed) {
   w.wq = reinterpret_cast<__half *>(p);
   p += a256(S * nv * kWQ * 2);
   w.sec = reinterpret_cast<float *>(p);
-  p += a256(S * nv * CH * 4);
+  p += a256(S * nv * kSecRec * 4);
   w.ut = reinterpret_cast<float *>(p);
   p += a256(S * nv * kRowF * 4);
   w.ot = reinterpret_cast<float *>(p);
   p += a256(S * nv * kRowF * 4);
-  w.gc = reinterpret_cast<float *>(p);
-  p += a256(S * nv * 4);
   w.simg = reinterpret_cast<__half *>(p);
   p += a256(S * nv * kWQ * 2);
   w.lr = reinterpret_cast<int *>(p);
+  p += a256((size_t)B * 4);
+  w.flag = reinterpret_cast<int *>(p);
   return w;
 }
 
@@ -150,6 +151,31 @@ __device__ __forceinline__ bool cta_wait(uint64_t *bar, uint32_t parity, unsigne
   const bool ok = mbar_wait_leader(bar, parity, threadIdx.x == 0, [](bool p) { return __syncthreads_or(p) != 0; });
   if (!ok && threadIdx.x == 0) set_status(status, GDN_ERR_TIMEOUT);
   return ok;
+}
+
+// A chunk unit's completion flag: set with release semantics at GPU scope,
+// read with acquire semantics (both through L2).
+__device__ __forceinline__ void release_flag(int *flag) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(flag), "r"(1) : "memory");
+}
+__device__ __forceinline__ bool acquire_flag(const int *flag) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+  return v != 0;
+}
+__device__ __forceinline__ bool relaxed_flag(const int *flag) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+  return v != 0;
+}
+// With a relaxed read of a flag before it, an acquire of what the flag's release published.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+// Orders this thread's bulk (async-proxy) global accesses with its generic ones.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 // Named barrier `id` over `n` threads (whole warps).
@@ -198,6 +224,7 @@ __global__ void __launch_bounds__(256, 4) front_kernel(LayerArgs A, Rows R, int 
   griddep_trigger();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, half = lane >> 4;
   const int s = blockIdx.x, gi = blockIdx.y, kd = A.nk * HD;
+  if (tid == 0 && gi >= 2 * A.nk) W.flag[(size_t)s * A.nv + gi - 2 * A.nk] = 0;  // unit (s, h) not yet published
   int r, c;
   R.locate(s, Ttot, r, c);
   if (r < 0) return;
@@ -307,6 +334,7 @@ constexpr int kOffPTH = 163840;  // [128 rows][128 B]: P rows 0-63 | T^T rows 64
 constexpr int kOffPTL = 180224;  // the same, lo parts
 constexpr int kOffSCR = 196608;  // fp32 [1024] solve scratch
 constexpr int kOffSm = 200704;   // g, beta, G, exp(G), exp(G_C - G): fp32 [5][64]; barriers; tmem base
+constexpr int kOffBar = kOffSm + 5 * 64 * 4;  // [0..2] chunk-local loads and products, [3..5] the chain's, TMEM base
 constexpr int kChunkSmem = kOffSm + 2048 + 1024;  // + alignment slack
 
 __device__ __forceinline__ void store_split8(unsigned char *hi_img, unsigned char *lo_img, uint32_t off,
@@ -317,10 +345,22 @@ __device__ __forceinline__ void store_split8(unsigned char *hi_img, unsigned cha
   *reinterpret_cast<uint4 *>(lo_img + off) = lo;
 }
 
-__global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int Ttot, Ws W) {
-  extern __shared__ unsigned char smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  unsigned char *sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+// Parities of the next phase that each barrier of the chunk-local pass
+// completes; a CTA that runs several chunk units carries them from one unit to
+// the next.
+struct UnitPhase {
+  uint32_t ld0, ld1, mma;
+};
+
+// The chunk-local pass of one (chunk slot s, value head h) unit, slot s holding
+// chunk c of row r (r >= 0). The caller has initialised the barriers at kOffBar, holds 256 TMEM columns at `tmem`
+// and has synchronised the CTA since any earlier use of shared memory or TMEM.
+// publish: once the unit's outputs are complete in global memory, set its
+// flag (release, GPU scope) for a chain pass of the same grid. Returns false
+// when a bounded wait ran out (the status word is set).
+__device__ __forceinline__ bool chunk_unit(unsigned char *sm, const LayerArgs &A, const Rows &R, int Ttot,
+                                           const Ws &W, int s, int h, int r, int c, uint32_t tmem,
+                                           UnitPhase &ph, bool publish) {
   unsigned char *KQH = sm + kOffKQH, *KQL = sm + kOffKQL;
   unsigned char *B2H = sm + kOffB2H, *B2L = sm + kOffB2L;
   float *AF = reinterpret_cast<float *>(sm + kOffAF);
@@ -332,32 +372,14 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
   float *sG = sb + 64;                                   // inclusive prefix of g
   float *sgam = sG + 64;                                 // exp(G_j)
   float *sec = sgam + 64;                                // exp(G_C - G_j)
-  uint64_t *bar_ld = reinterpret_cast<uint64_t *>(sec + 64);  // [0]: K|Q tiles, [1]: K^T|V^T tiles
+  uint64_t *bar_ld = reinterpret_cast<uint64_t *>(sm + kOffBar);  // [0]: K|Q tiles, [1]: K^T|V^T tiles
   uint64_t *bar_mma = bar_ld + 2;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_mma + 1);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int s = blockIdx.x, h = blockIdx.y, kh = h / A.G;
-  int r, c;
-  R.locate(s, Ttot, r, c);
-  if (r < 0) return;
+  const int kh = h / A.G;
   const int start = R.start(r), len = R.len(r);
   const int nvalid = min(CH, len - c * CH);
 
-  if (tid == 0) {
-    mbar_init(&bar_ld[0], 1);
-    mbar_init(&bar_ld[1], 1);
-    mbar_init(bar_mma, 1);
-    fence_mbar_init();
-  }
-  if (warp == 0) tmem_alloc(tmem_slot, 256);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  griddep_wait();  // the front kernel's images are complete
-  griddep_trigger();
   if (tid == 0) {  // the K|Q tiles first (the first product needs them), then K^T|V^T
     mbar_arrive_expect_tx(&bar_ld[0], 65536);
     for (int part = 0; part < 2; ++part) {
@@ -411,7 +433,8 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
       sec[j] = __expf(GC - sG[j]);
     }
   }
-  if (!cta_wait(&bar_ld[0], 0, A.status)) goto done;
+  if (!cta_wait(&bar_ld[0], ph.ld0, A.status)) return false;
+  ph.ld0 ^= 1;
 
   // ---- [K; Q] K^T -> TMEM columns [0, 64)
   if (tid == 0) {
@@ -421,10 +444,12 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
     umma_commit(bar_mma);
   }
   if (tid < CH) {  // per-token factors for the state pass: exp(G_C - G_j)
-    W.sec[((size_t)s * A.nv + h) * CH + tid] = sec[tid];
-    if (tid == 0) W.gc[(size_t)s * A.nv + h] = sgam[CH - 1];
+    float *rec = W.sec + ((size_t)s * A.nv + h) * kSecRec;
+    rec[tid] = sec[tid];
+    if (tid == 0) rec[CH] = sgam[CH - 1];  // gamma_C
   }
-  if (!cta_wait(bar_mma, 0, A.status)) goto done;
+  if (!cta_wait(bar_mma, ph.mma, A.status)) return false;
+  ph.mma ^= 1;
   tc_fence_after();
   {
     // A (rows 0-63: strictly lower, beta_i KK_ij Gamma_ij) in fp32; P (rows
@@ -559,7 +584,8 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
                     128, 64, umma_idesc_f16(128, 64));
     umma_commit(bar_mma);
   }
-  if (!cta_wait(bar_mma, 1, A.status)) goto done;
+  if (!cta_wait(bar_mma, ph.mma, A.status)) return false;
+  ph.mma ^= 1;
   tc_fence_after();
   // the P tiles are free: they take the second image [T; R] diag(beta)
   {
@@ -591,7 +617,8 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
 
   // ---- [T; R] diag(beta gamma) K -> TMEM columns [0, 128) (W | P W) and
   //      [T; R] diag(beta) V -> columns [128, 256) (U | P U)
-  if (!cta_wait(&bar_ld[1], 0, A.status)) goto done;  // long landed: loaded during the steps above
+  if (!cta_wait(&bar_ld[1], ph.ld1, A.status)) return false;  // long landed: loaded during the steps above
+  ph.ld1 ^= 1;
   if (tid == 0) {
     tc_fence_after();
     umma_tile_split(tmem, smem_u32(TRH), smem_u32(TRL), 128, smem_u32(B2H), smem_u32(B2L), 256, 64,
@@ -600,7 +627,8 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
                     smem_u32(B2L) + HD * 128, 256, 64, umma_idesc_f16(128, 128));
     umma_commit(bar_mma);
   }
-  if (!cta_wait(bar_mma, 0, A.status)) goto done;
+  if (!cta_wait(bar_mma, ph.mma, A.status)) return false;
+  ph.mma ^= 1;
   tc_fence_after();
   {
     // W / Q' into the K|Q image (plain fp16); U / O_local rows, fp32, staged in
@@ -654,14 +682,51 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
         bulk_s2g(W.ot + sh * kRowF, sm + kOffB2H + 32768, 32768);
       }
       bulk_commit();
-      bulk_wait_read_all();  // shared memory may be released; the writes land before the grid completes
+      if (publish) {
+        bulk_wait_all();  // the writes are complete: a chain pass of this grid reads them
+        fence_proxy_async_global();
+      } else {
+        bulk_wait_read_all();  // shared memory may be released; the writes land before the grid completes
+      }
     }
   }
-done:
+  if (publish) {
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();  // the other threads' stores (exp(G_C - G), gamma_C) before the flag
+      release_flag(W.flag + (size_t)s * A.nv + h);
+    }
+  }
+  return true;
+}
+
+__global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int Ttot, Ws W) {
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  unsigned char *sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  uint64_t *bar = reinterpret_cast<uint64_t *>(sm + kOffBar);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 6);
+  int r, c;
+  R.locate(blockIdx.x, Ttot, r, c);
+  if (r < 0) return;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 3; ++i) mbar_init(&bar[i], 1);
+    fence_mbar_init();
+  }
+  if (threadIdx.x < 32) tmem_alloc(tmem_slot, 256);
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 256);
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  griddep_wait();  // the front kernel's images are complete
+  griddep_trigger();
+  UnitPhase ph{0u, 0u, 0u};
+  (void)chunk_unit(sm, A, R, Ttot, W, blockIdx.x, blockIdx.y, r, c, tmem, ph, false);
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x < 32) tmem_dealloc(tmem, 256);
 }
+
 
 // ------------------------------------------------------------ state pass
 //
@@ -678,23 +743,37 @@ constexpr int kSOffW = 32768;     // 2 x W image [2 kb][64 rows][128 B] (16 KiB 
 constexpr int kSOffKT = 65536;    // 2 x K~^T image [128 rows][128 B] (16 KiB each)
 constexpr int kSOffUT = 98304;    // 2 x U fp32 [64 tokens][128 v] (32 KiB each)
 constexpr int kSOffUP = 163840;   // U'^T image [128 rows][128 B] (16 KiB)
-constexpr int kSOffSec = 180224;  // 2 x exp(G_C - G_j), fp32 [64]
-constexpr int kSOffBar = 180736;  // barriers, TMEM base
+constexpr int kSOffSec = 180224;  // 2 x the exp(G_C - G_j) | gamma_C record, fp32 [68]
+constexpr int kSOffBar = 180800;  // barriers, TMEM base
 constexpr int kStateSmem = kSOffBar + 64 + 1024;
 
-__global__ void __launch_bounds__(256, 1) state_kernel(LayerArgs A, Rows R, int Ttot, Ws W) {
-  extern __shared__ unsigned char smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  unsigned char *sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  unsigned char *SI = sm + kSOffS;
-  unsigned char *UP = sm + kSOffUP;
-  uint64_t *bar_ld = reinterpret_cast<uint64_t *>(sm + kSOffBar);  // [2]
-  uint64_t *bar_mma = bar_ld + 2;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_mma + 1);
-  __shared__ int s_min_zero, s_max_one, s_bad;
+// Thread 0: is the chunk unit behind `flag` published? With `block`, wait for
+// it (bounded; false and a recorded timeout when it never comes).
+__device__ __forceinline__ bool unit_ready(const int *flag, bool block, unsigned int *status) {
+  for (uint32_t i = 0;; ++i) {
+    if (acquire_flag(flag)) {
+      fence_proxy_async_global();  // the unit's bulk writes, before this thread's bulk reads
+      return true;
+    }
+    if (!block) return false;
+    if (i == (1u << 22)) {
+      set_status(status, GDN_ERR_TIMEOUT);
+      return false;
+    }
+    __nanosleep(64);
+  }
+}
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = blockIdx.x / A.nv, h = blockIdx.x % A.nv, kh = h / A.G;
+// What the (row b, value head h) chain needs before its chunks, and nothing
+// of theirs: the row's checks (slot, mask of ones then zeros -> real length,
+// recorded for the output pass) and the conv-tail update of the head's own
+// channels. False when the row is rejected (its status is set). With
+// prefetch_state the head's fp32 state is fetched into L2 for the chain.
+__device__ __forceinline__ bool chain_prologue(const LayerArgs &A, const Rows &R, int Ttot, const Ws &W, int b,
+                                               int h, bool prefetch_state) {
+  __shared__ int s_min_zero, s_max_one, s_bad;
+  const int tid = threadIdx.x;
+  const int kh = h / A.G;
   const int kd = A.nk * HD, C = A.C;
   const int start = R.start(b), len = R.len(b);
   const int slot = row_slot(A, b);
@@ -703,7 +782,7 @@ __global__ void __launch_bounds__(256, 1) state_kernel(LayerArgs A, Rows R, int 
       set_status(A.status, GDN_ERR_INDEX);
       if (h == 0) W.lr[b] = -1;
     }
-    return;
+    return false;
   }
   // real length: the mask row must be ones then zeros
   if (tid == 0) {
@@ -726,7 +805,7 @@ __global__ void __launch_bounds__(256, 1) state_kernel(LayerArgs A, Rows R, int 
       set_status(A.status, GDN_ERR_MASK);
       if (h == 0) W.lr[b] = -1;
     }
-    return;
+    return false;
   }
   if (tid == 0 && h == 0) W.lr[b] = Lr;  // read by the output kernel
   // conv tail: xin rows Lr .. Lr+2 (old rows when Lr < 3), own channels only
@@ -749,20 +828,31 @@ __global__ void __launch_bounds__(256, 1) state_kernel(LayerArgs A, Rows R, int 
       for (int rr = 0; rr < KC; ++rr) cs[(size_t)rr * C + ch] = nv3[rr];
     }
   }
+  if (prefetch_state) {  // 64 KiB: two 128-byte lines per thread
+    const char *gS = reinterpret_cast<const char *>(A.state + ((size_t)slot * A.nv + h) * HD * HD);
+    prefetch_l2(gS + 256 * tid);
+    prefetch_l2(gS + 256 * tid + 128);
+  }
+  return true;
+}
 
+// The sequential pass of one (row b, value head h) chain, after its
+// chain_prologue accepted the row. The caller has initialised the two load
+// barriers `bar_ld` and the product barrier `bar_mma`, holds 256 TMEM columns
+// at `tmem` and has synchronised the CTA since any earlier use of shared
+// memory or TMEM. wait_units: the chunk units run in this grid, so each
+// chunk's loads wait for its unit's flag. Returns false when a bounded wait
+// ran out.
+__device__ __forceinline__ bool state_chain(unsigned char *sm, uint64_t *bar_ld, uint64_t *bar_mma,
+                                            const LayerArgs &A, const Rows &R, const Ws &W, int b, int h,
+                                            uint32_t tmem, bool wait_units) {
+  unsigned char *SI = sm + kSOffS;
+  unsigned char *UP = sm + kSOffUP;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int kh = h / A.G;
+  const int len = R.len(b), slot = row_slot(A, b);
   const int n_chunks = (len + CH - 1) / CH;
   const int s0 = R.slot0(b);
-  if (tid == 0) {
-    mbar_init(&bar_ld[0], 1);
-    mbar_init(&bar_ld[1], 1);
-    mbar_init(bar_mma, 1);
-    fence_mbar_init();
-  }
-  if (warp == 0) tmem_alloc(tmem_slot, 256);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
 
   // chunk ci's W rows (rows 0-63 of each column block of the W|Q' image),
   // the fp16 K^T image of the key head, U and exp(G_C - G)
@@ -771,13 +861,50 @@ __global__ void __launch_bounds__(256, 1) state_kernel(LayerArgs A, Rows R, int 
     const size_t sh = (size_t)s * A.nv + h;
     const unsigned char *wq = reinterpret_cast<const unsigned char *>(W.wq + sh * kWQ);
     unsigned char *wdst = sm + kSOffW + buf * 16384;
-    mbar_arrive_expect_tx(&bar_ld[buf], 16384 + 16384 + 32768 + CH * 4);
+    mbar_arrive_expect_tx(&bar_ld[buf], 16384 + 16384 + 32768 + kSecRec * 4);
     bulk_g2s(wdst, wq, 8192, &bar_ld[buf]);
     bulk_g2s(wdst + 8192, wq + 16384, 8192, &bar_ld[buf]);
     bulk_g2s(sm + kSOffKT + buf * 16384, W.ktimg + ((size_t)s * A.nk + kh) * 2 * kImg, 16384, &bar_ld[buf]);
     bulk_g2s(sm + kSOffUT + buf * 32768, W.ut + sh * kRowF, 32768, &bar_ld[buf]);
-    bulk_g2s(sm + kSOffSec + buf * CH * 4, W.sec + sh * CH, CH * 4, &bar_ld[buf]);
+    bulk_g2s(sm + kSOffSec + buf * kSecRec * 4, W.sec + sh * kSecRec, kSecRec * 4, &bar_ld[buf]);
   };
+  // thread 0: the last chunk whose loads are issued, and the last chunk up to
+  // which every unit is known published and acquired
+  int issued = -1, acquired = wait_units ? -1 : n_chunks - 1;
+  auto issue_when_ready = [&](int ci, bool block) {  // thread 0
+    if (ci <= acquired || unit_ready(W.flag + (size_t)(s0 + ci) * A.nv + h, block, A.status)) {
+      if (ci > acquired) acquired = ci;
+      issue_loads(ci);
+      issued = ci;
+    }
+  };
+  // thread 0: the last chunk from `from` on up to which (consecutively) the units
+  // read as published, with unordered reads of up to 8 flags at once; from - 1
+  // when none
+  auto scan_published = [&](int from) {
+    bool f[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      f[e] = from + e < n_chunks && relaxed_flag(W.flag + (size_t)(s0 + from + e) * A.nv + h);
+    int seen = from - 1;
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      if (f[e] && seen == from + e - 1) seen = from + e;
+    return seen;
+  };
+  if (wait_units && tid == 0 && n_chunks > 0) {  // same grid: the first chunks' loads before the state's
+    const int seen = scan_published(0);
+    if (seen >= 0) {  // one acquire for every unit published so far
+      fence_acq_rel_gpu();
+      fence_proxy_async_global();
+      acquired = seen;
+    }
+    issue_when_ready(0, true);
+    if (n_chunks > 1 && acquired >= 1) {
+      issue_loads(1);
+      issued = 1;
+    }
+  }
   // thread <-> (value row v = TMEM lane, key half / token half hh)
   const int q = warp & 3, hh = warp >> 2, v = 32 * q + lane;
   float Sv[64];
@@ -793,9 +920,9 @@ __global__ void __launch_bounds__(256, 1) state_kernel(LayerArgs A, Rows R, int 
     fence_proxy_async_smem();
   };
   write_simg();
-  griddep_wait();  // the chunk kernel's outputs are complete
+  griddep_wait();  // the chunk kernel's outputs are complete (a no-op when this grid makes them)
   griddep_trigger();
-  if (tid == 0 && n_chunks > 0) issue_loads(0);
+  if (!wait_units && tid == 0 && n_chunks > 0) issue_when_ready(0, true);
   tc_fence_before();
   __syncthreads();
   if (tid == 0 && n_chunks > 0) {  // the state image at the start of chunk 0
@@ -803,23 +930,48 @@ __global__ void __launch_bounds__(256, 1) state_kernel(LayerArgs A, Rows R, int 
     bulk_commit();
   }
 
+  bool ok = true;
   for (int ci = 0; ci < n_chunks; ++ci) {
     const int buf = ci & 1, s = s0 + ci;
-    if (tid == 0 && ci + 1 < n_chunks) issue_loads(ci + 1);
-    const float gC = __ldg(W.gc + (size_t)s * A.nv + h);
-    if (!cta_wait(&bar_ld[buf], (uint32_t)((ci >> 1) & 1), A.status)) goto done;
+    int seen = -1;  // thread 0: the last chunk up to which the units read as published (unordered reads)
+    if (tid == 0) {  // a chunk not prefetched is waited for; the next one is prefetched when ready
+      if (issued < ci) issue_when_ready(ci, true);
+      if (issued == ci && ci + 1 < n_chunks) {
+        if (ci + 1 <= acquired) {
+          issue_loads(ci + 1);
+          issued = ci + 1;
+        } else {
+          seen = scan_published(ci + 1);
+        }
+      }
+    }
+    if (!cta_wait(&bar_ld[buf], (uint32_t)((ci >> 1) & 1), A.status)) {
+      ok = false;
+      break;
+    }
+    const float gC = reinterpret_cast<const float *>(sm + kSOffSec + buf * kSecRec * 4)[CH];
     if (tid == 0) {
       tc_fence_after();
       umma_tile(tmem, smem_u32(SI), 128, smem_u32(sm + kSOffW + buf * 16384), 64, 128, umma_idesc_f16(128, 64),
                 false);
       umma_commit(bar_mma);
+      if (seen > ci) {  // published: one acquire for all of them (off the product's path), then the loads
+        fence_acq_rel_gpu();
+        fence_proxy_async_global();
+        acquired = seen;
+        issue_loads(ci + 1);
+        issued = ci + 1;
+      }
     }
-    if (!cta_wait(bar_mma, 0, A.status)) goto done;
+    if (!cta_wait(bar_mma, 0, A.status)) {
+      ok = false;
+      break;
+    }
     tc_fence_after();
     {
       // (U - W S) * exp(G_C - G) for tokens 32hh .. 32hh+31 of value row v -> fp16 image row v
       const float *ut = reinterpret_cast<const float *>(sm + kSOffUT + buf * 32768);
-      const float *sec = reinterpret_cast<const float *>(sm + kSOffSec + buf * CH * 4) + 32 * hh;
+      const float *sec = reinterpret_cast<const float *>(sm + kSOffSec + buf * kSecRec * 4) + 32 * hh;
       float x[32];
       tmem_ld32(tmem_at(tmem, q, 32 * hh), x);
 #pragma unroll
@@ -844,7 +996,10 @@ __global__ void __launch_bounds__(256, 1) state_kernel(LayerArgs A, Rows R, int 
       umma_commit(bar_mma);
       bulk_wait_read_all();  // the copy of the previous state image has left shared memory
     }
-    if (!cta_wait(bar_mma, 1, A.status)) goto done;
+    if (!cta_wait(bar_mma, 1, A.status)) {
+      ok = false;
+      break;
+    }
     tc_fence_after();
     // S = gamma_C S + dS
 #pragma unroll
@@ -862,14 +1017,78 @@ __global__ void __launch_bounds__(256, 1) state_kernel(LayerArgs A, Rows R, int 
       bulk_commit();
     }
   }
-  if (tid == 0) bulk_wait_read_all();
+  if (tid == 0) bulk_wait_read_all();  // no bulk store may still read this CTA's shared memory
+  if (!ok) return false;
 #pragma unroll
   for (int k = 0; k < 64; ++k) gS[(size_t)(64 * hh + k) * HD + v] = Sv[k];
-done:
-  if (tid == 0) bulk_wait_read_all();  // no bulk store may still read this CTA's shared memory
+  return true;
+}
+
+__global__ void __launch_bounds__(256, 1) state_kernel(LayerArgs A, Rows R, int Ttot, Ws W) {
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  unsigned char *sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  uint64_t *bar = reinterpret_cast<uint64_t *>(sm + kSOffBar);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 3);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 3; ++i) mbar_init(&bar[i], 1);
+    fence_mbar_init();
+  }
+  if (threadIdx.x < 32) tmem_alloc(tmem_slot, 256);
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 256);
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int b = blockIdx.x / A.nv, h = blockIdx.x % A.nv;
+  if (chain_prologue(A, R, Ttot, W, b, h, false)) (void)state_chain(sm, bar, bar + 2, A, R, W, b, h, tmem, false);
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x < 32) tmem_dealloc(tmem, 256);
+}
+
+// ------------------------------------------------------------ chunk + state in one grid
+//
+// For calls with few (row, head) chains (a 512-token call of one row has 32):
+// the grid is one CTA per SM; CTA i runs chunk units i, i + grid, ... in
+// chunk-major order (all heads' first chunks first) and publishes each unit's
+// flag; then the last B*nv CTAs, which have the fewest units, run one chain
+// each, loading every chunk as soon as its unit is published. The chains'
+// early chunks thus overlap the units of the late chunks. The waiting CTAs are
+// at most half the grid and no CTA that runs units waits on another, so the
+// units always complete; every wait is bounded.
+__global__ void __launch_bounds__(256, 1) chunk_state_kernel(LayerArgs A, Rows R, int Ttot, Ws W) {
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  unsigned char *sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  uint64_t *bar = reinterpret_cast<uint64_t *>(sm + kOffBar);  // [0..2] units, [3..5] the chain
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 6);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 6; ++i) mbar_init(&bar[i], 1);
+    fence_mbar_init();
+  }
+  if (threadIdx.x < 32) tmem_alloc(tmem_slot, 256);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  griddep_wait();  // the front kernel's images and the zeroed flags are complete
+  griddep_trigger();
+  const int BH = A.B * A.nv, n_units = R.B * R.cpr * A.nv;
+  const int j = (int)gridDim.x - 1 - (int)blockIdx.x;  // chain of this CTA when j < BH
+  const bool chain = j < BH && chain_prologue(A, R, Ttot, W, j / A.nv, j % A.nv, true);
+  UnitPhase ph{0u, 0u, 0u};
+  bool ok = true;
+  for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
+    const int c = u / BH, rh = u % BH, r = rh / A.nv;  // chunk-major: unit (chunk c, row r, head rh % nv)
+    ok = chunk_unit(sm, A, R, Ttot, W, r * R.cpr + c, rh % A.nv, r, c, tmem, ph, true);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
+  if (ok && chain) (void)state_chain(sm, bar + 3, bar + 5, A, R, W, j / A.nv, j % A.nv, tmem, true);
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x < 32) tmem_dealloc(tmem, 256);
 }
 
 // ------------------------------------------------------------ outputs
@@ -889,9 +1108,11 @@ constexpr int kOutSmem = kOOffBar + 64 + 1024;
 
 // omap: out viewed as [Ttot][nv*dv] bf16, box [32 tokens][128 values];
 // zmap: z viewed the same way, box [64 tokens][128 values].
+// early: Q' and O_local were complete before the kernel this one follows
+// started (separate chunk and state kernels), so they load before the wait.
 __global__ void __launch_bounds__(256, 2) output_kernel(LayerArgs A, Rows R, int Ttot, Ws W,
                                                         const __grid_constant__ CUtensorMap omap,
-                                                        const __grid_constant__ CUtensorMap zmap) {
+                                                        const __grid_constant__ CUtensorMap zmap, int early) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   unsigned char *sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -920,18 +1141,19 @@ __global__ void __launch_bounds__(256, 2) output_kernel(LayerArgs A, Rows R, int
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const size_t sh = (size_t)s * A.nv + h;
-  // before the wait: what the chunk kernel (complete before the state kernel
-  // started) and the caller produced -- Q', O_local, z
-  if (tid == 0) {
+  // Q', O_local (from the chunk pass) and z (from the caller)
+  auto issue_qoz = [&]() {
     const unsigned char *wq = reinterpret_cast<const unsigned char *>(W.wq + sh * kWQ);
     mbar_arrive_expect_tx(bar_ld, 16384 + 32768 + 16384);
     bulk_g2s(sm + kOOffQ, wq + 8192, 8192, bar_ld);           // Q' rows, column block 0
     bulk_g2s(sm + kOOffQ + 8192, wq + 24576, 8192, bar_ld);   // Q' rows, column block 1
     bulk_g2s(sm + kOOffOT, W.ot + sh * kRowF, 32768, bar_ld);
     tma_load_2d(sm + kOOffZ, &zmap, h * HD, start + t0, bar_ld);  // rows past the tensor read as zeros
-  }
-  griddep_wait();  // the state kernel's images and row lengths are complete
+  };
+  if (early && tid == 0) issue_qoz();
+  griddep_wait();  // the state pass's images and row lengths are complete
   griddep_trigger();
+  if (!early && tid == 0) issue_qoz();
   const int Lr = W.lr[r];  // < 0: the row was rejected (its status is set)
   const int ntok = min(CH, len - t0), nreal = Lr < 0 ? 0 : max(0, min(CH, Lr - t0));
   // padded tokens of this chunk: zeros
@@ -1068,7 +1290,9 @@ gdn_status launch_prefill_tc(const LayerArgs &A, void *ws, cudaStream_t stream) 
         cudaFuncSetAttribute(tc::state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kStateSmem) !=
             cudaSuccess ||
         cudaFuncSetAttribute(tc::output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kOutSmem) !=
-            cudaSuccess)
+            cudaSuccess ||
+        cudaFuncSetAttribute(tc::chunk_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             tc::kChunkSmem) != cudaSuccess)
       return fail(GDN_ERR_CUDA, "prefill: cannot reserve shared memory");
     attr_set[dev.id].store(true, std::memory_order_release);
   }
@@ -1079,12 +1303,25 @@ gdn_status launch_prefill_tc(const LayerArgs &A, void *ws, cudaStream_t stream) 
   CUtensorMap omap, zmap;
   if (gdn_status st = tc::encode_rows_map(&omap, A.out, Ttot, A.nv * tc::HD, tc::CH / 2)) return st;
   if (gdn_status st = tc::encode_rows_map(&zmap, A.z, Ttot, A.nv * tc::HD, tc::CH)) return st;
-  if (launch_pdl(tc::chunk_kernel, dim3(S, A.nv), dim3(256), tc::kChunkSmem, stream, A, R, Ttot, W) != cudaSuccess)
-    return check_launch("prefill chunk");
-  if (launch_pdl(tc::state_kernel, dim3(A.B * A.nv), dim3(256), tc::kStateSmem, stream, A, R, Ttot, W) != cudaSuccess)
-    return check_launch("prefill state");
-  if (launch_pdl(tc::output_kernel, dim3(S, A.nv), dim3(256), tc::kOutSmem, stream, A, R, Ttot, W, omap, zmap) !=
-      cudaSuccess)
+  // Few chains (dense rows, at most half a grid of one CTA per SM): chunk units
+  // and chains in one grid, so that the chains start while late chunks are
+  // still being prepared. Otherwise two kernels.
+  const int n_units = S * A.nv, grid = n_units < dev.sms ? n_units : dev.sms;
+  const bool merged = !packed && 2 * A.B * A.nv <= grid;
+  if (merged) {
+    if (launch_pdl(tc::chunk_state_kernel, dim3(grid), dim3(256), tc::kChunkSmem, stream, A, R, Ttot, W) !=
+        cudaSuccess)
+      return check_launch("prefill chunk+state");
+  } else {
+    if (launch_pdl(tc::chunk_kernel, dim3(S, A.nv), dim3(256), tc::kChunkSmem, stream, A, R, Ttot, W) !=
+        cudaSuccess)
+      return check_launch("prefill chunk");
+    if (launch_pdl(tc::state_kernel, dim3(A.B * A.nv), dim3(256), tc::kStateSmem, stream, A, R, Ttot, W) !=
+        cudaSuccess)
+      return check_launch("prefill state");
+  }
+  if (launch_pdl(tc::output_kernel, dim3(S, A.nv), dim3(256), tc::kOutSmem, stream, A, R, Ttot, W, omap, zmap,
+                 merged ? 0 : 1) != cudaSuccess)
     return check_launch("prefill output");
   return check_launch("prefill output");
 }
