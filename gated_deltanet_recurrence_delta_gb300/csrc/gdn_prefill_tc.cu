@@ -1072,7 +1072,6 @@ __global__ void __launch_bounds__(256, 1) chunk_state_kernel(LayerArgs A, Rows R
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   griddep_wait();  // the front kernel's images and the zeroed flags are complete
-  griddep_trigger();
   const int BH = A.B * A.nv, n_units = R.B * R.cpr * A.nv;
   const int j = (int)gridDim.x - 1 - (int)blockIdx.x;  // chain of this CTA when j < BH
   const bool chain = j < BH && chain_prologue(A, R, Ttot, W, j / A.nv, j % A.nv, true);
@@ -1085,6 +1084,9 @@ __global__ void __launch_bounds__(256, 1) chunk_state_kernel(LayerArgs A, Rows R
     __syncthreads();
     tc_fence_after();
   }
+  // the output kernel may start once every CTA is past its units (it acquires
+  // the units' flags itself and waits for this grid before the state images)
+  griddep_trigger();
   if (ok && chain) (void)state_chain(sm, bar + 3, bar + 5, A, R, W, j / A.nv, j % A.nv, tmem, true);
   tc_fence_before();
   __syncthreads();
@@ -1108,8 +1110,11 @@ constexpr int kOutSmem = kOOffBar + 64 + 1024;
 
 // omap: out viewed as [Ttot][nv*dv] bf16, box [32 tokens][128 values];
 // zmap: z viewed the same way, box [64 tokens][128 values].
-// early: Q' and O_local were complete before the kernel this one follows
-// started (separate chunk and state kernels), so they load before the wait.
+// early: 1 = Q' and O_local were complete before the kernel this one follows
+// started (separate chunk and state kernels): they load before the wait.
+// 0 = they come from the grid this one follows, which published each chunk
+// unit with a flag: the unit's flag is acquired, then they load, still before
+// the wait (the state images load after it).
 __global__ void __launch_bounds__(256, 2) output_kernel(LayerArgs A, Rows R, int Ttot, Ws W,
                                                         const __grid_constant__ CUtensorMap omap,
                                                         const __grid_constant__ CUtensorMap zmap, int early) {
@@ -1150,10 +1155,12 @@ __global__ void __launch_bounds__(256, 2) output_kernel(LayerArgs A, Rows R, int
     bulk_g2s(sm + kOOffOT, W.ot + sh * kRowF, 32768, bar_ld);
     tma_load_2d(sm + kOOffZ, &zmap, h * HD, start + t0, bar_ld);  // rows past the tensor read as zeros
   };
-  if (early && tid == 0) issue_qoz();
+  if (tid == 0) {
+    if (early) issue_qoz();
+    else if (unit_ready(W.flag + sh, true, A.status)) issue_qoz();
+  }
   griddep_wait();  // the state pass's images and row lengths are complete
   griddep_trigger();
-  if (!early && tid == 0) issue_qoz();
   const int Lr = W.lr[r];  // < 0: the row was rejected (its status is set)
   const int ntok = min(CH, len - t0), nreal = Lr < 0 ? 0 : max(0, min(CH, Lr - t0));
   // padded tokens of this chunk: zeros
