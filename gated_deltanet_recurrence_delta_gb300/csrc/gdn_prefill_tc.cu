@@ -215,11 +215,13 @@ __device__ __forceinline__ void umma_tile_split(uint32_t tmem_d, uint32_t a_hi, 
 // ------------------------------------------------------------ front end
 
 // One CTA per (chunk slot, q/k/v head): 256 threads, thread = 8 channels (cb)
-// x 4 tokens (tb), all in registers. A token's 128 channels sit in one
-// half-warp, so its L2 norm is a 16-lane butterfly; warp w holds tokens
-// 8w .. 8w+7, which is one 16-byte chunk column of the transposed images, so
-// they are built by one exchange between the two half-warps.
+// x 4 tokens (tb) in registers. A token's 128 channels sit in one half-warp,
+// so its L2 norm is a 16-lane butterfly and its [token][d] chunks are stored
+// straight from registers; warp w holds tokens 8w .. 8w+7, which is one
+// 16-byte chunk column of the transposed images, so they are built by one
+// exchange between the two half-warps.
 __global__ void __launch_bounds__(256, 4) front_kernel(LayerArgs A, Rows R, int Ttot, Ws W) {
+  __shared__ __align__(128) unsigned char timg[2][kImg * 2];  // transposed image, hi | lo
   griddep_wait();  // the kernel before this call (a previous layer call) is complete
   griddep_trigger();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, half = lane >> 4;
@@ -296,9 +298,10 @@ __global__ void __launch_bounds__(256, 4) front_kernel(LayerArgs A, Rows R, int 
   if (which > 0) {
     // transposed [channel][token] image: chunk (n, w) holds tokens 8w .. 8w+7 of
     // channel n. Half 0 keeps channels 8cb+0..3, half 1 channels 8cb+4..7; the
-    // other four tokens of each come from the partner lane (lane ^ 16).
-    unsigned char *img = reinterpret_cast<unsigned char *>(
-        which == 1 ? W.ktimg + ((size_t)s * A.nk + head) * 2 * kImg : W.vtimg + ((size_t)s * A.nv + head) * 2 * kImg);
+    // other four tokens of each come from the partner lane (lane ^ 16). A
+    // warp's chunks fall in 32 different rows, so the image is assembled in
+    // shared memory and leaves as whole lines in two bulk copies.
+    unsigned char *img = timg[0];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       float x[8];
@@ -313,7 +316,17 @@ __global__ void __launch_bounds__(256, 4) front_kernel(LayerArgs A, Rows R, int 
       split8(x, hi, lo);
       const uint32_t off = sw128_chunk(HD, 8 * cb + 4 * half + j, warp);
       *reinterpret_cast<uint4 *>(img + off) = hi;
-      *reinterpret_cast<uint4 *>(img + kImg * 2 + off) = lo;
+      *reinterpret_cast<uint4 *>(timg[1] + off) = lo;
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      __half *dst = which == 1 ? W.ktimg + ((size_t)s * A.nk + head) * 2 * kImg
+                               : W.vtimg + ((size_t)s * A.nv + head) * 2 * kImg;
+      bulk_s2g(dst, timg[0], (uint32_t)(kImg * 2));
+      bulk_s2g(dst + kImg, timg[1], (uint32_t)(kImg * 2));
+      bulk_commit();
+      bulk_wait_read_all();  // the shared memory is released at exit
     }
   }
 }
