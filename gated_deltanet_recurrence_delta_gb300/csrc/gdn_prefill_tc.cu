@@ -66,6 +66,7 @@ struct Ws {
   __half *simg;         // [S][nv][2][128][64]  fp16 image of the state at the chunk's start (32 KiB)
   int *lr;              // [B]                  real length of each row, -1 = row rejected
   int *flag;            // [S][nv]              chunk unit published (chunk + state in one grid)
+  int2 *slot_rc;        // [S]                  (row, chunk) of each slot from the front kernel, row -1 = none
 };
 
 constexpr size_t kImg = 64 * 128;    // halves in a 64x128 image
@@ -83,7 +84,7 @@ size_t ws_bytes(int B, int T, int nk, int nv, bool packed) {
   const size_t S = slots_total(B, T, packed);
   return 3 * a256(S * nk * kImg * 4) + a256(S * nv * kImg * 4) + a256(S * nv * kWQ * 2) +
          a256(S * nv * kSecRec * 4) + 2 * a256(S * nv * kRowF * 4) +
-         a256(S * nv * kWQ * 2) + a256((size_t)B * 4) + a256(S * nv * 4);
+         a256(S * nv * kWQ * 2) + a256((size_t)B * 4) + a256(S * nv * 4) + a256(S * 8);
 }
 
 Ws carve(void *ws, int B, int T, int nk, int nv, bool packed) {
@@ -111,6 +112,8 @@ Ws carve(void *ws, int B, int T, int nk, int nv, bool packed) {
   w.lr = reinterpret_cast<int *>(p);
   p += a256((size_t)B * 4);
   w.flag = reinterpret_cast<int *>(p);
+  p += a256(S * nv * 4);
+  w.slot_rc = reinterpret_cast<int2 *>(p);
   return w;
 }
 
@@ -144,6 +147,19 @@ struct Rows {
     if (r < 0 || r >= B || c < 0 || st < 0 || ln < 0 || st + ln > Ttot || c * CH >= ln) r = -1;
   }
 };
+
+// (row, chunk) of slot s after the front kernel of the same call: packed rows
+// read the front kernel's map (one load through L2 instead of a binary search
+// over the row offsets); dense rows compute it.
+__device__ __forceinline__ void slot_row(const Rows &R, const Ws &W, int s, int Ttot, int &r, int &c) {
+  if (R.cu) {
+    const int2 v = __ldcg(W.slot_rc + s);
+    r = v.x;
+    c = v.y;
+  } else {
+    R.locate(s, Ttot, r, c);
+  }
+}
 
 // Bounded mbarrier wait agreed across the CTA (thread 0 polls, the rest sleep
 // in the barrier); false = give up.
@@ -229,6 +245,7 @@ __global__ void __launch_bounds__(256, 4) front_kernel(LayerArgs A, Rows R, int 
   if (tid == 0 && gi >= 2 * A.nk) W.flag[(size_t)s * A.nv + gi - 2 * A.nk] = 0;  // unit (s, h) not yet published
   int r, c;
   R.locate(s, Ttot, r, c);
+  if (tid == 0 && gi == 0) W.slot_rc[s] = make_int2(r, c);
   if (r < 0) return;
   const int start = R.start(r), len = R.len(r);
   const int which = gi < A.nk ? 0 : (gi < 2 * A.nk ? 1 : 2);
@@ -366,19 +383,27 @@ struct UnitPhase {
 };
 
 // The chunk-local pass of one (chunk slot s, value head h) unit, slot s holding
-// chunk c of row r (r >= 0). The caller has initialised the barriers at kOffBar, holds 256 TMEM columns at `tmem`
+// chunk c of row r (r >= 0). Two 64 KiB regions trade roles from one unit to
+// the next (parity): one holds the unit's K|Q tiles, the other its A / T /
+// [T; R] / P tiles; once the unit's last products are done the second is free
+// and takes the next unit's K|Q tiles (thread 0 learns the next unit, slot and
+// value head, from find_next() while the first product runs). kq_issued: this
+// unit's K|Q tiles were requested that way by the unit before. The caller has
+// initialised the barriers at kOffBar, holds 256 TMEM columns at `tmem`
 // and has synchronised the CTA since any earlier use of shared memory or TMEM.
 // publish: once the unit's outputs are complete in global memory, set its
 // flag (release, GPU scope) for a chain pass of the same grid. Returns false
 // when a bounded wait ran out (the status word is set).
-__device__ __forceinline__ bool chunk_unit(unsigned char *sm, const LayerArgs &A, const Rows &R, int Ttot,
-                                           const Ws &W, int s, int h, int r, int c, uint32_t tmem,
-                                           UnitPhase &ph, bool publish) {
-  unsigned char *KQH = sm + kOffKQH, *KQL = sm + kOffKQL;
+template <class FindNext>
+__device__ __forceinline__ bool chunk_unit(unsigned char *sm, const LayerArgs &A, const Rows &R, const Ws &W, int s,
+                                           int h, int r, int c, int parity, bool kq_issued, FindNext find_next,
+                                           uint32_t tmem, UnitPhase &ph, bool publish) {
+  const int xo = parity ? kOffAF : kOffKQH, yo = parity ? kOffKQH : kOffAF;  // K|Q region, A/T/P region
+  unsigned char *KQH = sm + xo, *KQL = sm + xo + (kOffKQL - kOffKQH);
   unsigned char *B2H = sm + kOffB2H, *B2L = sm + kOffB2L;
-  float *AF = reinterpret_cast<float *>(sm + kOffAF);
-  unsigned char *TRH = sm + kOffAF, *TRL = sm + kOffTRL;
-  unsigned char *PTH = sm + kOffPTH, *PTL = sm + kOffPTL;
+  float *AF = reinterpret_cast<float *>(sm + yo);
+  unsigned char *TRH = sm + yo, *TRL = sm + yo + (kOffTRL - kOffAF);
+  unsigned char *PTH = sm + yo + (kOffPTH - kOffAF), *PTL = sm + yo + (kOffPTL - kOffAF);
   float *SCR = reinterpret_cast<float *>(sm + kOffSCR);
   float *sg = reinterpret_cast<float *>(sm + kOffSm);  // g
   float *sb = sg + 64;                                   // beta
@@ -393,17 +418,23 @@ __device__ __forceinline__ bool chunk_unit(unsigned char *sm, const LayerArgs &A
   const int start = R.start(r), len = R.len(r);
   const int nvalid = min(CH, len - c * CH);
 
-  if (tid == 0) {  // the K|Q tiles first (the first product needs them), then K^T|V^T
+  // thread 0: the K|Q tiles of (slot s2, key head kh2) into the region at
+  // dstH (hi) / dstH + 32 KiB (lo)
+  auto issue_kq = [&](int s2, int kh2, unsigned char *dstH) {
     mbar_arrive_expect_tx(&bar_ld[0], 65536);
     for (int part = 0; part < 2; ++part) {
-      const __half *ki = W.kimg + ((size_t)s * A.nk + kh) * 2 * kImg + part * kImg;
-      const __half *qi = W.qimg + ((size_t)s * A.nk + kh) * 2 * kImg + part * kImg;
-      unsigned char *dst = part ? KQL : KQH;
+      const __half *ki = W.kimg + ((size_t)s2 * A.nk + kh2) * 2 * kImg + part * kImg;
+      const __half *qi = W.qimg + ((size_t)s2 * A.nk + kh2) * 2 * kImg + part * kImg;
+      unsigned char *dst = dstH + part * (kOffKQL - kOffKQH);
       bulk_g2s(dst, ki, 8192, &bar_ld[0]);                 // K, column block 0
       bulk_g2s(dst + 8192, qi, 8192, &bar_ld[0]);          // Q, column block 0
       bulk_g2s(dst + 16384, ki + 4096, 8192, &bar_ld[0]);  // K, column block 1
       bulk_g2s(dst + 24576, qi + 4096, 8192, &bar_ld[0]);  // Q, column block 1
     }
+  };
+  int2 nx = make_int2(-1, 0);  // thread 0: the next unit (slot, value head), slot -1 = none
+  if (tid == 0) {  // the K|Q tiles first (the first product needs them), then K^T|V^T
+    if (!kq_issued) issue_kq(s, kh, KQH);
     mbar_arrive_expect_tx(&bar_ld[1], 65536);
     for (int part = 0; part < 2; ++part) {
       unsigned char *b2 = part ? B2L : B2H;  // K^T rows 0-127, V^T rows 128-255
@@ -455,6 +486,7 @@ __device__ __forceinline__ bool chunk_unit(unsigned char *sm, const LayerArgs &A
     umma_tile_split(tmem, smem_u32(KQH), smem_u32(KQL), 128, smem_u32(KQH), smem_u32(KQL), 128, 128,
                     umma_idesc_f16(128, 64));
     umma_commit(bar_mma);
+    nx = find_next();
   }
   if (tid < CH) {  // per-token factors for the state pass: exp(G_C - G_j)
     float *rec = W.sec + ((size_t)s * A.nv + h) * kSecRec;
@@ -643,6 +675,8 @@ __device__ __forceinline__ bool chunk_unit(unsigned char *sm, const LayerArgs &A
   if (!cta_wait(bar_mma, ph.mma, A.status)) return false;
   ph.mma ^= 1;
   tc_fence_after();
+  // the A / T / [T; R] / P tiles are consumed: that region takes the next unit's K|Q
+  if (tid == 0 && nx.x >= 0) issue_kq(nx.x, nx.y / A.G, sm + yo);
   {
     // W / Q' into the K|Q image (plain fp16); U / O_local rows, fp32, staged in
     // the free B2 tiles in the row-swizzled layout of the workspace (16-byte
@@ -713,15 +747,17 @@ __device__ __forceinline__ bool chunk_unit(unsigned char *sm, const LayerArgs &A
   return true;
 }
 
-__global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int Ttot, Ws W) {
+// Persistent: one CTA per SM runs units u = blockIdx.x, + gridDim.x, ...
+// (unit u = slot u / nv, value head u % nv: the value heads of a key head run
+// side by side and share its K|Q tiles in L2), each unit prefetching the next
+// one's K|Q tiles. Slots without a chunk are skipped.
+__global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int Ttot, Ws W, int n_units) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   unsigned char *sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   uint64_t *bar = reinterpret_cast<uint64_t *>(sm + kOffBar);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 6);
-  int r, c;
-  R.locate(blockIdx.x, Ttot, r, c);
-  if (r < 0) return;
+  __shared__ int3 s_next;  // this CTA's next unit (u, row, chunk), u -1 = none; written by thread 0
   if (threadIdx.x == 0) {
     for (int i = 0; i < 3; ++i) mbar_init(&bar[i], 1);
     fence_mbar_init();
@@ -731,15 +767,43 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  griddep_wait();  // the front kernel's images are complete
+  griddep_wait();  // the front kernel's images and slot map are complete
   griddep_trigger();
+  // thread 0: the first unit from `from` on (stride gridDim.x) whose slot holds a chunk
+  auto first_unit = [&](int from) {
+    for (int v = from; v < n_units; v += gridDim.x) {
+      int r, c;
+      slot_row(R, W, v / A.nv, Ttot, r, c);
+      if (r >= 0) return make_int3(v, r, c);
+    }
+    return make_int3(-1, 0, 0);
+  };
+  if (threadIdx.x == 0) s_next = first_unit(blockIdx.x);
+  __syncthreads();
+  int3 cur = s_next;
   UnitPhase ph{0u, 0u, 0u};
-  (void)chunk_unit(sm, A, R, Ttot, W, blockIdx.x, blockIdx.y, r, c, tmem, ph, false);
+  int parity = 0;
+  bool kq = false;
+  while (cur.x >= 0) {
+    auto find_next = [&]() {  // thread 0, during the unit: published for the CTA in s_next
+      const int3 n = first_unit(cur.x + gridDim.x);
+      s_next = n;
+      return make_int2(n.x < 0 ? -1 : n.x / A.nv, n.x < 0 ? 0 : n.x % A.nv);
+    };
+    const bool ok =
+        chunk_unit(sm, A, R, W, cur.x / A.nv, cur.x % A.nv, cur.y, cur.z, parity, kq, find_next, tmem, ph, false);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (!ok) break;
+    cur = s_next;
+    kq = true;
+    parity ^= 1;
+  }
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x < 32) tmem_dealloc(tmem, 256);
 }
-
 
 // ------------------------------------------------------------ state pass
 //
@@ -1090,9 +1154,15 @@ __global__ void __launch_bounds__(256, 1) chunk_state_kernel(LayerArgs A, Rows R
   const bool chain = j < BH && chain_prologue(A, R, Ttot, W, j / A.nv, j % A.nv, true);
   UnitPhase ph{0u, 0u, 0u};
   bool ok = true;
-  for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
+  int parity = 0;
+  for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x, parity ^= 1) {
     const int c = u / BH, rh = u % BH, r = rh / A.nv;  // chunk-major: unit (chunk c, row r, head rh % nv)
-    ok = chunk_unit(sm, A, R, Ttot, W, r * R.cpr + c, rh % A.nv, r, c, tmem, ph, true);
+    auto find_next = [&]() {
+      const int v = u + (int)gridDim.x, c2 = v / BH, rh2 = v % BH;
+      return v < n_units ? make_int2((rh2 / A.nv) * R.cpr + c2, rh2 % A.nv) : make_int2(-1, 0);
+    };
+    ok = chunk_unit(sm, A, R, W, r * R.cpr + c, rh % A.nv, r, c, parity, u != (int)blockIdx.x, find_next, tmem, ph,
+                    true);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1144,7 +1214,7 @@ __global__ void __launch_bounds__(256, 2) output_kernel(LayerArgs A, Rows R, int
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int s = blockIdx.x, h = blockIdx.y;
   int r, c;
-  R.locate(s, Ttot, r, c);
+  slot_row(R, W, s, Ttot, r, c);  // the front kernel completed before the kernel this one follows started
   if (r < 0) return;
   const int start = R.start(r), len = R.len(r), t0 = c * CH;
   if (tid == 0) {
@@ -1333,7 +1403,7 @@ gdn_status launch_prefill_tc(const LayerArgs &A, void *ws, cudaStream_t stream) 
         cudaSuccess)
       return check_launch("prefill chunk+state");
   } else {
-    if (launch_pdl(tc::chunk_kernel, dim3(S, A.nv), dim3(256), tc::kChunkSmem, stream, A, R, Ttot, W) !=
+    if (launch_pdl(tc::chunk_kernel, dim3(grid), dim3(256), tc::kChunkSmem, stream, A, R, Ttot, W, n_units) !=
         cudaSuccess)
       return check_launch("prefill chunk");
     if (launch_pdl(tc::state_kernel, dim3(A.B * A.nv), dim3(256), tc::kStateSmem, stream, A, R, Ttot, W) !=
