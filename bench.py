@@ -395,7 +395,7 @@ def phase_varlen(gdn, world, steps, warmup, peak_tf, n_layers=24):
             gdn.prefill_chunked(d["dims"], d["inp"], d["conv_state"], d["state"], d["out"], ws)
 
     ms = timed(world, steps, warmup, step)
-    kms = ms  # the roofline covers whole layers (all four kernels)
+    kms = ms  # the roofline covers whole layers (all their kernels)
     flops = prefill_flops_per_token(s) * real * n_layers
     res = {"real_tokens_per_s": real * world / (ms * 1e-3),
            "layer_tokens_per_s": real * n_layers * world / (ms * 1e-3), "ms_per_step": ms,
