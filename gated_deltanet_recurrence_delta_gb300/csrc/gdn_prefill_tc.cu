@@ -15,8 +15,9 @@
 //
 // Kernels (one call = front -> chunk -> state -> output, stream ordered):
 //   front  conv + SiLU + q/k L2 norm per (chunk slot, q/k/v head), written
-//          as split fp16 tiles (128B-swizzled K-major images): K and Q as
-//          [token][d], K^T and V^T as [d][token].
+//          as split fp16 tiles, 128B-swizzled [token][d] images of Q, K and V
+//          (K-major operands where d is the contraction, MN-major ones where
+//          the tokens are).
 //   chunk  per (chunk slot, value head), all chunks in parallel: [K;Q] K^T on
 //          tcgen05 (M=128,N=64,K=128); A and P in fp32 from TMEM; T by a
 //          blocked fp32 triangular inverse; R = P T (tcgen05); then the
@@ -27,8 +28,8 @@
 //   state  per (row, value head), sequential over its chunks with the state
 //          in registers (fp32) and an fp16 copy in shared memory:
 //          X = S_math W^T (tcgen05 M=128,N=64,K=128) -> U' = U - X,
-//          dS = (U' exp(G_C - G))^T-image x K^T-image (tcgen05 M=128,N=128,
-//          K=64) ->
+//          dS = (U' exp(G_C - G))^T-image x K-image (tcgen05 M=128,N=128,
+//          K=64, K read MN-major) ->
 //          S = gamma_C S + dS; the fp16 state image at every chunk start
 //          is copied out.
 //   output per (chunk slot, value head), all chunks in parallel:
@@ -57,8 +58,7 @@ constexpr int HD = 128;  // head size handled here
 
 struct Ws {
   __half *kimg, *qimg;  // [S][nk][2 hi|lo][2][64][64]  K, Q as swizzled [token][dk] images (2 x 16 KiB)
-  __half *ktimg;        // [S][nk][2 hi|lo][128][64]    K^T as a swizzled [dk][token] image
-  __half *vtimg;        // [S][nv][2 hi|lo][128][64]    V^T as a swizzled [dv][token] image
+  __half *vimg;         // [S][nv][2 hi|lo][2][64][64]  V as a swizzled [token][dv] image
   __half *wq;           // [S][nv][2][128][64]  W (rows 0-63) | Q' (rows 64-127) image (32 KiB)
   float *sec;           // [S][nv][68]          exp(G_C - G_j) per token j < 64, then gamma_C (and 3 pad)
   float *ut, *ot;       // [S][nv][64][128]     U and O_local, token-major fp32, 16-byte chunk c of
@@ -82,7 +82,7 @@ size_t slots_total(int B, int T, bool packed) {
 
 size_t ws_bytes(int B, int T, int nk, int nv, bool packed) {
   const size_t S = slots_total(B, T, packed);
-  return 3 * a256(S * nk * kImg * 4) + a256(S * nv * kImg * 4) + a256(S * nv * kWQ * 2) +
+  return 2 * a256(S * nk * kImg * 4) + a256(S * nv * kImg * 4) + a256(S * nv * kWQ * 2) +
          a256(S * nv * kSecRec * 4) + 2 * a256(S * nv * kRowF * 4) +
          a256(S * nv * kWQ * 2) + a256((size_t)B * 4) + a256(S * nv * 4) + a256(S * 8);
 }
@@ -95,9 +95,7 @@ Ws carve(void *ws, int B, int T, int nk, int nv, bool packed) {
   p += a256(S * nk * kImg * 4);
   w.qimg = reinterpret_cast<__half *>(p);
   p += a256(S * nk * kImg * 4);
-  w.ktimg = reinterpret_cast<__half *>(p);
-  p += a256(S * nk * kImg * 4);
-  w.vtimg = reinterpret_cast<__half *>(p);
+  w.vimg = reinterpret_cast<__half *>(p);
   p += a256(S * nv * kImg * 4);
   w.wq = reinterpret_cast<__half *>(p);
   p += a256(S * nv * kWQ * 2);
@@ -228,19 +226,26 @@ __device__ __forceinline__ void umma_tile_split(uint32_t tmem_d, uint32_t a_hi, 
   umma_tile(tmem_d, a_lo, RA, b_hi, RB, K, idesc, true);
 }
 
+// D = A B in split fp16 with B read MN-major (blocks lbo bytes apart)
+__device__ __forceinline__ void umma_tile_split_bmn(uint32_t tmem_d, uint32_t a_hi, uint32_t a_lo, int RA,
+                                                    uint32_t b_hi, uint32_t b_lo, uint32_t lbo, int K,
+                                                    uint32_t idesc) {
+  umma_tile_bmn(tmem_d, a_hi, RA, b_hi, lbo, K, idesc, false);
+  umma_tile_bmn(tmem_d, a_hi, RA, b_lo, lbo, K, idesc, true);
+  umma_tile_bmn(tmem_d, a_lo, RA, b_hi, lbo, K, idesc, true);
+}
+
 // ------------------------------------------------------------ front end
 
 // One CTA per (chunk slot, q/k/v head): 256 threads, thread = 8 channels (cb)
 // x 4 tokens (tb) in registers. A token's 128 channels sit in one half-warp,
-// so its L2 norm is a 16-lane butterfly and its [token][d] chunks are stored
-// straight from registers; warp w holds tokens 8w .. 8w+7, which is one
-// 16-byte chunk column of the transposed images, so they are built by one
-// exchange between the two half-warps.
+// so its L2 norm is a 16-lane butterfly, and each thread's 16-byte chunks of
+// the [token][d] image are stored straight from registers (a warp writes
+// whole lines).
 __global__ void __launch_bounds__(256, 4) front_kernel(LayerArgs A, Rows R, int Ttot, Ws W) {
-  __shared__ __align__(128) unsigned char timg[2][kImg * 2];  // transposed image, hi | lo
   griddep_wait();  // the kernel before this call (a previous layer call) is complete
   griddep_trigger();
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, half = lane >> 4;
+  const int tid = threadIdx.x;
   const int s = blockIdx.x, gi = blockIdx.y, kd = A.nk * HD;
   if (tid == 0 && gi >= 2 * A.nk) W.flag[(size_t)s * A.nv + gi - 2 * A.nk] = 0;  // unit (s, h) not yet published
   int r, c;
@@ -290,13 +295,15 @@ __global__ void __launch_bounds__(256, 4) front_kernel(LayerArgs A, Rows R, int 
       y[t][e] = (slot >= 0 && pos0 + t < len) ? conv4_silu_fast(w0, w1, w2, w3, x[t], x[t + 1], x[t + 2], x[t + 3])
                                               : 0.0f;
   }
-  if (which < 2) {
-    // L2 norm per token over the 16 lanes of the half-warp, then the [token][d] image
-    const float sc = which == 0 ? A.scale : 1.0f;
-    unsigned char *img = reinterpret_cast<unsigned char *>((which == 0 ? W.qimg : W.kimg) +
-                                                           ((size_t)s * A.nk + head) * 2 * kImg);
+  // q, k: L2 norm per token over the 16 lanes of the half-warp; then the
+  // [token][d] image, each thread's chunks straight from registers
+  const float sc = which == 0 ? A.scale : 1.0f;
+  unsigned char *img = reinterpret_cast<unsigned char *>(
+      which == 2 ? W.vimg + ((size_t)s * A.nv + head) * 2 * kImg
+                 : (which == 0 ? W.qimg : W.kimg) + ((size_t)s * A.nk + head) * 2 * kImg);
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
+  for (int t = 0; t < 4; ++t) {
+    if (which < 2) {
       float ss = 0.0f;
 #pragma unroll
       for (int e = 0; e < 8; ++e) ss = __fmaf_rn(y[t][e], y[t][e], ss);
@@ -305,46 +312,12 @@ __global__ void __launch_bounds__(256, 4) front_kernel(LayerArgs A, Rows R, int 
       const float rn = __fdiv_rn(sc, sqrtf(__fadd_rn(ss, A.l2_eps)));
 #pragma unroll
       for (int e = 0; e < 8; ++e) y[t][e] = __fmul_rn(y[t][e], rn);
-      uint4 hi, lo;
-      split8(y[t], hi, lo);
-      const uint32_t off = sw128_chunk(CH, 4 * tb + t, cb);
-      *reinterpret_cast<uint4 *>(img + off) = hi;
-      *reinterpret_cast<uint4 *>(img + kImg * 2 + off) = lo;
     }
-  }
-  if (which > 0) {
-    // transposed [channel][token] image: chunk (n, w) holds tokens 8w .. 8w+7 of
-    // channel n. Half 0 keeps channels 8cb+0..3, half 1 channels 8cb+4..7; the
-    // other four tokens of each come from the partner lane (lane ^ 16). A
-    // warp's chunks fall in 32 different rows, so the image is assembled in
-    // shared memory and leaves as whole lines in two bulk copies.
-    unsigned char *img = timg[0];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      float x[8];
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const float mine = half ? y[t][4 + j] : y[t][j];
-        const float other = __shfl_xor_sync(0xffffffffu, half ? y[t][j] : y[t][4 + j], 16);
-        x[t] = half ? other : mine;
-        x[t + 4] = half ? mine : other;
-      }
-      uint4 hi, lo;
-      split8(x, hi, lo);
-      const uint32_t off = sw128_chunk(HD, 8 * cb + 4 * half + j, warp);
-      *reinterpret_cast<uint4 *>(img + off) = hi;
-      *reinterpret_cast<uint4 *>(timg[1] + off) = lo;
-    }
-    fence_proxy_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-      __half *dst = which == 1 ? W.ktimg + ((size_t)s * A.nk + head) * 2 * kImg
-                               : W.vtimg + ((size_t)s * A.nv + head) * 2 * kImg;
-      bulk_s2g(dst, timg[0], (uint32_t)(kImg * 2));
-      bulk_s2g(dst + kImg, timg[1], (uint32_t)(kImg * 2));
-      bulk_commit();
-      bulk_wait_read_all();  // the shared memory is released at exit
-    }
+    uint4 hi, lo;
+    split8(y[t], hi, lo);
+    const uint32_t off = sw128_chunk(CH, 4 * tb + t, cb);
+    *reinterpret_cast<uint4 *>(img + off) = hi;
+    *reinterpret_cast<uint4 *>(img + kImg * 2 + off) = lo;
   }
 }
 
@@ -354,8 +327,8 @@ __global__ void __launch_bounds__(256, 4) front_kernel(LayerArgs A, Rows R, int 
 // are the two fp16 parts of a split operand.
 constexpr int kOffKQH = 0;       // [2 kb][128 rows][128 B]: K rows 0-63 | Q rows 64-127 (hi); later W|Q'
 constexpr int kOffKQL = 32768;   // the same, lo parts
-constexpr int kOffB2H = 65536;   // [256 rows][128 B]: (beta gamma K)^T rows 0-127 | (beta V)^T rows 128-255 (hi)
-constexpr int kOffB2L = 98304;   // the same, lo parts
+constexpr int kOffB2H = 65536;   // V image [2 kb][64 rows][128 B] (hi), then the lo parts at +16 KiB;
+                                 // at the end the U | O_local staging (64 KiB)
 constexpr int kOffAF = 131072;   // fp32 [64][kLD]: A, then T in place; later the [T; R] image (hi)
 constexpr int kLD = 65;          // padded row stride: column-wise accesses hit distinct banks
                                  // (the 256 bytes past 16 KiB overlap the [T; R] lo image, unused until then)
@@ -400,7 +373,7 @@ __device__ __forceinline__ bool chunk_unit(unsigned char *sm, const LayerArgs &A
                                            uint32_t tmem, UnitPhase &ph, bool publish) {
   const int xo = parity ? kOffAF : kOffKQH, yo = parity ? kOffKQH : kOffAF;  // K|Q region, A/T/P region
   unsigned char *KQH = sm + xo, *KQL = sm + xo + (kOffKQL - kOffKQH);
-  unsigned char *B2H = sm + kOffB2H, *B2L = sm + kOffB2L;
+  unsigned char *B2H = sm + kOffB2H;
   float *AF = reinterpret_cast<float *>(sm + yo);
   unsigned char *TRH = sm + yo, *TRL = sm + yo + (kOffTRL - kOffAF);
   unsigned char *PTH = sm + yo + (kOffPTH - kOffAF), *PTL = sm + yo + (kOffPTL - kOffAF);
@@ -410,7 +383,7 @@ __device__ __forceinline__ bool chunk_unit(unsigned char *sm, const LayerArgs &A
   float *sG = sb + 64;                                   // inclusive prefix of g
   float *sgam = sG + 64;                                 // exp(G_j)
   float *sec = sgam + 64;                                // exp(G_C - G_j)
-  uint64_t *bar_ld = reinterpret_cast<uint64_t *>(sm + kOffBar);  // [0]: K|Q tiles, [1]: K^T|V^T tiles
+  uint64_t *bar_ld = reinterpret_cast<uint64_t *>(sm + kOffBar);  // [0]: K|Q tiles, [1]: V tiles
   uint64_t *bar_mma = bar_ld + 2;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -433,14 +406,10 @@ __device__ __forceinline__ bool chunk_unit(unsigned char *sm, const LayerArgs &A
     }
   };
   int2 nx = make_int2(-1, 0);  // thread 0: the next unit (slot, value head), slot -1 = none
-  if (tid == 0) {  // the K|Q tiles first (the first product needs them), then K^T|V^T
+  if (tid == 0) {  // the K|Q tiles first (the first product needs them), then V
     if (!kq_issued) issue_kq(s, kh, KQH);
-    mbar_arrive_expect_tx(&bar_ld[1], 65536);
-    for (int part = 0; part < 2; ++part) {
-      unsigned char *b2 = part ? B2L : B2H;  // K^T rows 0-127, V^T rows 128-255
-      bulk_g2s(b2, W.ktimg + ((size_t)s * A.nk + kh) * 2 * kImg + part * kImg, 16384, &bar_ld[1]);
-      bulk_g2s(b2 + 16384, W.vtimg + ((size_t)s * A.nv + h) * 2 * kImg + part * kImg, 16384, &bar_ld[1]);
-    }
+    mbar_arrive_expect_tx(&bar_ld[1], 32768);
+    bulk_g2s(B2H, W.vimg + ((size_t)s * A.nv + h) * 2 * kImg, 32768, &bar_ld[1]);  // hi | lo
   }
   // gates of the chunk's tokens; padding and tokens past the row end get g = beta = 0
   if (tid < CH) {
@@ -666,10 +635,12 @@ __device__ __forceinline__ bool chunk_unit(unsigned char *sm, const LayerArgs &A
   ph.ld1 ^= 1;
   if (tid == 0) {
     tc_fence_after();
-    umma_tile_split(tmem, smem_u32(TRH), smem_u32(TRL), 128, smem_u32(B2H), smem_u32(B2L), 256, 64,
-                    umma_idesc_f16(128, 128));
-    umma_tile_split(tmem + 128, smem_u32(PTH), smem_u32(PTL), 128, smem_u32(B2H) + HD * 128,
-                    smem_u32(B2L) + HD * 128, 256, 64, umma_idesc_f16(128, 128));
+    // K (rows 0-63 of the K|Q tiles, column blocks 16 KiB apart) and V (its own
+    // tiles, column blocks 8 KiB apart), both read MN-major: tokens contract
+    umma_tile_split_bmn(tmem, smem_u32(TRH), smem_u32(TRL), 128, smem_u32(KQH), smem_u32(KQL), 16384, 64,
+                        umma_idesc_f16_bmn(128, 128));
+    umma_tile_split_bmn(tmem + 128, smem_u32(PTH), smem_u32(PTL), 128, smem_u32(B2H), smem_u32(B2H) + 16384, 8192,
+                        64, umma_idesc_f16_bmn(128, 128));
     umma_commit(bar_mma);
   }
   if (!cta_wait(bar_mma, ph.mma, A.status)) return false;
@@ -809,7 +780,7 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
 //
 // The sequential part only: per (row, value head), over its chunks,
 //   X = S_math W^T (tcgen05 M=128 v, N=64 tokens, K=128) -> U' = U - X,
-//   dS = (U' * exp(G_C - G))^T-image x K^T-image (M=128, N=128, K=64) ->
+//   dS = (U' * exp(G_C - G))^T-image x K-image (M=128, N=128, K=64, K read MN-major) ->
 //   S = gamma_C S + dS,
 // with the state in registers (fp32) and an fp16 copy in shared memory. The
 // fp16 image of the state at the start of every chunk is copied out (bulk
@@ -817,7 +788,7 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
 
 constexpr int kSOffS = 0;         // S_math fp16 image [2 kb][128 rows][128 B] (32 KiB)
 constexpr int kSOffW = 32768;     // 2 x W image [2 kb][64 rows][128 B] (16 KiB each)
-constexpr int kSOffKT = 65536;    // 2 x K~^T image [128 rows][128 B] (16 KiB each)
+constexpr int kSOffKT = 65536;    // 2 x K image (hi) [2 kb][64 rows][128 B] (16 KiB each), read MN-major
 constexpr int kSOffUT = 98304;    // 2 x U fp32 [64 tokens][128 v] (32 KiB each)
 constexpr int kSOffUP = 163840;   // U'^T image [128 rows][128 B] (16 KiB)
 constexpr int kSOffSec = 180224;  // 2 x the exp(G_C - G_j) | gamma_C record, fp32 [68]
@@ -932,7 +903,7 @@ __device__ __forceinline__ bool state_chain(unsigned char *sm, uint64_t *bar_ld,
   const int s0 = R.slot0(b);
 
   // chunk ci's W rows (rows 0-63 of each column block of the W|Q' image),
-  // the fp16 K^T image of the key head, U and exp(G_C - G)
+  // the fp16 K image (hi) of the key head, U and exp(G_C - G)
   auto issue_loads = [&](int ci) {  // thread 0
     const int buf = ci & 1, s = s0 + ci;
     const size_t sh = (size_t)s * A.nv + h;
@@ -941,7 +912,7 @@ __device__ __forceinline__ bool state_chain(unsigned char *sm, uint64_t *bar_ld,
     mbar_arrive_expect_tx(&bar_ld[buf], 16384 + 16384 + 32768 + kSecRec * 4);
     bulk_g2s(wdst, wq, 8192, &bar_ld[buf]);
     bulk_g2s(wdst + 8192, wq + 16384, 8192, &bar_ld[buf]);
-    bulk_g2s(sm + kSOffKT + buf * 16384, W.ktimg + ((size_t)s * A.nk + kh) * 2 * kImg, 16384, &bar_ld[buf]);
+    bulk_g2s(sm + kSOffKT + buf * 16384, W.kimg + ((size_t)s * A.nk + kh) * 2 * kImg, 16384, &bar_ld[buf]);
     bulk_g2s(sm + kSOffUT + buf * 32768, W.ut + sh * kRowF, 32768, &bar_ld[buf]);
     bulk_g2s(sm + kSOffSec + buf * kSecRec * 4, W.sec + sh * kSecRec, kSecRec * 4, &bar_ld[buf]);
   };
@@ -1068,8 +1039,8 @@ __device__ __forceinline__ bool state_chain(unsigned char *sm, uint64_t *bar_ld,
     __syncthreads();
     if (tid == 0) {
       tc_fence_after();
-      umma_tile(tmem + 128, smem_u32(UP), 128, smem_u32(sm + kSOffKT + buf * 16384), 128, 64,
-                umma_idesc_f16(128, 128), false);
+      umma_tile_bmn(tmem + 128, smem_u32(UP), 128, smem_u32(sm + kSOffKT + buf * 16384), 8192, 64,
+                    umma_idesc_f16_bmn(128, 128), false);
       umma_commit(bar_mma);
       bulk_wait_read_all();  // the copy of the previous state image has left shared memory
     }

@@ -47,6 +47,29 @@ __device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t da, uint64_t 
       : "memory");
 }
 
+// Descriptor of an MN-major SW128 fp16 operand stored [K rows][MN columns]:
+// 64-column MN blocks `lbo` bytes apart, each [rows][128 bytes] with the same
+// chunk swizzle as a K-major image, 8-row K groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t umma_desc_mn(uint32_t saddr, uint32_t lbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(lbo >> 4) << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// kind::f16 instruction descriptor with B read MN-major (A K-major).
+__host__ __device__ constexpr uint32_t umma_idesc_f16_bmn(int M, int N) { return umma_idesc_f16(M, N) | (1u << 16); }
+
+// D = A[0:M, 0:K] * B[0:K, 0:N]: A a K-major SW128 image with RA rows, B an
+// MN-major image [K rows][N] whose 64-column blocks are lbo bytes apart
+// (a [token][d] image read with the tokens as the contraction).
+__device__ __forceinline__ void umma_tile_bmn(uint32_t tmem_d, uint32_t sa, int RA, uint32_t sb, uint32_t lbo, int K,
+                                              uint32_t idesc, bool acc_first) {
+  for (int k = 0; k < K / 16; ++k) {
+    const int kb = k >> 2, ks = k & 3;
+    umma_f16(tmem_d, umma_desc(sa + kb * RA * 128 + ks * 32), umma_desc_mn(sb + k * 2048, lbo), idesc,
+             acc_first || k > 0);
+  }
+}
+
 // A full MxN product over K (multiple of 16), operands as SW128 images with
 // RA / RB rows: D = A[0:M, 0:K] * B[0:N, 0:K]^T.
 __device__ __forceinline__ void umma_tile(uint32_t tmem_d, uint32_t sa, int RA, uint32_t sb, int RB, int K,
