@@ -406,10 +406,16 @@ __device__ __forceinline__ bool chunk_unit(unsigned char *sm, const LayerArgs &A
     }
   };
   int2 nx = make_int2(-1, 0);  // thread 0: the next unit (slot, value head), slot -1 = none
-  if (tid == 0) {  // the K|Q tiles first (the first product needs them), then V
-    if (!kq_issued) issue_kq(s, kh, KQH);
+  auto issue_v = [&]() {  // thread 0
     mbar_arrive_expect_tx(&bar_ld[1], 32768);
     bulk_g2s(B2H, W.vimg + ((size_t)s * A.nv + h) * 2 * kImg, 32768, &bar_ld[1]);  // hi | lo
+  };
+  // Without publish, the unit before may still be storing its outputs from
+  // the V region and from the region this unit's A / P tiles go to: V is
+  // requested, and those tiles written, once its stores have read them.
+  if (tid == 0) {  // the K|Q tiles first (the first product needs them), then V
+    if (!kq_issued) issue_kq(s, kh, KQH);
+    if (publish) issue_v();
   }
   // gates of the chunk's tokens; padding and tokens past the row end get g = beta = 0
   if (tid < CH) {
@@ -462,9 +468,11 @@ __device__ __forceinline__ bool chunk_unit(unsigned char *sm, const LayerArgs &A
     rec[tid] = sec[tid];
     if (tid == 0) rec[CH] = sgam[CH - 1];  // gamma_C
   }
+  if (!publish && (tid == 0 || tid == 128)) bulk_wait_read_all();  // the unit before's stores (see above)
   if (!cta_wait(bar_mma, ph.mma, A.status)) return false;
   ph.mma ^= 1;
   tc_fence_after();
+  if (!publish && tid == 0) issue_v();
   {
     // A (rows 0-63: strictly lower, beta_i KK_ij Gamma_ij) in fp32; P (rows
     // 64-127: QK_ij Gamma_ij for j <= i) as a split image
@@ -703,9 +711,7 @@ __device__ __forceinline__ bool chunk_unit(unsigned char *sm, const LayerArgs &A
       if (publish) {
         bulk_wait_all();  // the writes are complete: a chain pass of this grid reads them
         fence_proxy_async_global();
-      } else {
-        bulk_wait_read_all();  // shared memory may be released; the writes land before the grid completes
-      }
+      }  // else the next unit, or the CTA's exit, waits for the stores to read shared memory
     }
   }
   if (publish) {
@@ -771,6 +777,7 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
     kq = true;
     parity ^= 1;
   }
+  if (threadIdx.x == 0 || threadIdx.x == 128) bulk_wait_read_all();  // the last unit's stores
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x < 32) tmem_dealloc(tmem, 256);
