@@ -24,11 +24,14 @@
  *   - Kernels are launched with programmatic stream serialization: a kernel
  *     may start while the kernel before it in the stream is finishing, and it
  *     waits (griddepcontrol.wait) for that kernel to complete before it reads
- *     or writes any tensor; it then lets the next kernel in the stream start
- *     early (griddepcontrol.launch_dependents). Stream order is preserved for
- *     ordinary kernels; a caller's kernel that itself opts into programmatic
- *     launch after a libgdn call must wait before reading libgdn's outputs, as
- *     with any programmatic dependent.
+ *     or writes any caller tensor; it then lets the next kernel in the stream
+ *     start early (griddepcontrol.launch_dependents). Inside one prefill call
+ *     a kernel may read workspace data of an earlier kernel of the same call
+ *     before its wait, once an earlier wait or a flag (release / acquire at
+ *     GPU scope) has ordered it. Stream order is preserved for ordinary
+ *     kernels; a caller's kernel that itself opts into programmatic launch
+ *     after a libgdn call must wait before reading libgdn's outputs, as with
+ *     any programmatic dependent.
  *   - Arguments are validated on the host before anything is launched; an
  *     invalid call returns an error status, launches nothing and leaves every
  *     buffer untouched. gdn_last_error() then describes it.
@@ -139,7 +142,14 @@ gdn_status gdn_verify_with_checkpoints(const gdn_dims *dims, const gdn_inputs *i
  *   tensors [1][T][...], T = total packed tokens, mask [T].
  *   out        bf16 [B][T][nv][dv] (or [1][T][nv][dv]); zero at padded tokens
  *   workspace  device scratch of at least gdn_prefill_workspace_size(dims)
- *              bytes, 256-byte aligned; its contents need not be preserved. */
+ *              bytes, 256-byte aligned; its contents need not be preserved.
+ * Head size 128 runs three or four kernels: front (conv, norms, operand
+ * tiles), then the chunk and state passes and the output pass. With few
+ * (row, value head) chains (dense rows, at most half as many chains as the
+ * GPU has SMs) the chunk and state passes share one grid of one CTA per SM
+ * whose chain CTAs wait on per-unit flags that the other CTAs publish; every
+ * such wait is bounded and reports GDN_ERR_TIMEOUT through the status word if
+ * it runs out. */
 gdn_status gdn_prefill_chunked(const gdn_dims *dims, const gdn_inputs *in, void *conv_state,
                                float *recurrent_state, void *out, void *workspace,
                                size_t workspace_bytes, void *stream);
