@@ -13,12 +13,15 @@
 //   S_C = gamma_C S_0 + (K * exp(G_C - G))^T U'
 // (S on the stored transpose St[k][v]). exp(-G) is never formed.
 //
-// Kernels (one call = front -> chunk -> state -> output, stream ordered):
+// Passes (one call = front -> chunk -> state -> output, stream ordered; the
+// chunk and state passes are one grid when there are few chains, two kernels
+// otherwise):
 //   front  conv + SiLU + q/k L2 norm per (chunk slot, q/k/v head), written
 //          as split fp16 tiles, 128B-swizzled [token][d] images of Q, K and V
 //          (K-major operands where d is the contraction, MN-major ones where
 //          the tokens are).
-//   chunk  per (chunk slot, value head), all chunks in parallel: [K;Q] K^T on
+//   chunk  per (chunk slot, value head) unit, all chunks in parallel, one
+//          persistent CTA per SM walking its units: [K;Q] K^T on
 //          tcgen05 (M=128,N=64,K=128); A and P in fp32 from TMEM; T by a
 //          blocked fp32 triangular inverse; R = P T (tcgen05); then the
 //          tcgen05 products [T; R] diag(beta gamma) K and [T; R] diag(beta) V
