@@ -1178,7 +1178,9 @@ constexpr int kOutSmem = kOOffBar + 64 + 1024;
 // started (separate chunk and state kernels): they load before the wait.
 // 0 = they come from the grid this one follows, which published each chunk
 // unit with a flag: the unit's flag is acquired, then they load, still before
-// the wait (the state images load after it).
+// the wait (the state images load after it). That grid triggers this launch
+// only after all its units are published, so the flag is set when read: the
+// acquire orders memory, it does not wait for a running producer.
 __global__ void __launch_bounds__(256, 2) output_kernel(LayerArgs A, Rows R, int Ttot, Ws W,
                                                         const __grid_constant__ CUtensorMap omap,
                                                         const __grid_constant__ CUtensorMap zmap, int early) {
