@@ -309,9 +309,8 @@ def phase_verify(gdn, world, steps, warmup, peak_hbm):
         d["cks"] = torch.empty((P, K, s.nv, s.dk, s.dv), dtype=torch.float32, device="cuda")
         d["ckc"] = torch.empty((P, K, 3, s.C), dtype=torch.bfloat16, device="cuda")
         d["idx"] = torch.zeros(P, dtype=torch.int32, device="cuda")
-        L = d["accept_len"].tolist()
-        win = max(range(P), key=lambda p: (L[p], -p))
-        d["src"] = torch.tensor([win * K + L[win] - 1 if L[win] > 0 else -1], dtype=torch.int32, device="cuda")
+        _, src = gdn.commit_source_slot(d["accept_len"].tolist(), K)  # the winner's checkpoint, -1 = none
+        d["src"] = torch.tensor([src], dtype=torch.int32, device="cuda")
         d["dst"] = torch.zeros(1, dtype=torch.int32, device="cuda")
         d["dims"] = _dims(gdn, s, P, K, 1)
         d["inp"] = _inp(gdn, d, state_idx=d["idx"])

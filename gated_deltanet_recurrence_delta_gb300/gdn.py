@@ -153,6 +153,22 @@ def state_copy(dims: Dims, src_state, src_conv, dst_state, dst_conv, src_slot, d
                                          int(n_src_slots), int(n_dst_slots), _stream(stream)))
 
 
+def commit_source_slot(accept_len, T: int) -> tuple[int, int]:
+    """The checkpoint to commit after a verify call of len(accept_len) paths x T
+    draft tokens: (winner path, checkpoint slot for gdn_state_copy's src_slot).
+
+    generate.py (sparkle, mlx_streaming/mtp), commit_tree_row(row, accepted_len):
+    the winner is the first path with the longest accept length (ties go to the
+    lower index); its checkpoint slot is winner * T + L - 1, the state after its
+    L accepted tokens. L = 0 commits nothing: slot -1 (gdn_state_copy skips it).
+    Host arithmetic only."""
+    L = [int(x) for x in accept_len]
+    if not L or any(x < 0 or x > T for x in L):
+        raise ValueError("accept lengths must lie in [0, T] and there must be at least one path")
+    win = max(range(len(L)), key=lambda p: (L[p], -p))
+    return win, (win * T + L[win] - 1 if L[win] > 0 else -1)
+
+
 def check_status(stream=None):
     """Synchronise the stream and raise on a device-detected error."""
     _check(load_library().gdn_check_status(_stream(stream)))

@@ -5,6 +5,7 @@ import ctypes
 import re
 from pathlib import Path
 
+import numpy as np
 import pytest
 
 from gated_deltanet_recurrence_delta_gb300 import build, gdn
@@ -157,3 +158,31 @@ def test_state_copy_validation(lib):
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError):
         gdn.load_library(tmp_path / "missing" / "libgdn.so")
+
+
+def test_commit_source_slot_reading():
+    """The commit rule of the speculative verify (generate.py, sparkle:
+    commit_tree_row): first path with the longest accept length, its checkpoint
+    winner * T + L - 1, nothing (-1) when no token is accepted."""
+    from gated_deltanet_recurrence_delta_gb300 import gdn
+    assert gdn.commit_source_slot([3, 5, 5, 0], 8) == (1, 1 * 8 + 4)
+    assert gdn.commit_source_slot([0, 0, 0], 8) == (0, -1)
+    assert gdn.commit_source_slot([8, 2], 8) == (0, 7)
+    assert gdn.commit_source_slot([1], 1) == (0, 0)
+    assert gdn.commit_source_slot([2, 7, 1, 7, 7], 7) == (1, 7 + 6)
+    with pytest.raises(ValueError):
+        gdn.commit_source_slot([9], 8)
+    with pytest.raises(ValueError):
+        gdn.commit_source_slot([], 8)
+
+
+def test_commit_source_slot_matches_argmax_definition():
+    """Against numpy's argmax (first maximum) on random accept lengths: the
+    winner and its flat checkpoint index agree on every draw."""
+    from gated_deltanet_recurrence_delta_gb300 import gdn
+    rng = np.random.default_rng(7)
+    for _ in range(500):
+        P, T = int(rng.integers(1, 12)), int(rng.integers(1, 10))
+        L = rng.integers(0, T + 1, size=P)
+        win = int(np.argmax(L))
+        assert gdn.commit_source_slot(L, T) == (win, win * T + int(L[win]) - 1 if L[win] > 0 else -1)
