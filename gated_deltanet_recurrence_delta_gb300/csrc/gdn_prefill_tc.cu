@@ -326,8 +326,10 @@ __global__ void __launch_bounds__(256, 4) front_kernel(LayerArgs A, Rows R, int 
 
 // ------------------------------------------------------------ chunk-local
 
-// Shared memory of chunk_kernel (bytes from a 1024-aligned base). "hi"/"lo"
-// are the two fp16 parts of a split operand.
+// Shared memory of a chunk unit (chunk_kernel, chunk_state_kernel; bytes from
+// a 1024-aligned base). "hi"/"lo" are the two fp16 parts of a split operand.
+// The K|Q region [0, 64 KiB) and the A / T / [T; R] / P region [128, 192 KiB)
+// below are the layout of an even unit; an odd unit swaps the two.
 constexpr int kOffKQH = 0;       // [2 kb][128 rows][128 B]: K rows 0-63 | Q rows 64-127 (hi); later W|Q'
 constexpr int kOffKQL = 32768;   // the same, lo parts
 constexpr int kOffB2H = 65536;   // V image [2 kb][64 rows][128 B] (hi), then the lo parts at +16 KiB;
@@ -368,8 +370,11 @@ struct UnitPhase {
 // initialised the barriers at kOffBar, holds 256 TMEM columns at `tmem`
 // and has synchronised the CTA since any earlier use of shared memory or TMEM.
 // publish: once the unit's outputs are complete in global memory, set its
-// flag (release, GPU scope) for a chain pass of the same grid. Returns false
-// when a bounded wait ran out (the status word is set).
+// flag (release, GPU scope) for a chain pass of the same grid. Without
+// publish the unit returns with its output stores possibly still reading
+// shared memory; the next unit waits for them before it reuses those regions,
+// and the caller before the CTA exits. Returns false when a bounded wait ran
+// out (the status word is set).
 template <class FindNext>
 __device__ __forceinline__ bool chunk_unit(unsigned char *sm, const LayerArgs &A, const Rows &R, const Ws &W, int s,
                                            int h, int r, int c, int parity, bool kq_issued, FindNext find_next,
