@@ -55,11 +55,28 @@ def peaks():
     return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
-def csrc_hash() -> str:
-    """Hash of the kernel sources' code: comments and whitespace are dropped, so
-    an edit of comments alone keeps the counters taken on the same code."""
+# The sources each kernel's code is built from (its own file, the headers it
+# includes, and the host dispatch): recorded DRAM counters stay valid while
+# these are unchanged, whatever happens to the other kernels' files.
+_COMMON_SOURCES = ("gdn_common.cuh", "gdn_launch.h", "gdn_api.cu")
+_PREFILL_SOURCES = ("gdn_prefill_tc.cu", "gdn_token.cuh", "gdn_umma.cuh") + _COMMON_SOURCES
+KERNEL_SOURCES = {
+    "decode_kernel": ("gdn_decode.cu", "gdn_token.cuh") + _COMMON_SOURCES,
+    "verify_split_kernel": ("gdn_verify.cu", "gdn_token.cuh") + _COMMON_SOURCES,
+    "state_copy_kernel": ("gdn_state_copy.cu",) + _COMMON_SOURCES,
+    **{k: _PREFILL_SOURCES for k in ("front_kernel", "chunk_state_kernel", "output_kernel", "chunk_kernel",
+                                     "state_kernel", "prefill_call_512")},
+}
+
+
+def csrc_hash(kernel: str | None = None) -> str:
+    """Hash of the code of `kernel`'s sources (all kernel sources when None):
+    comments and whitespace are dropped, so an edit of comments alone keeps the
+    counters taken on the same code."""
     h = hashlib.sha256()
-    for p in sorted((ROOT / "gated_deltanet_recurrence_delta_gb300" / "csrc").glob("*")):
+    csrc = ROOT / "gated_deltanet_recurrence_delta_gb300" / "csrc"
+    files = [csrc / f for f in sorted(KERNEL_SOURCES[kernel])] if kernel else sorted(csrc.glob("*"))
+    for p in files:
         t = p.read_text(errors="replace")
         t = re.sub(r"/\*.*?\*/", " ", t, flags=re.S)
         t = re.sub(r"//[^\n]*", " ", t)
@@ -76,7 +93,7 @@ def dram_traffic(kernel: str):
         return None
     d = json.loads(p.read_text())
     e = d.get(kernel)
-    if not e or e.get("csrc_hash") != csrc_hash():
+    if not e or e.get("csrc_hash") != csrc_hash(kernel):
         return None
     return float(e["bytes_per_launch"])
 
