@@ -173,3 +173,34 @@ def test_tensor_core_path_gqa_groups(oracle_mod, nk, nv):
     assert torch.count_nonzero(out[1, 61:].float()) == 0
     assert_state(S, ref["state"])
     assert torch.equal(conv.cpu().double(), torch.from_numpy(ref["conv_state"]))
+
+
+def test_tensor_core_path_rejected_row(oracle_mod):
+    """Head size 128, three rows in one call (the chunk and state passes then
+    share one grid): a row whose mask is not ones then zeros is reported
+    (GDN_ERR_MASK) and skipped -- its state, conv tail and outputs are not
+    written -- while the other rows match the oracle."""
+    shape = I.Shape(nk=2, nv=4, dk=128, dv=128)
+    d = I.decode_batch(seed=90, B=3, shape=shape)
+    T = 130
+    acts = I.activations(shape, 3, T, torch.Generator().manual_seed(91))
+    mask = torch.ones((3, T))
+    mask[1, 40] = 0  # a hole: not a prefix of ones
+    w = _wd(d)
+    conv, S = dev(d["conv_state"]).clone(), dev(d["state"]).clone()
+    out = torch.full((3, T, shape.nv, shape.dv), 7.0, dtype=torch.bfloat16, device="cuda")
+    dm = dims(shape, 3, T, 3)
+    ws = gdn.workspace(dm)
+    dacts = {n: dev(a) for n, a in acts.items()}
+    gdn.prefill_chunked(dm, inputs(w, dacts, mask=dev(mask)), conv, S, out, ws)
+    with pytest.raises(gdn.GdnError) as e:
+        gdn.check_status()
+    assert e.value.name == "GDN_ERR_MASK"
+    assert torch.equal(S[1].cpu(), d["state"][1]) and torch.equal(conv[1].cpu(), d["conv_state"][1])
+    assert bool(torch.all(out[1].float() == 7.0))
+    for r in (0, 2):
+        ra = {n: a[r:r + 1] for n, a in acts.items()}
+        ref = oracle_layer(oracle_mod, shape, d, ra, d["conv_state"][r:r + 1], d["state"][r:r + 1])
+        assert_out(out[r:r + 1], ref["out"], f"row {r}")
+        assert_state(S[r], ref["state"][0], f"row {r}")
+        assert torch.equal(conv[r].cpu().double(), torch.from_numpy(ref["conv_state"][0]))
