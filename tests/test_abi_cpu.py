@@ -186,3 +186,47 @@ def test_commit_source_slot_matches_argmax_definition():
         L = rng.integers(0, T + 1, size=P)
         win = int(np.argmax(L))
         assert gdn.commit_source_slot(L, T) == (win, win * T + int(L[win]) - 1 if L[win] > 0 else -1)
+
+
+C_CALLER = r"""
+#include <stdio.h>
+#include <string.h>
+#include "gdn.h"
+
+int main(void) {
+  /* a Qwen3.5-9B-like layer, one 512-token prefill call */
+  gdn_dims d;
+  memset(&d, 0, sizeof d);
+  d.B = 1; d.T = 512; d.nk = 16; d.nv = 32; d.dk = 128; d.dv = 128; d.conv_k = 4; d.n_slots = 1;
+  d.scale = 0.08838834764831845f; d.l2_eps = 1e-6f; d.rms_eps = 1e-6f;
+  size_t ws = gdn_prefill_workspace_size(&d);
+  /* a decode step without inputs: rejected on the host */
+  d.T = 1;
+  gdn_status st = gdn_decode_step(&d, NULL, NULL, NULL, NULL, NULL);
+  const char *msg = gdn_last_error();
+  printf("%zu %d %d\n", ws, (int)st, msg != NULL && msg[0] != '\0');
+  return 0;
+}
+"""
+
+
+def test_plain_c_caller(lib, tmp_path):
+    """A C99 program with no CUDA or C++ headers includes gdn.h, links libgdn
+    and calls it: the boundary is a plain C ABI. Only host-validated calls are
+    made, so no GPU is needed."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc is not installed")
+    src = tmp_path / "caller.c"
+    src.write_text(C_CALLER)
+    exe = tmp_path / "caller"
+    libdir = Path(gdn.LIB_PATH).parent
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", str(ROOT / "include"),
+                    str(src), "-o", str(exe), "-L", str(libdir), "-lgdn", f"-Wl,-rpath,{libdir}"], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
+    ws, st, has_msg = int(out[0]), int(out[1]), int(out[2])
+    assert ws == gdn.prefill_workspace_size(gdn.make_dims(B=1, T=512, nk=16, nv=32, dk=128, dv=128, n_slots=1))
+    assert ws > 0
+    assert st == 1 and has_msg == 1  # GDN_ERR_ARG with a message
