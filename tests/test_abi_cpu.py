@@ -230,3 +230,17 @@ def test_plain_c_caller(lib, tmp_path):
     assert ws == gdn.prefill_workspace_size(gdn.make_dims(B=1, T=512, nk=16, nv=32, dk=128, dv=128, n_slots=1))
     assert ws > 0
     assert st == 1 and has_msg == 1  # GDN_ERR_ARG with a message
+
+
+def test_bench_kernel_source_map_is_complete():
+    """Every source the bench maps a kernel to exists (a renamed file would
+    break the DRAM-traffic check), and each kernel's code hash computes."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_for_test", ROOT / "bench.py")
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    csrc = ROOT / "gated_deltanet_recurrence_delta_gb300" / "csrc"
+    for kernel, files in bench.KERNEL_SOURCES.items():
+        for f in files:
+            assert (csrc / f).is_file(), f"{kernel}: {f} missing"
+        assert re.fullmatch(r"[0-9a-f]{16}", bench.csrc_hash(kernel))
