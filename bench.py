@@ -59,7 +59,7 @@ def peaks():
 # includes, and the host dispatch): recorded DRAM counters stay valid while
 # these are unchanged, whatever happens to the other kernels' files.
 _COMMON_SOURCES = ("gdn_common.cuh", "gdn_launch.h", "gdn_api.cu")
-_PREFILL_SOURCES = ("gdn_prefill_tc.cu", "gdn_token.cuh", "gdn_umma.cuh") + _COMMON_SOURCES
+_PREFILL_SOURCES = ("gdn_prefill_tc.cu", "gdn_prefill.cu", "gdn_token.cuh", "gdn_umma.cuh") + _COMMON_SOURCES
 KERNEL_SOURCES = {
     "decode_kernel": ("gdn_decode.cu", "gdn_token.cuh") + _COMMON_SOURCES,
     "verify_split_kernel": ("gdn_verify.cu", "gdn_token.cuh") + _COMMON_SOURCES,
@@ -408,7 +408,7 @@ def phase_varlen(gdn, world, steps, warmup, peak_tf, n_layers=24):
         d["dims"] = _dims(gdn, s, 32, total, 32)
         d["inp"] = _inp(gdn, d, mask=d["mask"][0], cu_seqlens=d["cu_dev"])
         layers.append(d)
-    ws = gdn.workspace(layers[0]["dims"])
+    ws = gdn.workspace(layers[0]["dims"], packed=True)
     real = sum(layers[0]["real"])
     padded = int(layers[0]["cu_seqlens"][-1])
 

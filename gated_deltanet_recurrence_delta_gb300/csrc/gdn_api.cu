@@ -169,6 +169,20 @@ LayerArgs make_args(const gdn_dims *d, const gdn_inputs *in, void *conv_state, f
 
 }  // namespace
 
+namespace gdn {
+gdn_status validate_prefill(const gdn_dims *dims, const gdn_inputs *in, const void *conv_state,
+                            const float *recurrent_state, const void *out) {
+  GDN_TRY(check_dims(dims, true));
+  GDN_TRY(check_inputs(in, true));
+  GDN_TRY(check_ptr(conv_state, "conv_state"));
+  GDN_TRY(check_ptr(recurrent_state, "recurrent_state"));
+  GDN_TRY(check_ptr(out, "out"));
+  if ((long long)(in->cu_seqlens ? 1 : dims->B) * dims->T > (1LL << 31) - 1)
+    return fail(GDN_ERR_SHAPE, "too many tokens in one call");
+  return GDN_OK;
+}
+}  // namespace gdn
+
 extern "C" {
 
 gdn_status gdn_decode_step(const gdn_dims *dims, const gdn_inputs *in, void *conv_state, float *recurrent_state,
@@ -205,23 +219,16 @@ gdn_status gdn_verify_with_checkpoints(const gdn_dims *dims, const gdn_inputs *i
   return launch_verify(A, ckpt_state, static_cast<bf16 *>(ckpt_conv), static_cast<cudaStream_t>(stream));
 }
 
-size_t gdn_prefill_workspace_size(const gdn_dims *dims) {
+size_t gdn_prefill_workspace_size(const gdn_dims *dims, int packed) {
   if (check_dims(dims, true) != GDN_OK) return 0;
-  // Enough for either layout: dense holds B*T tokens, packed holds T.
   const int B = dims->B > 1 ? dims->B : 1;
-  return prefill_workspace_bytes(B, dims->T, dims->nk, dims->nv, dims->dk, false);
+  return prefill_workspace_bytes(B, dims->T, dims->nk, dims->nv, dims->dk, packed != 0);
 }
 
 gdn_status gdn_prefill_chunked(const gdn_dims *dims, const gdn_inputs *in, void *conv_state, float *recurrent_state,
                                void *out, void *workspace, size_t workspace_bytes, void *stream) {
-  GDN_TRY(check_dims(dims, true));
-  GDN_TRY(check_inputs(in, true));
-  GDN_TRY(check_ptr(conv_state, "conv_state"));
-  GDN_TRY(check_ptr(recurrent_state, "recurrent_state"));
-  GDN_TRY(check_ptr(out, "out"));
+  GDN_TRY(validate_prefill(dims, in, conv_state, recurrent_state, out));
   const bool packed = in->cu_seqlens != nullptr;
-  if ((long long)(packed ? 1 : dims->B) * dims->T > (1LL << 31) - 1)
-    return fail(GDN_ERR_SHAPE, "too many tokens in one call");
   if (dims->B == 0 || dims->T == 0) return GDN_OK;
   const size_t need = prefill_workspace_bytes(dims->B, dims->T, dims->nk, dims->nv, dims->dk, packed);
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < need)

@@ -46,6 +46,11 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Host checks of a prefill call (dims, inputs, pointers, token count), as
+// gdn_prefill_chunked runs them before anything else: GDN_OK or the error.
+gdn_status validate_prefill(const gdn_dims *dims, const gdn_inputs *in, const void *conv_state,
+                            const float *recurrent_state, const void *out);
+
 gdn_status launch_decode(const LayerArgs &A, cudaStream_t stream);
 gdn_status launch_verify(const LayerArgs &A, float *ckpt_state, bf16 *ckpt_conv, cudaStream_t stream);
 size_t prefill_workspace_bytes(int B, int T, int nk, int nv, int D, bool packed);

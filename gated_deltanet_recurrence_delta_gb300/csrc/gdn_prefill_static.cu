@@ -7,8 +7,13 @@
 // where a cudaMalloc could block, fail or synchronise the device.
 //
 // The scratch is one file-scope __device__ array of kStaticScratchBytes
-// (64 MiB) per GPU; every GPU on which this entry point has run keeps it until
-// the process exits. All calls on a device share it, and it keeps whatever
+// (64 MiB) per GPU. With lazy module loading (the CUDA default) the array is
+// reserved on a GPU when this entry point first runs there and kept until the
+// process exits; with CUDA_MODULE_LOADING=EAGER every GPU whose context the
+// process creates reserves it at context creation, whether or not it ever
+// calls this entry point. The cached device address stays valid for the life
+// of the device's primary context: cudaDeviceReset must not be called while
+// the library is in use. All calls on a device share it, and it keeps whatever
 // the last call left there (the prefill overwrites every byte it reads, so
 // nothing needs clearing). Two calls that overlap on the GPU (different
 // streams, no ordering between them) race on it.
@@ -52,16 +57,16 @@ using namespace gdn;
 extern "C" gdn_status gdn_prefill_chunked_static_scratch(const gdn_dims *dims, const gdn_inputs *in,
                                                          void *conv_state, float *recurrent_state, void *out,
                                                          void *stream) {
-  if (!dims) return fail(GDN_ERR_ARG, "dims is NULL");
-  if (!in) return fail(GDN_ERR_ARG, "inputs is NULL");
-  if (dims->B > 0 && dims->T > 0 && dims->nk > 0 && dims->nv > 0 && dims->dk > 0) {
-    const size_t need =
-        prefill_workspace_bytes(dims->B, dims->T, dims->nk, dims->nv, dims->dk, in->cu_seqlens != nullptr);
-    if (need > kStaticScratchBytes)
-      return fail(GDN_ERR_WORKSPACE,
-                  "this prefill needs more scratch than the 64 MiB static array holds; use gdn_prefill_chunked "
-                  "with a workspace");
-  }
+  // the same host checks as gdn_prefill_chunked, before the array is touched:
+  // a call that fails them, or has nothing to do, never loads it
+  if (gdn_status st = validate_prefill(dims, in, conv_state, recurrent_state, out)) return st;
+  if (dims->B == 0 || dims->T == 0) return GDN_OK;
+  const size_t need =
+      prefill_workspace_bytes(dims->B, dims->T, dims->nk, dims->nv, dims->dk, in->cu_seqlens != nullptr);
+  if (need > kStaticScratchBytes)
+    return fail(GDN_ERR_WORKSPACE,
+                "this prefill needs more scratch than the 64 MiB static array holds; use gdn_prefill_chunked "
+                "with a workspace");
   void *scratch = nullptr;
   if (gdn_status st = scratch_address(&scratch)) return st;
   return gdn_prefill_chunked(dims, in, conv_state, recurrent_state, out, scratch, kStaticScratchBytes, stream);

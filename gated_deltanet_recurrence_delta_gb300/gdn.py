@@ -59,7 +59,7 @@ def load_library(path: Path | str | None = None):
     lib.gdn_verify_with_checkpoints.argtypes = [DP, IP, P, P, P, P, P, P]
     lib.gdn_prefill_chunked.argtypes = [DP, IP, P, P, P, P, ctypes.c_size_t, P]
     lib.gdn_prefill_chunked_static_scratch.argtypes = [DP, IP, P, P, P, P]
-    lib.gdn_prefill_workspace_size.argtypes = [DP]
+    lib.gdn_prefill_workspace_size.argtypes = [DP, ctypes.c_int]
     lib.gdn_prefill_workspace_size.restype = ctypes.c_size_t
     lib.gdn_state_copy.argtypes = [DP, P, P, P, P, P, P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, P]
     lib.gdn_check_status.argtypes = [P]
@@ -125,8 +125,9 @@ def verify_with_checkpoints(dims: Dims, inputs: Inputs, conv_state, recurrent_st
         _ptr(ckpt_state), _ptr(ckpt_conv), _stream(stream)))
 
 
-def prefill_workspace_size(dims: Dims) -> int:
-    return int(load_library().gdn_prefill_workspace_size(ctypes.byref(dims)))
+def prefill_workspace_size(dims: Dims, packed: bool = False) -> int:
+    """Workspace bytes of a prefill call: dense rows, or packed rows (cu_seqlens)."""
+    return int(load_library().gdn_prefill_workspace_size(ctypes.byref(dims), int(bool(packed))))
 
 
 def prefill_chunked(dims: Dims, inputs: Inputs, conv_state, recurrent_state, out, workspace, workspace_bytes=None,
@@ -174,7 +175,8 @@ def check_status(stream=None):
     _check(load_library().gdn_check_status(_stream(stream)))
 
 
-def workspace(dims: Dims, device="cuda") -> torch.Tensor:
-    """A workspace tensor for gdn_prefill_chunked (torch allocations are 256-byte aligned)."""
-    n = prefill_workspace_size(dims)
+def workspace(dims: Dims, packed: bool = False, device="cuda") -> torch.Tensor:
+    """A workspace tensor for gdn_prefill_chunked (torch allocations are
+    256-byte aligned); packed: the call passes cu_seqlens."""
+    n = prefill_workspace_size(dims, packed)
     return torch.empty(max(n, 1), dtype=torch.uint8, device=device)

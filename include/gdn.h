@@ -141,8 +141,9 @@ gdn_status gdn_verify_with_checkpoints(const gdn_dims *dims, const gdn_inputs *i
  *   Dense layout: tensors [B][T][...]. Packed layout (cu_seqlens != NULL):
  *   tensors [1][T][...], T = total packed tokens, mask [T].
  *   out        bf16 [B][T][nv][dv] (or [1][T][nv][dv]); zero at padded tokens
- *   workspace  device scratch of at least gdn_prefill_workspace_size(dims)
- *              bytes, 256-byte aligned; its contents need not be preserved.
+ *   workspace  device scratch of at least
+ *              gdn_prefill_workspace_size(dims, cu_seqlens != NULL) bytes,
+ *              256-byte aligned; its contents need not be preserved.
  * Head size 128 runs three or four kernels: front (conv, norms, operand
  * tiles), then the chunk and state passes and the output pass. With few
  * (row, value head) chains (dense rows, at most half as many chains as the
@@ -154,19 +155,35 @@ gdn_status gdn_prefill_chunked(const gdn_dims *dims, const gdn_inputs *in, void 
                                float *recurrent_state, void *out, void *workspace,
                                size_t workspace_bytes, void *stream);
 
-/* Workspace bytes gdn_prefill_chunked needs for these dimensions (0 on invalid dims). */
-size_t gdn_prefill_workspace_size(const gdn_dims *dims);
+/* Workspace bytes gdn_prefill_chunked needs for these dimensions and layout
+ * (0 on invalid dims).
+ *   packed  0: dense rows, B rows of T tokens (cu_seqlens == NULL);
+ *           nonzero: packed rows, T = total packed tokens over B rows
+ *           (cu_seqlens != NULL).
+ * Head size 128 keeps per-chunk operand images: a dense call needs
+ * B * ceil(T/64) chunk slots, a packed call T/64 + B + 1 (each row may end in
+ * a partial chunk), so a packed call of many short rows needs far less than the
+ * dense size of the same B and T. A packed call given only the packed size
+ * runs; the dense size is always enough for either layout. */
+size_t gdn_prefill_workspace_size(const gdn_dims *dims, int packed);
 
 /* gdn_prefill_chunked for callers that cannot allocate device memory (a
  * serving engine whose pool owns all free HBM, a C host program without an
  * allocator, a latency-critical loop where cudaMalloc could block or fail).
  * No counterpart on the pages: it is a deployment variant of the call above.
  * Same arguments and results as gdn_prefill_chunked, minus the workspace: the
- * scratch is one 64 MiB device array inside this library, per GPU, held by
- * every GPU on which this entry point has run until the process exits. It
- * allocates nothing and calls no allocating routine.
+ * scratch is one 64 MiB device array inside this library, per GPU. Under lazy
+ * module loading (the CUDA default) a GPU reserves it when this entry point
+ * first runs there and holds it until the process exits; with
+ * CUDA_MODULE_LOADING=EAGER every GPU whose context the process creates
+ * reserves it at once. It allocates nothing and calls no allocating routine.
+ *   - The host checks of gdn_prefill_chunked run first; a call that fails them
+ *     or has nothing to do (B == 0 or T == 0) does not touch the array.
  *   - A call whose scratch need (gdn_prefill_workspace_size of its dims and
  *     layout) exceeds 64 MiB returns GDN_ERR_WORKSPACE and launches nothing.
+ *   - The array's device address is cached per device for the life of its
+ *     primary context: do not call cudaDeviceReset while libgdn is in use (the
+ *     device status word's address is cached the same way).
  *   - All calls on a device share the array and it keeps the last call's
  *     contents; calls that overlap on the GPU (unordered streams) race.
  *   - The first call on a device looks up the array's device address (set-up

@@ -123,16 +123,40 @@ def test_verify_rejects_null_checkpoints(lib):
 
 def test_prefill_workspace_rules(lib):
     d = _good_dims(T=100)
-    need = lib.gdn_prefill_workspace_size(ctypes.byref(d))
+    need = lib.gdn_prefill_workspace_size(ctypes.byref(d), 0)
     assert need > 0
     bad = _good_dims(dk=48, dv=48)
-    assert lib.gdn_prefill_workspace_size(ctypes.byref(bad)) == 0
+    assert lib.gdn_prefill_workspace_size(ctypes.byref(bad), 0) == 0
     st = lib.gdn_prefill_chunked(ctypes.byref(d), ctypes.byref(_fake_inputs()), P, P, P, P, need - 1, None)
     assert gdn.STATUS[st] == "GDN_ERR_WORKSPACE"
     st = lib.gdn_prefill_chunked(ctypes.byref(d), ctypes.byref(_fake_inputs()), P, P, P, None, need, None)
     assert gdn.STATUS[st] == "GDN_ERR_WORKSPACE"
     st = lib.gdn_prefill_chunked(ctypes.byref(d), ctypes.byref(_fake_inputs()), P, P, P, P + 16, need, None)
     assert gdn.STATUS[st] == "GDN_ERR_WORKSPACE"  # not 256-byte aligned
+
+
+def test_packed_workspace_counts_packed_slots(lib):
+    """The size query takes the layout: a packed call (cu_seqlens) of B rows and
+    T packed tokens needs T/64 + B + 1 chunk slots, a dense call B * ceil(T/64).
+    For the 32 packed varlen rows (lengths U{16..2048} padded to chunk buckets,
+    head size 128) the packed size is a small fraction of the dense one."""
+    from gated_deltanet_recurrence_delta_gb300 import inputs as I
+    _, padded, cu = I.varlen_lengths()
+    total = cu[-1]
+    d = gdn.make_dims(B=32, T=total, nk=16, nv=32, dk=128, dv=128, n_slots=32)
+    dense = gdn.prefill_workspace_size(d, packed=False)
+    packed = gdn.prefill_workspace_size(d, packed=True)
+    slots_dense, slots_packed = 32 * -(-total // 64), total // 64 + 32 + 1
+    assert 0 < packed < dense
+    # every per-slot image scales with the slot count; the per-row table is tiny
+    assert abs(packed / dense - slots_packed / slots_dense) < 1e-3
+    assert packed < 4 * 2**30
+    # one slot more per 64 packed tokens
+    d2 = gdn.make_dims(B=32, T=total + 64, nk=16, nv=32, dk=128, dv=128, n_slots=32)
+    per_slot = gdn.prefill_workspace_size(d2, packed=True) - packed
+    assert abs(per_slot * slots_packed - packed) / packed < 1e-3
+    d3 = gdn.make_dims(B=32, T=total + 128, nk=16, nv=32, dk=128, dv=128, n_slots=32)
+    assert abs(gdn.prefill_workspace_size(d3, packed=True) - packed - 2 * per_slot) <= 1024
 
 
 def test_empty_calls_launch_nothing(lib):
@@ -199,7 +223,7 @@ int main(void) {
   memset(&d, 0, sizeof d);
   d.B = 1; d.T = 512; d.nk = 16; d.nv = 32; d.dk = 128; d.dv = 128; d.conv_k = 4; d.n_slots = 1;
   d.scale = 0.08838834764831845f; d.l2_eps = 1e-6f; d.rms_eps = 1e-6f;
-  size_t ws = gdn_prefill_workspace_size(&d);
+  size_t ws = gdn_prefill_workspace_size(&d, 0);
   /* a decode step without inputs: rejected on the host */
   d.T = 1;
   gdn_status st = gdn_decode_step(&d, NULL, NULL, NULL, NULL, NULL);

@@ -30,7 +30,7 @@ def _prefill(shape, w, acts, conv, S, mask=None, cu=None, B=None, state_idx=None
     B = Bx if B is None else B
     out = torch.empty((Bx, T, shape.nv, shape.dv), dtype=torch.bfloat16, device="cuda")
     dm = dims(shape, B, T, n_slots or conv.shape[0])
-    ws = gdn.workspace(dm)
+    ws = gdn.workspace(dm, packed=cu is not None)  # exactly the size the layout needs
     gdn.prefill_chunked(dm, inputs(w, acts, mask=mask, cu=cu, state_idx=state_idx), conv, S, out, ws)
     return out
 
