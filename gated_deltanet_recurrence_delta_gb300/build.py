@@ -39,23 +39,30 @@ def _deps():
     return list(CSRC.glob("*.cu")) + list(CSRC.glob("*.cuh")) + list(CSRC.glob("*.h")) + list(INCLUDE.glob("*.h"))
 
 
-def up_to_date() -> bool:
-    if not LIB.exists():
+def up_to_date(lib: Path = LIB) -> bool:
+    if not lib.exists():
         return False
-    t = LIB.stat().st_mtime
+    t = lib.stat().st_mtime
     return all(p.stat().st_mtime <= t for p in _deps() + [Path(__file__)])
 
 
-def build(force: bool = False, verbose: bool = False) -> Path:
-    if not force and up_to_date():
-        return LIB
-    OUT_DIR.mkdir(parents=True, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, out_dir: Path | None = None,
+          defines: tuple[str, ...] = ()) -> Path:
+    """Build libgdn.so (in-tree by default). out_dir / defines: a separate
+    library built with extra preprocessor definitions (the tests' variant
+    builds), never the in-tree one."""
+    odir = Path(out_dir) if out_dir else OUT_DIR
+    lib = odir / "libgdn.so"
+    if not force and up_to_date(lib):
+        return lib
+    odir.mkdir(parents=True, exist_ok=True)
     cc = nvcc()
     srcs = _sources()
+    dflags = [f"-D{d}" for d in defines]
 
     def compile_one(src: Path) -> Path:
-        obj = OUT_DIR / (src.stem + ".o")
-        cmd = [cc, *ARCH, *NVCC_FLAGS, "-I", str(INCLUDE), "-c", str(src), "-o", str(obj)]
+        obj = odir / (src.stem + ".o")
+        cmd = [cc, *ARCH, *NVCC_FLAGS, *dflags, "-I", str(INCLUDE), "-c", str(src), "-o", str(obj)]
         if verbose:
             print(" ".join(cmd), flush=True)
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -67,13 +74,13 @@ def build(force: bool = False, verbose: bool = False) -> Path:
 
     with ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB.with_suffix(f".{os.getpid()}.tmp")
+    tmp = lib.with_suffix(f".{os.getpid()}.tmp")
     cmd = [cc, *ARCH, "-shared", "-o", str(tmp), *map(str, objs), "-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

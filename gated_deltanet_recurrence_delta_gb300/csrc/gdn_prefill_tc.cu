@@ -67,7 +67,8 @@ struct Ws {
   float *ut, *ot;       // [S][nv][64][128]     U and O_local, token-major fp32, 16-byte chunk c of
                         //                      row i stored at c ^ (i % 8) (32 KiB each)
   __half *simg;         // [S][nv][2][128][64]  fp16 image of the state at the chunk's start (32 KiB)
-  int *lr;              // [B]                  real length of each row, -1 = row rejected
+  int *lr;              // [B][nv]              real length of each row, per value head; -1 = the
+                        //                      row was rejected or the head's chain stopped
   int *flag;            // [S][nv]              chunk unit published (chunk + state in one grid)
   int2 *slot_rc;        // [S]                  (row, chunk) of each slot from the front kernel, row -1 = none
 };
@@ -87,7 +88,7 @@ size_t ws_bytes(int B, int T, int nk, int nv, bool packed) {
   const size_t S = slots_total(B, T, packed);
   return 2 * a256(S * nk * kImg * 4) + a256(S * nv * kImg * 4) + a256(S * nv * kWQ * 2) +
          a256(S * nv * kSecRec * 4) + 2 * a256(S * nv * kRowF * 4) +
-         a256(S * nv * kWQ * 2) + a256((size_t)B * 4) + a256(S * nv * 4) + a256(S * 8);
+         a256(S * nv * kWQ * 2) + a256((size_t)B * nv * 4) + a256(S * nv * 4) + a256(S * 8);
 }
 
 Ws carve(void *ws, int B, int T, int nk, int nv, bool packed) {
@@ -111,7 +112,7 @@ Ws carve(void *ws, int B, int T, int nk, int nv, bool packed) {
   w.simg = reinterpret_cast<__half *>(p);
   p += a256(S * nv * kWQ * 2);
   w.lr = reinterpret_cast<int *>(p);
-  p += a256((size_t)B * 4);
+  p += a256((size_t)B * nv * 4);
   w.flag = reinterpret_cast<int *>(p);
   p += a256(S * nv * 4);
   w.slot_rc = reinterpret_cast<int2 *>(p);
@@ -163,11 +164,18 @@ __device__ __forceinline__ void slot_row(const Rows &R, const Ws &W, int s, int 
 }
 
 // Bounded mbarrier wait agreed across the CTA (thread 0 polls, the rest sleep
-// in the barrier); false = give up.
-__device__ __forceinline__ bool cta_wait(uint64_t *bar, uint32_t parity, unsigned int *status) {
-  const bool ok = mbar_wait_leader(bar, parity, threadIdx.x == 0, [](bool p) { return __syncthreads_or(p) != 0; });
-  if (!ok && threadIdx.x == 0) set_status(status, GDN_ERR_TIMEOUT);
-  return ok;
+// in the barrier); false = give up. abort (thread 0): do not wait at all, the
+// CTA leaves (thread 0 has already recorded why).
+__device__ __forceinline__ bool cta_wait(uint64_t *bar, uint32_t parity, unsigned int *status, bool abort = false) {
+  const bool lead = threadIdx.x == 0;
+  bool ok = true;
+  if (lead) ok = !abort && mbar_wait_bounded(bar, parity);
+  if (__syncthreads_or(!ok)) {
+    if (lead && !abort) set_status(status, GDN_ERR_TIMEOUT);
+    return false;
+  }
+  if (!lead) (void)mbar_try_wait(bar, parity);
+  return true;
 }
 
 // A chunk unit's completion flag: set with release semantics at GPU scope,
@@ -810,16 +818,43 @@ constexpr int kSOffSec = 180224;  // 2 x the exp(G_C - G_j) | gamma_C record, fp
 constexpr int kSOffBar = 180800;  // barriers, TMEM base
 constexpr int kStateSmem = kSOffBar + 64 + 1024;
 
+// Polls of a unit flag before a blocking wait gives up (about a quarter of a
+// second with the 64 ns sleeps between polls).
+#ifndef GDN_FLAG_WAIT_CAP
+#define GDN_FLAG_WAIT_CAP (1u << 22)
+#endif
+
+// A chain's reads of the unit flags. The test build that checks the expiry of
+// the chains' flag waits (GDN_TEST_CHAIN_FLAGS_UNSET) reads every flag as
+// unset, as if no unit were ever published; nothing else changes.
+__device__ __forceinline__ bool chain_flag_relaxed(const int *flag) {
+#ifdef GDN_TEST_CHAIN_FLAGS_UNSET
+  (void)flag;
+  return false;
+#else
+  return relaxed_flag(flag);
+#endif
+}
+__device__ __forceinline__ bool chain_flag_acquire(const int *flag) {
+#ifdef GDN_TEST_CHAIN_FLAGS_UNSET
+  (void)flag;
+  return false;
+#else
+  return acquire_flag(flag);
+#endif
+}
+
 // Thread 0: is the chunk unit behind `flag` published? With `block`, wait for
-// it (bounded; false and a recorded timeout when it never comes).
-__device__ __forceinline__ bool unit_ready(const int *flag, bool block, unsigned int *status) {
+// it (bounded; false and a recorded timeout when it never comes). chain: the
+// reader is a state chain (see chain_flag_acquire).
+__device__ __forceinline__ bool unit_ready(const int *flag, bool block, unsigned int *status, bool chain) {
   for (uint32_t i = 0;; ++i) {
-    if (acquire_flag(flag)) {
+    if (chain ? chain_flag_acquire(flag) : acquire_flag(flag)) {
       fence_proxy_async_global();  // the unit's bulk writes, before this thread's bulk reads
       return true;
     }
     if (!block) return false;
-    if (i == (1u << 22)) {
+    if (i >= (uint32_t)GDN_FLAG_WAIT_CAP) {
       set_status(status, GDN_ERR_TIMEOUT);
       return false;
     }
@@ -828,22 +863,20 @@ __device__ __forceinline__ bool unit_ready(const int *flag, bool block, unsigned
 }
 
 // What the (row b, value head h) chain needs before its chunks, and nothing
-// of theirs: the row's checks (slot, mask of ones then zeros -> real length,
-// recorded for the output pass) and the conv-tail update of the head's own
-// channels. False when the row is rejected (its status is set). With
-// prefetch_state the head's fp32 state is fetched into L2 for the chain.
+// of theirs: the row's checks (slot, mask of ones then zeros -> real length
+// Lr, recorded per head for the output pass). False when the row is rejected
+// (its status is set). With prefetch_state the head's fp32 state is fetched
+// into L2 for the chain.
 __device__ __forceinline__ bool chain_prologue(const LayerArgs &A, const Rows &R, int Ttot, const Ws &W, int b,
-                                               int h, bool prefetch_state) {
+                                               int h, bool prefetch_state, int &Lr_out) {
   __shared__ int s_min_zero, s_max_one, s_bad;
   const int tid = threadIdx.x;
-  const int kh = h / A.G;
-  const int kd = A.nk * HD, C = A.C;
   const int start = R.start(b), len = R.len(b);
   const int slot = row_slot(A, b);
   if (slot < 0 || start < 0 || len < 0 || start + len > Ttot) {
     if (tid == 0) {
       set_status(A.status, GDN_ERR_INDEX);
-      if (h == 0) W.lr[b] = -1;
+      W.lr[(size_t)b * A.nv + h] = -1;
     }
     return false;
   }
@@ -866,12 +899,30 @@ __device__ __forceinline__ bool chain_prologue(const LayerArgs &A, const Rows &R
   if (s_bad || s_max_one >= Lr) {
     if (tid == 0) {
       set_status(A.status, GDN_ERR_MASK);
-      if (h == 0) W.lr[b] = -1;
+      W.lr[(size_t)b * A.nv + h] = -1;
     }
     return false;
   }
-  if (tid == 0 && h == 0) W.lr[b] = Lr;  // read by the output kernel
-  // conv tail: xin rows Lr .. Lr+2 (old rows when Lr < 3), own channels only
+  if (tid == 0) W.lr[(size_t)b * A.nv + h] = Lr;  // read by the output kernel
+  Lr_out = Lr;
+  if (prefetch_state) {  // 64 KiB: two 128-byte lines per thread
+    const char *gS = reinterpret_cast<const char *>(A.state + ((size_t)slot * A.nv + h) * HD * HD);
+    prefetch_l2(gS + 256 * tid);
+    prefetch_l2(gS + 256 * tid + 128);
+  }
+  return true;
+}
+
+// After the (row b, value head h) chain completed: the conv-tail update of the
+// head's own channels (its value channels, and the q / k channels of its key
+// head when h is the first value head of the group), xin rows Lr .. Lr+2 (old
+// rows when Lr < 3). A chain that stopped leaves them as they were.
+__device__ __forceinline__ void chain_tail(const LayerArgs &A, const Rows &R, int b, int h, int Lr) {
+  const int tid = threadIdx.x;
+  const int kh = h / A.G;
+  const int kd = A.nk * HD, C = A.C;
+  const int start = R.start(b);
+  const int slot = row_slot(A, b);
   {
     bf16 *cs = A.conv_state + (size_t)slot * KC * C;
     const bool qk = (h % A.G) == 0;
@@ -891,12 +942,6 @@ __device__ __forceinline__ bool chain_prologue(const LayerArgs &A, const Rows &R
       for (int rr = 0; rr < KC; ++rr) cs[(size_t)rr * C + ch] = nv3[rr];
     }
   }
-  if (prefetch_state) {  // 64 KiB: two 128-byte lines per thread
-    const char *gS = reinterpret_cast<const char *>(A.state + ((size_t)slot * A.nv + h) * HD * HD);
-    prefetch_l2(gS + 256 * tid);
-    prefetch_l2(gS + 256 * tid + 128);
-  }
-  return true;
 }
 
 // The sequential pass of one (row b, value head h) chain, after its
@@ -932,13 +977,18 @@ __device__ __forceinline__ bool state_chain(unsigned char *sm, uint64_t *bar_ld,
     bulk_g2s(sm + kSOffSec + buf * kSecRec * 4, W.sec + sh * kSecRec, kSecRec * 4, &bar_ld[buf]);
   };
   // thread 0: the last chunk whose loads are issued, and the last chunk up to
-  // which every unit is known published and acquired
+  // which every unit is known published and acquired; gave_up: a unit's flag
+  // wait expired (no load of that chunk is in flight), the chain stops
   int issued = -1, acquired = wait_units ? -1 : n_chunks - 1;
+  bool gave_up = false;
   auto issue_when_ready = [&](int ci, bool block) {  // thread 0
-    if (ci <= acquired || unit_ready(W.flag + (size_t)(s0 + ci) * A.nv + h, block, A.status)) {
+    if (gave_up) return;
+    if (ci <= acquired || unit_ready(W.flag + (size_t)(s0 + ci) * A.nv + h, block, A.status, true)) {
       if (ci > acquired) acquired = ci;
       issue_loads(ci);
       issued = ci;
+    } else if (block) {
+      gave_up = true;
     }
   };
   // thread 0: the last chunk from `from` on up to which (consecutively) the units
@@ -948,7 +998,7 @@ __device__ __forceinline__ bool state_chain(unsigned char *sm, uint64_t *bar_ld,
     bool f[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e)
-      f[e] = from + e < n_chunks && relaxed_flag(W.flag + (size_t)(s0 + from + e) * A.nv + h);
+      f[e] = from + e < n_chunks && chain_flag_relaxed(W.flag + (size_t)(s0 + from + e) * A.nv + h);
     int seen = from - 1;
 #pragma unroll
     for (int e = 0; e < 8; ++e)
@@ -1008,7 +1058,7 @@ __device__ __forceinline__ bool state_chain(unsigned char *sm, uint64_t *bar_ld,
         }
       }
     }
-    if (!cta_wait(&bar_ld[buf], (uint32_t)((ci >> 1) & 1), A.status)) {
+    if (!cta_wait(&bar_ld[buf], (uint32_t)((ci >> 1) & 1), A.status, gave_up)) {
       ok = false;
       break;
     }
@@ -1087,6 +1137,16 @@ __device__ __forceinline__ bool state_chain(unsigned char *sm, uint64_t *bar_ld,
   return true;
 }
 
+// The end of an accepted chain: when it completed, the conv-tail update of the
+// head's channels; when it stopped (a wait expired, or this grid's units did
+// not complete), the head is marked so that the output pass writes nothing
+// for it: its state, conv-tail channels and outputs stay as they were.
+__device__ __forceinline__ void chain_finish(const LayerArgs &A, const Rows &R, const Ws &W, int b, int h, int Lr,
+                                             bool completed) {
+  if (completed) chain_tail(A, R, b, h, Lr);
+  else if (threadIdx.x == 0) W.lr[(size_t)b * A.nv + h] = -1;
+}
+
 __global__ void __launch_bounds__(256, 1) state_kernel(LayerArgs A, Rows R, int Ttot, Ws W) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -1103,7 +1163,9 @@ __global__ void __launch_bounds__(256, 1) state_kernel(LayerArgs A, Rows R, int 
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int b = blockIdx.x / A.nv, h = blockIdx.x % A.nv;
-  if (chain_prologue(A, R, Ttot, W, b, h, false)) (void)state_chain(sm, bar, bar + 2, A, R, W, b, h, tmem, false);
+  int Lr = 0;
+  if (chain_prologue(A, R, Ttot, W, b, h, false, Lr)) chain_finish(A, R, W, b, h, Lr,
+                                                                  state_chain(sm, bar, bar + 2, A, R, W, b, h, tmem, false));
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x < 32) tmem_dealloc(tmem, 256);
@@ -1137,7 +1199,8 @@ __global__ void __launch_bounds__(256, 1) chunk_state_kernel(LayerArgs A, Rows R
   griddep_wait();  // the front kernel's images and the zeroed flags are complete
   const int BH = A.B * A.nv, n_units = R.B * R.cpr * A.nv;
   const int j = (int)gridDim.x - 1 - (int)blockIdx.x;  // chain of this CTA when j < BH
-  const bool chain = j < BH && chain_prologue(A, R, Ttot, W, j / A.nv, j % A.nv, true);
+  int Lr = 0;
+  const bool chain = j < BH && chain_prologue(A, R, Ttot, W, j / A.nv, j % A.nv, true, Lr);
   UnitPhase ph{0u, 0u, 0u};
   bool ok = true;
   int parity = 0;
@@ -1156,7 +1219,9 @@ __global__ void __launch_bounds__(256, 1) chunk_state_kernel(LayerArgs A, Rows R
   // the output kernel may start once every CTA is past its units (it acquires
   // the units' flags itself and waits for this grid before the state images)
   griddep_trigger();
-  if (ok && chain) (void)state_chain(sm, bar + 3, bar + 5, A, R, W, j / A.nv, j % A.nv, tmem, true);
+  if (chain)
+    chain_finish(A, R, W, j / A.nv, j % A.nv, Lr,
+                 ok && state_chain(sm, bar + 3, bar + 5, A, R, W, j / A.nv, j % A.nv, tmem, true));
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x < 32) tmem_dealloc(tmem, 256);
@@ -1226,13 +1291,14 @@ __global__ void __launch_bounds__(256, 2) output_kernel(LayerArgs A, Rows R, int
     bulk_g2s(sm + kOOffOT, W.ot + sh * kRowF, 32768, bar_ld);
     tma_load_2d(sm + kOOffZ, &zmap, h * HD, start + t0, bar_ld);  // rows past the tensor read as zeros
   };
+  bool issued = false;  // thread 0: Q', O_local and z were requested (else its flag wait expired)
   if (tid == 0) {
-    if (early) issue_qoz();
-    else if (unit_ready(W.flag + sh, true, A.status)) issue_qoz();
+    issued = early || unit_ready(W.flag + sh, true, A.status, false);
+    if (issued) issue_qoz();
   }
   griddep_wait();  // the state pass's images and row lengths are complete
   griddep_trigger();
-  const int Lr = W.lr[r];  // < 0: the row was rejected (its status is set)
+  const int Lr = W.lr[(size_t)r * A.nv + h];  // < 0: rejected row or stopped chain (its status is set)
   const int ntok = min(CH, len - t0), nreal = Lr < 0 ? 0 : max(0, min(CH, Lr - t0));
   // padded tokens of this chunk: zeros
   if (Lr >= 0)
@@ -1240,14 +1306,14 @@ __global__ void __launch_bounds__(256, 2) output_kernel(LayerArgs A, Rows R, int
       reinterpret_cast<uint4 *>(A.out + ((size_t)(start + t0 + e / 16) * A.nv + h) * HD)[e % 16] =
           make_uint4(0u, 0u, 0u, 0u);
   if (nreal == 0) {  // nothing to compute: let the loads in flight land, then leave
-    (void)cta_wait(bar_ld, 0, A.status);
+    (void)cta_wait(bar_ld, 0, A.status, !issued);
     goto done;
   }
-  if (tid == 0) {
+  if (tid == 0 && issued) {
     mbar_arrive_expect_tx(bar_s, 32768);
     bulk_g2s(sm + kOOffS, W.simg + sh * kWQ, 32768, bar_s);
   }
-  if (!cta_wait(bar_ld, 0, A.status)) goto done;
+  if (!cta_wait(bar_ld, 0, A.status, !issued)) goto done;
   if (!cta_wait(bar_s, 0, A.status)) goto done;
   if (tid == 0) {
     tc_fence_after();

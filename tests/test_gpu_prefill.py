@@ -93,30 +93,42 @@ def test_head_sizes_with_padding(oracle_mod, shape):
     assert torch.equal(S[2].cpu(), d["state"][2]) and torch.equal(conv[2].cpu(), d["conv_state"][2])
 
 
-def test_varlen_rows_sampled(oracle_mod):
-    """32 packed rows, lengths U{16..2048} padded to chunk buckets (mask 0 on the
-    padding), each from its own state: layer 0 of the varlen stack at full size,
-    with the oracle run on the shortest, the longest and two other rows."""
-    d = I.varlen_layer(0)
+@pytest.mark.parametrize("layer", range(24))
+def test_varlen_layer_stack(oracle_mod, layer):
+    """The packed varlen workload as the benchmark runs it, layer by layer: 32
+    rows, lengths U{16..2048} padded to chunk buckets (mask 0 on the padding),
+    each from its own state, with the layer's own weights and inputs drawn on
+    the device by the same seeded generator. Every row of every one of the 24
+    layers against the oracle: outputs at real tokens, zeros at padding, the
+    final state and the conv tail (bit for bit)."""
+    from concurrent.futures import ThreadPoolExecutor
+    d = I.varlen_layer(layer, device="cuda")
     s = d["shape"]
     cu = d["cu_seqlens"]
-    w = _wd(d)
-    acts = {n: dev(d[n]) for n in ACTS}
-    conv, S = dev(d["conv_state"]).clone(), dev(d["state"]).clone()
-    out = _prefill(s, w, acts, conv, S, mask=dev(d["mask"][0]), cu=dev(cu), B=32)
+    acts = {n: d[n] for n in ACTS}
+    conv, S = d["conv_state"].clone(), d["state"].clone()
+    out = _prefill(s, {n: d[n] for n in WEIGHTS}, acts, conv, S, mask=d["mask"][0], cu=cu.to("cuda"), B=32)
     gdn.check_status()
-    real = d["real"]
-    rows = sorted({int(np.argmin(real)), int(np.argmax(real)), 5, 17})
-    for r in rows:
+    h = {n: d[n].cpu() for n in ACTS + WEIGHTS}
+    conv0, S0, mask = d["conv_state"].cpu(), d["state"].cpu(), d["mask"].cpu()
+    out_h, S_h, conv_h = out.cpu(), S.cpu(), conv.cpu()
+    del d, acts, out, S, conv
+    real = I.varlen_lengths()[0]
+
+    def row(r):
         a, b_ = int(cu[r]), int(cu[r + 1])
-        ra = {n: d[n][:, a:b_] for n in ACTS}
-        ref = oracle_layer(oracle_mod, s, d, ra, d["conv_state"][r:r + 1], d["state"][r:r + 1],
-                           mask=d["mask"][:, a:b_])
-        Lr = real[r]
-        assert_out(out[:, a:a + Lr], ref["out"][:, :Lr], f"row {r}")
-        assert torch.count_nonzero(out[:, a + Lr:b_]) == 0
-        assert_state(S[r], ref["state"][0], f"row {r}")
-        assert torch.equal(conv[r].cpu().double(), torch.from_numpy(ref["conv_state"][0]))
+        ra = {n: h[n][:, a:b_] for n in ACTS}
+        return r, oracle_layer(oracle_mod, s, h, ra, conv0[r:r + 1], S0[r:r + 1], mask=mask[:, a:b_])
+
+    order = sorted(range(32), key=lambda r: -real[r])  # longest rows first
+    with ThreadPoolExecutor(max_workers=4) as ex:
+        for r, ref in ex.map(row, order):
+            a, b_ = int(cu[r]), int(cu[r + 1])
+            Lr = real[r]
+            assert_out(out_h[:, a:a + Lr], ref["out"][:, :Lr], f"layer {layer} row {r}")
+            assert torch.count_nonzero(out_h[:, a + Lr:b_]) == 0
+            assert_state(S_h[r], ref["state"][0], f"layer {layer} row {r}")
+            assert torch.equal(conv_h[r].double(), torch.from_numpy(ref["conv_state"][0]))
 
 
 def test_split_call_equals_whole_call(oracle_mod):
