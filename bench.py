@@ -10,7 +10,7 @@ per-token checkpoints, commit of the winner), chunked prefill (one row of
 (32 rows U{16..2048} padded to chunk buckets, 24 independent layers).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--phases decode,verify,prefill,varlen]
+                  [--phases decode,verify,decode_mxfp8,stack,prefill,varlen]
 
 --impl reference times the fp64 CPU oracle (the reference implementation of
 this path) on the same decode workload, on the host's cores.
@@ -40,6 +40,8 @@ METRIC = "GDN layer tokens/s (prefill, decode, verify) and % of HBM / tensor roo
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_BYTES = 129 * 1024 * 1024
+TRAFFIC_NOTE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch; writes still held in L2 when "
+                "the launch ends are not counted, so for write-heavy kernels this is a lower bound")
 ACTS = ("q", "k", "v", "z", "a", "b")
 WN = ("A_log", "dt_bias", "conv_w", "norm_w")
 
@@ -261,7 +263,8 @@ def phase_decode(gdn, world, steps, warmup, peak_hbm, local=0, e2e=True):
            "kernel_ms": kms, "launches_per_step": 1,
            "roofline": {"bound": "hbm", "achieved": nbytes / (kms * 1e-3) / 1e9, "peak": peak_hbm,
                         "unit": "GB/s", "frac": nbytes / (kms * 1e-3) / 1e9 / peak_hbm,
-                        "traffic": dram_traffic("decode_kernel"), "algorithmic_bytes": nbytes},
+                        "traffic": dram_traffic("decode_kernel"), "traffic_note": TRAFFIC_NOTE,
+                        "algorithmic_bytes": nbytes},
            "l2": f"inputs larger than L2: {n_sets} rotating layer buffer sets of {per_set / 2**20:.0f} MiB state",
            "clocks": clk.summary()}
     if e2e:
@@ -303,6 +306,47 @@ def phase_decode(gdn, world, steps, warmup, peak_hbm, local=0, e2e=True):
         res["e2e"] = {"value": B * world / (ems * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                       "d2h_bytes_per_step": d2h}
         del dev_in
+    del sets
+    torch.cuda.empty_cache()
+    return res
+
+
+def decode_mxfp8_bytes(s, B):
+    state = 2 * B * s.nv * s.dk * s.dv * 4
+    tok = s.C + s.vd  # e4m3 q | k | v and z, one byte each
+    per_row = tok + tok // 32 + 2 * s.nv * 2 + s.vd * 2 + 2 * 3 * s.C * 2  # + scales, a, b, out, conv tail r+w
+    weights = s.C * 4 * 2 + s.nv * 8 + s.dv * 2
+    return state + B * per_row + weights
+
+
+def phase_decode_mxfp8(gdn, world, steps, warmup, peak_hbm):
+    """The headline decode step with the token channels in MXFP8."""
+    s, B = I.QWEN35_9B, 64
+    per_set = B * s.nv * s.dk * s.dv * 4
+    n_sets = max(4, math.ceil(3 * L2_BYTES / per_set))
+    sets = []
+    for i in range(n_sets):
+        d = I.decode_batch(seed=1 + 1009 * i, B=B, device="cuda")
+        enc = {n: I.mxfp8(d[n]) for n in ("q", "k", "v", "z")}
+        d["enc"] = enc
+        d["out"] = torch.empty((B, 1, s.nv, s.dv), dtype=torch.bfloat16, device="cuda")
+        d["dims"] = _dims(gdn, s, B, 1, B)
+        d["inp"] = gdn.make_inputs_mxfp8(*(enc[n][0] for n in ("q", "k", "v", "z")),
+                                         *(enc[n][1] for n in ("q", "k", "v", "z")), d["a"], d["b"],
+                                         *(d[n] for n in WN))
+        sets.append(d)
+
+    def step(i, _):
+        d = sets[i % n_sets]
+        gdn.decode_step_mxfp8(d["dims"], d["inp"], d["conv_state"], d["state"], d["out"])
+
+    ms = timed(world, steps, warmup, step)
+    nbytes = decode_mxfp8_bytes(s, B)
+    res = {"tokens_per_s": B * world / (ms * 1e-3), "ms_per_step": ms, "tokens_per_step": B, "launches_per_step": 1,
+           "roofline": {"bound": "hbm", "kernel": "decode_kernel (MXFP8 inputs)",
+                        "achieved": nbytes / (ms * 1e-3) / 1e9, "peak": peak_hbm, "unit": "GB/s",
+                        "frac": nbytes / (ms * 1e-3) / 1e9 / peak_hbm, "algorithmic_bytes": nbytes},
+           "l2": f"inputs larger than L2: {n_sets} rotating layer buffer sets of {per_set / 2**20:.0f} MiB state"}
     del sets
     torch.cuda.empty_cache()
     return res
@@ -352,8 +396,49 @@ def phase_verify(gdn, world, steps, warmup, peak_hbm):
            "step_hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peak_hbm,
            "roofline": {"bound": "hbm", "kernel": "verify_split_kernel", "achieved": vbytes / (kms * 1e-3) / 1e9,
                         "peak": peak_hbm, "unit": "GB/s", "frac": vbytes / (kms * 1e-3) / 1e9 / peak_hbm,
-                        "traffic": dram_traffic("verify_split_kernel")}}
+                        "traffic": dram_traffic("verify_split_kernel"), "traffic_note": TRAFFIC_NOTE}}
     del sets
+    torch.cuda.empty_cache()
+    return res
+
+
+def phase_stack(gdn, world, steps, warmup, peak_hbm, n_layers=24):
+    """A 24-layer stack on per-layer pools, each step one replay of a captured
+    CUDA graph: (1) a decode token for 64 rows through every layer; (2) every
+    layer's verify of 8 paths x 8 draft tokens from one shared slot, then the
+    fused commit of the winner in all layers (one launch)."""
+    from gated_deltanet_recurrence_delta_gb300.stack import LayerStack
+    s, B = I.QWEN35_9B, 64
+    g = torch.Generator(device="cuda").manual_seed(11)
+    weights = [I.weights(s, g, device="cuda") for _ in range(n_layers)]
+    stack = LayerStack(s, weights, n_slots=B)
+    stack.state_pool.normal_(0.0, 0.1, generator=g)
+    stack.conv_pool.copy_(torch.randn(stack.conv_pool.shape, generator=g, device="cuda").to(torch.bfloat16))
+    dec = stack.capture_decode(B)
+    for acts in dec.acts:
+        for t in acts.values():
+            t.copy_(torch.randn(t.shape, generator=g, device="cuda").to(torch.bfloat16))
+    ms = timed(world, steps, warmup, lambda i, _: dec.replay())
+    nbytes = n_layers * decode_bytes(s, B)
+    res = {"decode": {"tokens_per_s": B * world / (ms * 1e-3), "layer_tokens_per_s": B * n_layers * world / (ms * 1e-3),
+                      "ms_per_step": ms, "ms_per_layer": ms / n_layers, "launches_per_step": n_layers,
+                      "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peak_hbm, "algorithmic_bytes_per_step": nbytes,
+                      "l2": f"inputs larger than L2: {n_layers} layers x {B * s.nv * s.dk * s.dv * 4 / 2**20:.0f} MiB state"}}
+    del dec
+    P, K = 8, 8
+    ver = stack.capture_verify_commit(P, K, P)
+    for acts in ver.acts:
+        for t in acts.values():
+            t.copy_(torch.randn(t.shape, generator=g, device="cuda").to(torch.bfloat16))
+    acc = torch.randint(0, K + 1, (P,), generator=g, device="cuda").to(torch.int32)
+    ver.accept_len.copy_(acc)
+    ms = timed(world, steps, warmup, lambda i, _: ver.replay())
+    nbytes = n_layers * verify_bytes(s, P, K)
+    res["verify_commit"] = {"tokens_per_s": P * K * world / (ms * 1e-3), "ms_per_step": ms,
+                            "ms_per_layer": ms / n_layers, "launches_per_step": n_layers + 1,
+                            "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peak_hbm, "algorithmic_bytes_per_step": nbytes,
+                            "l2": f"inputs larger than L2: {n_layers} layers x 128 MiB of checkpoints"}
+    del ver, stack, weights
     torch.cuda.empty_cache()
     return res
 
@@ -391,6 +476,7 @@ def phase_prefill(gdn, world, steps, warmup, peak_tf):
            "roofline": {"bound": "tensor", "kernel": "front+chunk_state+output", "achieved": flops / (kms * 1e-3) / 1e12, "peak": peak_tf,
                         "unit": "TFLOP/s", "frac": flops / (kms * 1e-3) / 1e12 / peak_tf,
                         "traffic": dram_traffic("prefill_call_512"), "traffic_scope": "one 512-token call (three kernels)",
+                        "traffic_note": TRAFFIC_NOTE,
                         "algorithmic_flops_per_token": prefill_flops_per_token(s)}}
     del d, calls, ws
     torch.cuda.empty_cache()
@@ -430,26 +516,117 @@ def phase_varlen(gdn, world, steps, warmup, peak_tf, n_layers=24):
 
 
 # ---------------------------------------------------------- CPU oracle
+#
+# The fp64 oracle as it stands (never tuned for this), on the host's cores:
+# one baseline per phase, each on the phase's own workload or a bounded
+# sample of it (stated in `sample`).
 
-def oracle_decode_rate(seconds=10.0, max_steps=None):
-    """The fp64 oracle on the decode workload (64 rows x 1 token x 32 heads),
-    repeated for about `seconds`; returns (tokens/s, steps, threads)."""
+def _oracle():
     from oracle import oracle
     oracle.build()
-    d = I.decode_batch(seed=1)
+    return oracle
+
+
+def _okw(d, s, acts, conv_state, state, threads, **extra):
+    return dict(**{n: acts[n] for n in ACTS}, **{n: d[n] for n in WN}, conv_state=conv_state, state=state,
+                nk=s.nk, nv=s.nv, dk=s.dk, dv=s.dv, n_threads=threads, **extra)
+
+
+def oracle_decode_steps(steps, rows=64, d=None):
+    """`steps` oracle decode steps over the first `rows` rows of the decode
+    workload (64 rows x 1 token x 32 heads); returns (tokens/s, seconds)."""
+    oracle = _oracle()
+    d = d or I.decode_batch(seed=1)
     s = d["shape"]
     threads = os.cpu_count() or 1
-    kw = dict(**{n: d[n] for n in ACTS}, **{n: d[n] for n in WN}, conv_state=d["conv_state"], state=d["state"],
-              nk=s.nk, nv=s.nv, dk=s.dk, dv=s.dv, n_threads=threads)
-    oracle.layer(**kw)  # load + warm
+    acts = {n: d[n][:rows] for n in ACTS}
+    kw = _okw(d, s, acts, d["conv_state"][:rows], d["state"][:rows], threads)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle.layer(**kw)
+    el = time.perf_counter() - t0
+    return rows * steps / el, el
+
+
+def cpu_decode(seconds=10.0):
+    oracle = _oracle()
+    d = I.decode_batch(seed=1)
+    oracle_decode_steps(1, d=d)  # load + warm
+    n, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        oracle_decode_steps(1, d=d)
+        n += 1
+    rate = 64 * n / (time.perf_counter() - t0)
+    return {"value": rate, "unit": "tokens/s", "cores": os.cpu_count() or 1, "kind": "oracle",
+            "sample": f"{n} full decode steps of the workload (64 rows x 32 heads), ~{seconds:.0f} s"}
+
+
+def cpu_verify(seconds=5.0):
+    """Whole verify calls: 8 paths x 8 tokens from the shared state, with the
+    per-token state and conv-tail checkpoints."""
+    oracle = _oracle()
+    d = I.verify_paths(seed=3)
+    s = d["shape"]
+    threads = os.cpu_count() or 1
+    P, K = d["q"].shape[0], d["q"].shape[1]
+    kw = _okw(d, s, d, d["conv_state"].expand(P, -1, -1), d["state"].expand(P, -1, -1, -1), threads,
+              checkpoints=True)
+    oracle.layer(**kw)
     n, t0 = 0, time.perf_counter()
     while True:
         oracle.layer(**kw)
         n += 1
-        el = time.perf_counter() - t0
-        if el >= seconds or (max_steps and n >= max_steps):
+        if time.perf_counter() - t0 >= seconds:
             break
-    return 64 * n / el, n, threads
+    rate = P * K * n / (time.perf_counter() - t0)
+    return {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} full verify calls (8 paths x 8 tokens, 64 state + conv checkpoints each)"}
+
+
+def cpu_prefill():
+    """The whole 8192-token row, one uninterrupted oracle pass."""
+    oracle = _oracle()
+    d = I.prefill_long(seed=2)
+    s = d["shape"]
+    threads = os.cpu_count() or 1
+    T = d["q"].shape[1]
+    t0 = time.perf_counter()
+    oracle.layer(**_okw(d, s, d, d["conv_state"], d["state"], threads))
+    el = time.perf_counter() - t0
+    return {"value": T / el, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"the whole workload: one row of {T} tokens, 32 heads, one pass ({el:.1f} s)"}
+
+
+def cpu_varlen(n_layers=1, stack=24):
+    """The first n_layers layers of the varlen stack in full (all 32 rows, one
+    oracle call per row, four rows at a time); the rate is real tokens per
+    second through the whole stack, from the time per layer."""
+    from concurrent.futures import ThreadPoolExecutor
+    oracle = _oracle()
+    threads = os.cpu_count() or 1
+    el, real = 0.0, None
+    for layer in range(n_layers):
+        d = I.varlen_layer(layer, device="cuda") if torch.cuda.is_available() else I.varlen_layer(layer)
+        h = {n: d[n].cpu() for n in ACTS + WN}
+        conv0, S0, mask = d["conv_state"].cpu(), d["state"].cpu(), d["mask"].cpu()
+        cu, real = d["cu_seqlens"], d["real"]
+        s = d["shape"]
+        del d
+
+        def row(r):
+            a, b_ = int(cu[r]), int(cu[r + 1])
+            oracle.layer(**_okw(h, s, {n: h[n][:, a:b_] for n in ACTS}, conv0[r:r + 1], S0[r:r + 1], threads,
+                                mask=mask[:, a:b_]))
+
+        order = sorted(range(len(real)), key=lambda r: -real[r])
+        t0 = time.perf_counter()
+        with ThreadPoolExecutor(max_workers=4) as ex:
+            list(ex.map(row, order))
+        el += time.perf_counter() - t0
+    per_layer = el / n_layers
+    return {"value": sum(real) / (per_layer * stack), "unit": "real tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n_layers} of the {stack} layers in full (all 32 rows, {sum(real)} real tokens per layer, "
+                      f"{per_layer:.1f} s per layer); the layers are alike in cost, so the stack takes {stack} x that"}
 
 
 # ------------------------------------------------------------------ main
@@ -460,8 +637,10 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
-    ap.add_argument("--phases", default="decode,verify,prefill,varlen")
+    ap.add_argument("--phases", default="decode,verify,decode_mxfp8,stack,prefill,varlen")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-varlen-layers", type=int, default=3,
+                    help="varlen layers the oracle baseline runs in full (24 = the whole stack)")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     steps, warmup = args.steps, max(3, args.warmup)
@@ -469,15 +648,23 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        oracle_decode_rate(seconds=0.0, max_steps=warmup)               # untimed warm-up steps
-        rate, n, threads = oracle_decode_rate(seconds=0.0, max_steps=steps)
+        # the oracle on the headline decode workload: W untimed then exactly K
+        # timed steps; a step is every row of the workload unless K full steps
+        # would run past ~90 s, then the first `rows` rows (a bounded sample)
+        d = I.decode_batch(seed=1)
+        _, t1 = oracle_decode_steps(1, d=d)
+        rows = 64 if steps * t1 <= 90.0 else max(1, int(64 * 90.0 / (steps * t1)))
+        oracle_decode_steps(warmup, rows=rows, d=d)
+        rate, el = oracle_decode_steps(steps, rows=rows, d=d)
+        threads = os.cpu_count() or 1
         line = {"impl": "reference", "metric": METRIC, "value": rate, "unit": "tokens/s", "n_gpus": 1,
-                "steps": steps, "warmup": warmup, "ms_per_step": 64 / rate * 1e3, "higher_is_better": True,
+                "steps": steps, "warmup": warmup, "ms_per_step": el / steps * 1e3, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": {"workload": "decode step: B=64 rows, T=1, 16 key / 32 value heads, d=128, fp32 state",
                            "global_batch": 64, "seq_len": 1, "parallelism": "host threads"},
                 "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                                 "sample": f"{n} full decode steps of the workload (64 rows x 32 heads)"},
+                                 "sample": f"{steps} timed steps after {warmup} untimed, each the oracle decode "
+                                           f"step of {rows} of the workload's 64 rows x 32 heads"},
                 "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
         return
@@ -493,20 +680,31 @@ def main():
     results = {}
     results["decode"] = phase_decode(gdn, world, steps, warmup, peak_hbm, local=local)
     clocks = results["decode"].pop("clocks")
+    # prefill calls and varlen layers take well under a second each, so their
+    # tensor roofline is the burst bf16 peak
     if "verify" in phases:
         results["verify"] = phase_verify(gdn, world, steps, warmup, peak_hbm)
+    if "decode_mxfp8" in phases:
+        results["decode_mxfp8"] = phase_decode_mxfp8(gdn, world, steps, warmup, peak_hbm)
+    if "stack" in phases:
+        results["stack"] = phase_stack(gdn, world, max(3, steps // 40), warmup, peak_hbm)
     if "prefill" in phases:
-        results["prefill"] = phase_prefill(gdn, world, max(3, steps // 400), warmup, peak_tf_sus)
+        results["prefill"] = phase_prefill(gdn, world, max(3, steps // 400), warmup, peak_tf)
     if "varlen" in phases:
-        results["varlen"] = phase_varlen(gdn, world, max(2, steps // 1000), 3, peak_tf_sus)
+        results["varlen"] = phase_varlen(gdn, world, max(2, steps // 1000), 3, peak_tf)
     gdn.check_status()
 
     dec = results["decode"]
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, n, threads = oracle_decode_rate(seconds=10.0)
-        cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-               "sample": f"{n} full decode steps of the headline workload (64 rows x 32 heads), ~10 s"}
+        cpu = cpu_decode(seconds=10.0)
+        dec["cpu_baseline"] = cpu
+        if "verify" in results:
+            results["verify"]["cpu_baseline"] = cpu_verify()
+        if "prefill" in results:
+            results["prefill"]["cpu_baseline"] = cpu_prefill()
+        if "varlen" in results:
+            results["varlen"]["cpu_baseline"] = cpu_varlen(n_layers=args.oracle_varlen_layers)
     launches = steps * dec["launches_per_step"]
     line = {
         "metric": METRIC, "value": dec["tokens_per_s"], "unit": "tokens/s", "n_gpus": world, "steps": steps,

@@ -164,6 +164,12 @@ LayerArgs make_args(const gdn_dims *d, const gdn_inputs *in, void *conv_state, f
   A.state = state;
   A.out = static_cast<bf16 *>(out);
   A.status = status;
+  A.mx = MxInputs{};
+  A.ckpt = nullptr;
+  A.n_ckpt = 0;
+  A.n_ckpt_slots = 0;
+  A.ckpt_state = nullptr;
+  A.ckpt_conv = nullptr;
   return A;
 }
 
@@ -197,6 +203,54 @@ gdn_status gdn_decode_step(const gdn_dims *dims, const gdn_inputs *in, void *con
   const DeviceInfo *dev;
   GDN_TRY(current_device(&dev));
   LayerArgs A = make_args(dims, in, conv_state, recurrent_state, out, dev->status);
+  return launch_decode(A, static_cast<cudaStream_t>(stream));
+}
+
+gdn_status gdn_decode_step_mxfp8(const gdn_dims *dims, const gdn_inputs_mxfp8 *in, void *conv_state,
+                                 float *recurrent_state, void *out, void *stream) {
+  GDN_TRY(check_dims(dims, false));
+  if (dims->T != 1) return fail(GDN_ERR_SHAPE, "decode needs T == 1");
+  if (!in) return fail(GDN_ERR_ARG, "inputs is NULL");
+  GDN_TRY(check_ptr(in->q, "q"));
+  GDN_TRY(check_ptr(in->k, "k"));
+  GDN_TRY(check_ptr(in->v, "v"));
+  GDN_TRY(check_ptr(in->z, "z"));
+  GDN_TRY(check_ptr(in->q_scale, "q_scale", 1));
+  GDN_TRY(check_ptr(in->k_scale, "k_scale", 1));
+  GDN_TRY(check_ptr(in->v_scale, "v_scale", 1));
+  GDN_TRY(check_ptr(in->z_scale, "z_scale", 1));
+  // the bf16 / fp32 members are checked as in gdn_decode_step (token channels
+  // stand in for q / k / v / z there: they are not read as bf16)
+  gdn_inputs rest = {};
+  rest.q = in->q;
+  rest.k = in->k;
+  rest.v = in->v;
+  rest.z = in->z;
+  rest.a = in->a;
+  rest.b = in->b;
+  rest.A_log = in->A_log;
+  rest.dt_bias = in->dt_bias;
+  rest.conv_w = in->conv_w;
+  rest.norm_w = in->norm_w;
+  rest.mask = in->mask;
+  rest.state_idx = in->state_idx;
+  GDN_TRY(check_inputs(&rest, false));
+  GDN_TRY(check_ptr(conv_state, "conv_state"));
+  GDN_TRY(check_ptr(recurrent_state, "recurrent_state"));
+  GDN_TRY(check_ptr(out, "out"));
+  if (dims->B == 0) return GDN_OK;
+  const DeviceInfo *dev;
+  GDN_TRY(current_device(&dev));
+  LayerArgs A = make_args(dims, &rest, conv_state, recurrent_state, out, dev->status);
+  A.q = A.k = A.v = A.z = nullptr;  // read through A.mx only
+  A.mx.q = static_cast<const uint8_t *>(in->q);
+  A.mx.k = static_cast<const uint8_t *>(in->k);
+  A.mx.v = static_cast<const uint8_t *>(in->v);
+  A.mx.z = static_cast<const uint8_t *>(in->z);
+  A.mx.qs = static_cast<const uint8_t *>(in->q_scale);
+  A.mx.ks = static_cast<const uint8_t *>(in->k_scale);
+  A.mx.vs = static_cast<const uint8_t *>(in->v_scale);
+  A.mx.zs = static_cast<const uint8_t *>(in->z_scale);
   return launch_decode(A, static_cast<cudaStream_t>(stream));
 }
 
@@ -239,6 +293,36 @@ gdn_status gdn_prefill_chunked(const gdn_dims *dims, const gdn_inputs *in, void 
   return launch_prefill(A, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
+gdn_status gdn_prefill_chunked_ckpt(const gdn_dims *dims, const gdn_inputs *in, void *conv_state,
+                                    float *recurrent_state, void *out, void *workspace, size_t workspace_bytes,
+                                    const int32_t *ckpt, int32_t n_ckpt, float *ckpt_state, void *ckpt_conv,
+                                    int32_t n_ckpt_slots, void *stream) {
+  GDN_TRY(validate_prefill(dims, in, conv_state, recurrent_state, out));
+  if (n_ckpt < 0 || n_ckpt > (1 << 20)) return fail(GDN_ERR_SHAPE, "n_ckpt must be in [0, 2^20]");
+  if (n_ckpt > 0) {
+    GDN_TRY(check_ptr(ckpt, "ckpt", 4));
+    GDN_TRY(check_ptr(ckpt_state, "ckpt_state"));
+    GDN_TRY(check_ptr(ckpt_conv, "ckpt_conv"));
+    if (n_ckpt_slots < 1) return fail(GDN_ERR_SHAPE, "n_ckpt_slots must be >= 1");
+  }
+  const bool packed = in->cu_seqlens != nullptr;
+  if (dims->B == 0 || dims->T == 0) return GDN_OK;
+  const size_t need = prefill_workspace_bytes(dims->B, dims->T, dims->nk, dims->nv, dims->dk, packed);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < need)
+    return fail(GDN_ERR_WORKSPACE, "workspace missing, not 256-byte aligned, or too small");
+  const DeviceInfo *dev;
+  GDN_TRY(current_device(&dev));
+  LayerArgs A = make_args(dims, in, conv_state, recurrent_state, out, dev->status);
+  if (n_ckpt > 0) {
+    A.ckpt = ckpt;
+    A.n_ckpt = n_ckpt;
+    A.n_ckpt_slots = n_ckpt_slots;
+    A.ckpt_state = ckpt_state;
+    A.ckpt_conv = static_cast<bf16 *>(ckpt_conv);
+  }
+  return launch_prefill(A, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
 gdn_status gdn_state_copy(const gdn_dims *dims, const float *src_state, const void *src_conv, float *dst_state,
                           void *dst_conv, const int32_t *src_slot, const int32_t *dst_slot, int32_t n,
                           int32_t n_src_slots, int32_t n_dst_slots, void *stream) {
@@ -268,6 +352,41 @@ gdn_status gdn_state_copy(const gdn_dims *dims, const float *src_state, const vo
   return launch_state_copy(src_state, static_cast<const bf16 *>(src_conv), dst_state, static_cast<bf16 *>(dst_conv),
                            src_slot, dst_slot, n, n_src_slots, n_dst_slots, state_floats, conv_elems,
                            static_cast<cudaStream_t>(stream));
+}
+
+gdn_status gdn_commit_accepted(const gdn_dims *dims, int32_t n_layers, int32_t paths, const float *ckpt_state,
+                               const void *ckpt_conv, float *state_pool, void *conv_pool, const int32_t *accept_len,
+                               const int32_t *dst_slot, int32_t *winner, void *stream) {
+  if (!dims) return fail(GDN_ERR_ARG, "dims is NULL");
+  if (dims->nk <= 0 || dims->nv <= 0 || dims->dk <= 0 || dims->dv <= 0 || dims->conv_k < 2)
+    return fail(GDN_ERR_SHAPE, "bad head dimensions");
+  if (dims->B < 0 || dims->T < 1 || dims->T > 8) return fail(GDN_ERR_SHAPE, "B must be >= 0 and 1 <= T <= 8");
+  if (dims->n_slots < 1) return fail(GDN_ERR_SHAPE, "n_slots must be >= 1");
+  if (paths < 1 || dims->B % paths != 0) return fail(GDN_ERR_SHAPE, "B must be a multiple of paths >= 1");
+  if (n_layers < 1) return fail(GDN_ERR_SHAPE, "n_layers must be >= 1");
+  if ((long long)(dims->B / paths) * n_layers > 65535) return fail(GDN_ERR_SHAPE, "too many (group, layer) pairs");
+  GDN_TRY(check_ptr(ckpt_state, "ckpt_state"));
+  GDN_TRY(check_ptr(state_pool, "state_pool"));
+  GDN_TRY(check_ptr(accept_len, "accept_len", 4));
+  GDN_TRY(check_ptr(dst_slot, "dst_slot", 4));
+  if (winner && !aligned(winner, 4)) return fail(GDN_ERR_ARG, "winner is not 4-byte aligned");
+  if ((ckpt_conv == nullptr) != (conv_pool == nullptr))
+    return fail(GDN_ERR_ARG, "ckpt_conv and conv_pool must both be given or both be NULL");
+  if (ckpt_conv) {
+    GDN_TRY(check_ptr(ckpt_conv, "ckpt_conv"));
+    GDN_TRY(check_ptr(conv_pool, "conv_pool"));
+  }
+  const size_t state_floats = (size_t)dims->nv * dims->dk * dims->dv;
+  const size_t C = 2 * (size_t)dims->nk * dims->dk + (size_t)dims->nv * dims->dv;
+  const size_t conv_elems = (size_t)(dims->conv_k - 1) * C;
+  if (state_floats % 4 != 0 || (ckpt_conv && conv_elems % 8 != 0))
+    return fail(GDN_ERR_SHAPE, "slot sizes must be multiples of 16 bytes");
+  if (dims->B == 0) return GDN_OK;
+  const DeviceInfo *dev;
+  GDN_TRY(current_device(&dev));
+  return launch_commit(ckpt_state, static_cast<const bf16 *>(ckpt_conv), state_pool, static_cast<bf16 *>(conv_pool),
+                       accept_len, dst_slot, winner, dims->B, dims->T, paths, n_layers, dims->n_slots, state_floats,
+                       conv_elems, static_cast<cudaStream_t>(stream));
 }
 
 gdn_status gdn_check_status(void *stream) {

@@ -12,6 +12,14 @@ namespace gdn {
 
 using bf16 = __nv_bfloat16;
 
+// MXFP8 token channels (decode variant): e4m3 elements, one E8M0 scale (a
+// power of two, 2^(s-127)) per 32 consecutive channels of a token. All NULL
+// for bf16 inputs.
+struct MxInputs {
+  const uint8_t *q, *k, *v, *z;          // [B][T][channels]
+  const uint8_t *qs, *ks, *vs, *zs;      // [B][T][channels / 32]
+};
+
 // Everything a layer kernel needs, in device-pointer form.
 struct LayerArgs {
   int B, T, nk, nv, D, G, C, n_slots;
@@ -26,7 +34,19 @@ struct LayerArgs {
   float *state;         // [n_slots][nv][D][D]
   bf16 *out;
   unsigned int *status; // device status word (bit n = gdn_status n)
+  MxInputs mx;          // MXFP8 q / k / v / z (decode variant); all NULL otherwise
+  // prefill checkpoints: n_ckpt (row, position, slot) triples; the state and
+  // conv tail of `row` after its first `position` tokens of the call go to
+  // slot `slot` of ckpt_state [n_ckpt_slots][nv][D][D] / ckpt_conv
+  // [n_ckpt_slots][3][C]. n_ckpt == 0: none.
+  const int32_t *ckpt;
+  int n_ckpt, n_ckpt_slots;
+  float *ckpt_state;
+  bf16 *ckpt_conv;
 };
+
+// Most checkpoints one row of a prefill call may request.
+constexpr int kMaxRowCkpt = 64;
 
 constexpr int KC = 3;  // saved conv rows (kernel width 4)
 

@@ -20,6 +20,8 @@
 //     behind the current unit's state stream; row slots are resolved once
 //     into a shared table.
 // The per-token arithmetic is the shared code of gdn_token.cuh.
+#include <cuda_fp8.h>
+
 #include "gdn_launch.h"
 #include "gdn_token.cuh"
 
@@ -44,6 +46,9 @@ struct FrontRegs {
   uint2 w[kPre];                    // 4 conv taps (bf16) per channel
   bf16 x[kPre], t0[kPre], t1[kPre], t2[kPre];
   bf16 z[kZPre];
+  // MXFP8 inputs: the raw element and scale bytes, dequantized only where they
+  // are used (converting at load time would wait for the loads a unit early)
+  uint8_t xe[kPre], xs[kPre], ze[kZPre], zs[kZPre];
   bf16 ga, gb;
   float alog, dtb;
 };
@@ -60,6 +65,62 @@ struct UnitGeom {
   }
 };
 
+// One MXFP8 element: e4m3 (exact in half precision) times its block's scale
+// 2^(s-127) (s = 0: 2^-127; s = 255: NaN, the format's NaN code). The product
+// is exact in fp32 and, inside bf16's normal range, in bf16, so the conv and
+// the saved conv tail see exactly the dequantized input.
+__device__ __forceinline__ bf16 mx_dequant(uint8_t e, uint8_t s) {
+  const float f = __half2float(__half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)e, __NV_E4M3)));
+  const float scale = s == 255 ? __int_as_float(0x7fc00000) : (s == 0 ? __int_as_float(0x00400000)
+                                                                       : __int_as_float((int)s << 23));
+  return __float2bfloat16_rn(f * scale);
+}
+
+// Addresses of the MXFP8 element and scale of token channel ch of row b.
+__device__ __forceinline__ void mx_x_at(const LayerArgs &A, const UnitGeom &U, int b, int ch, const uint8_t *&e,
+                                        const uint8_t *&sc) {
+  const int kd = U.kd, vd = U.nv * U.D;
+  if (ch < kd) {
+    e = A.mx.q + (size_t)b * kd + ch;
+    sc = A.mx.qs + (size_t)b * (kd / 32) + ch / 32;
+  } else if (ch < 2 * kd) {
+    const int c = ch - kd;
+    e = A.mx.k + (size_t)b * kd + c;
+    sc = A.mx.ks + (size_t)b * (kd / 32) + c / 32;
+  } else {
+    const int c = ch - 2 * kd;
+    e = A.mx.v + (size_t)b * vd + c;
+    sc = A.mx.vs + (size_t)b * (vd / 32) + c / 32;
+  }
+}
+// ... and of z value e of the G value heads of key head kh, row b.
+__device__ __forceinline__ void mx_z_at(const LayerArgs &A, const UnitGeom &U, int b, int kh, int e,
+                                        const uint8_t *&el, const uint8_t *&sc) {
+  const int vd = U.nv * U.D, c = kh * U.G * U.D + e;
+  el = A.mx.z + (size_t)b * vd + c;
+  sc = A.mx.zs + (size_t)b * (vd / 32) + c / 32;
+}
+
+// Token channel ch of row b (one decode token per row): the bf16 input, or the
+// dequantized MXFP8 one.
+template <bool MX>
+__device__ __forceinline__ bf16 load_x(const LayerArgs &A, const UnitGeom &U, int b, int ch) {
+  if (!MX) return *U.src(A, b, ch);
+  const uint8_t *e, *sc;
+  mx_x_at(A, U, b, ch, e, sc);
+  return mx_dequant(*e, *sc);
+}
+
+// z value e of the G value heads of key head kh, row b.
+template <bool MX>
+__device__ __forceinline__ bf16 load_z(const LayerArgs &A, const UnitGeom &U, int b, int kh, int e) {
+  if (!MX) return A.z[((size_t)b * A.nv + kh * U.G) * U.D + e];
+  const uint8_t *el, *sc;
+  mx_z_at(A, U, b, kh, e, el, sc);
+  return mx_dequant(*el, *sc);
+}
+
+template <bool MX>
 __device__ __forceinline__ void load_front(FrontRegs &R, const LayerArgs &A, const UnitGeom &U, int b, int kh,
                                            int slot, int tid) {
   const int nch = (2 + U.G) * U.D;
@@ -69,18 +130,33 @@ __device__ __forceinline__ void load_front(FrontRegs &R, const LayerArgs &A, con
     const int e = tid + 256 * i;
     if (e < nch) {
       const int ch = U.chan(e, kh);
-      R.x[i] = *U.src(A, b, ch);
+      if (MX) {
+        const uint8_t *e8, *s8;
+        mx_x_at(A, U, b, ch, e8, s8);
+        R.xe[i] = *e8;
+        R.xs[i] = *s8;
+      } else {
+        R.x[i] = *U.src(A, b, ch);
+      }
       R.t0[i] = cs[ch];
       R.t1[i] = cs[U.C + ch];
       R.t2[i] = cs[2 * U.C + ch];
       R.w[i] = *reinterpret_cast<const uint2 *>(A.conv_w + (size_t)ch * 4);
     }
   }
-  const bf16 *zb = A.z + ((size_t)b * A.nv + kh * U.G) * U.D;
 #pragma unroll
   for (int i = 0; i < kZPre; ++i) {
     const int e = tid + 256 * i;
-    if (e < U.G * U.D) R.z[i] = zb[e];
+    if (e < U.G * U.D) {
+      if (MX) {
+        const uint8_t *e8, *s8;
+        mx_z_at(A, U, b, kh, e, e8, s8);
+        R.ze[i] = *e8;
+        R.zs[i] = *s8;
+      } else {
+        R.z[i] = A.z[((size_t)b * A.nv + kh * U.G) * U.D + e];
+      }
+    }
   }
   if (tid < U.G) {
     const int hh = kh * U.G + tid;
@@ -106,7 +182,8 @@ __device__ __forceinline__ bool compute_sync_or(bool pred) {
   return r != 0;
 }
 
-template <int D, int NS>
+// MX: the token channels q / k / v / z arrive as MXFP8 (A.mx) instead of bf16.
+template <int D, int NS, bool MX>
 __global__ void __launch_bounds__(288, 1) decode_kernel(LayerArgs A) {
   using L = StateLayout<D>;
   using S = DecodeSmem<D, NS>;
@@ -212,7 +289,7 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(LayerArgs A) {
   {
     const int s0 = unit_slot(0);
     const int u0 = (int)blockIdx.x;
-    if (s0 >= 0) load_front(R, A, U, u0 / A.nk, u0 % A.nk, s0, tid);
+    if (s0 >= 0) load_front<MX>(R, A, U, u0 / A.nk, u0 % A.nk, s0, tid);
   }
 
   for (int n = 0; n < n_tasks; ++n) {
@@ -230,17 +307,18 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(LayerArgs A) {
         const int e = tid + 256 * p;
         if (e < nch) {
           const int ch = U.chan(e, kh);
+          const bf16 xv = MX ? mx_dequant(R.xe[p], R.xs[p]) : R.x[p];
           fq[e] = conv4_silu(bf_lo(R.w[p].x), bf_hi(R.w[p].x), bf_lo(R.w[p].y), bf_hi(R.w[p].y),
                              __bfloat162float(R.t0[p]), __bfloat162float(R.t1[p]), __bfloat162float(R.t2[p]),
-                             __bfloat162float(R.x[p]));
+                             __bfloat162float(xv));
           cs[ch] = R.t1[p];
           cs[A.C + ch] = R.t2[p];
-          cs[2 * A.C + ch] = R.x[p];
+          cs[2 * A.C + ch] = xv;
         }
       }
       for (int e = tid + 256 * kPre; e < nch; e += 256) {  // groups wider than the prefetch
         const int ch = U.chan(e, kh);
-        const bf16 x0 = cs[ch], x1 = cs[A.C + ch], x2 = cs[2 * A.C + ch], x3 = *U.src(A, b, ch);
+        const bf16 x0 = cs[ch], x1 = cs[A.C + ch], x2 = cs[2 * A.C + ch], x3 = load_x<MX>(A, U, b, ch);
         const bf16 *w = A.conv_w + (size_t)ch * 4;
         fq[e] = conv4_silu(ldbf(w), ldbf(w + 1), ldbf(w + 2), ldbf(w + 3), __bfloat162float(x0),
                            __bfloat162float(x1), __bfloat162float(x2), __bfloat162float(x3));
@@ -251,17 +329,17 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(LayerArgs A) {
 #pragma unroll
       for (int p = 0; p < kZPre; ++p) {
         const int e = tid + 256 * p;
-        if (e < G * D) fz[e] = __bfloat162float(R.z[p]);
+        if (e < G * D) fz[e] = __bfloat162float(MX ? mx_dequant(R.ze[p], R.zs[p]) : R.z[p]);
       }
       for (int e = tid + 256 * kZPre; e < G * D; e += 256)
-        fz[e] = ldbf(A.z + ((size_t)b * A.nv + kh * G) * D + e);
+        fz[e] = __bfloat162float(load_z<MX>(A, U, b, kh, e));
       float decay = 0.f, beta = 0.f;
       if (tid < G) gdn_gates(__bfloat162float(R.ga), __bfloat162float(R.gb), R.alog, R.dtb, decay, beta);
       // next unit's inputs, in flight while this unit's heads stream
       if (i + 1 < my_units) {
         const int s1 = unit_slot(i + 1);
         const int u1 = u + (int)gridDim.x;
-        if (s1 >= 0) load_front(R, A, U, u1 / A.nk, u1 % A.nk, s1, tid);
+        if (s1 >= 0) load_front<MX>(R, A, U, u1 / A.nk, u1 % A.nk, s1, tid);
       }
       csync();
       if (warp == 0) warp_l2norm<D>(fq, A.l2_eps, A.scale, lane);
@@ -280,7 +358,7 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(LayerArgs A) {
       // skipped unit: still prefetch the next one
       const int s1 = unit_slot(i + 1);
       const int u1 = u + (int)gridDim.x;
-      if (s1 >= 0) load_front(R, A, U, u1 / A.nk, u1 % A.nk, s1, tid);
+      if (s1 >= 0) load_front<MX>(R, A, U, u1 / A.nk, u1 % A.nk, s1, tid);
     }
 
     // ---- the value head's state
@@ -315,34 +393,35 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(LayerArgs A) {
   }
 }
 
-template <int D, int NS>
+template <int D, int NS, bool MX>
 static gdn_status launch_decode_t(const LayerArgs &A, cudaStream_t stream) {
   using S = DecodeSmem<D, NS>;
   const DeviceInfo &dev = device_info();
   // set once per device; concurrent first calls may both set it (idempotent)
   static std::atomic<bool> attr_set[kMaxDevices];
   if (!attr_set[dev.id].load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(decode_kernel<D, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::kBytes) !=
+    if (cudaFuncSetAttribute(decode_kernel<D, NS, MX>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::kBytes) !=
         cudaSuccess)
       return fail(GDN_ERR_CUDA, "decode: cannot reserve shared memory");
     attr_set[dev.id].store(true, std::memory_order_release);
   }
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<D, NS>, 288, S::kBytes) != cudaSuccess ||
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<D, NS, MX>, 288, S::kBytes) != cudaSuccess ||
       per_sm < 1)
     return fail(GDN_ERR_CUDA, "decode: kernel does not fit on an SM");
   const int n_units = A.B * A.nk;
   const int grid = n_units < dev.sms * per_sm ? n_units : dev.sms * per_sm;
-  if (launch_pdl(decode_kernel<D, NS>, dim3(grid), dim3(288), S::kBytes, stream, A) != cudaSuccess)
+  if (launch_pdl(decode_kernel<D, NS, MX>, dim3(grid), dim3(288), S::kBytes, stream, A) != cudaSuccess)
     return check_launch("decode");
   return check_launch("decode");
 }
 
 gdn_status launch_decode(const LayerArgs &A, cudaStream_t stream) {
+  const bool mx = A.mx.q != nullptr;
   switch (A.D) {
-    case 128: return launch_decode_t<128, 3>(A, stream);
-    case 64: return launch_decode_t<64, 4>(A, stream);
-    case 32: return launch_decode_t<32, 4>(A, stream);
+    case 128: return mx ? launch_decode_t<128, 3, true>(A, stream) : launch_decode_t<128, 3, false>(A, stream);
+    case 64: return mx ? launch_decode_t<64, 4, true>(A, stream) : launch_decode_t<64, 4, false>(A, stream);
+    case 32: return mx ? launch_decode_t<32, 4, true>(A, stream) : launch_decode_t<32, 4, false>(A, stream);
   }
   return fail(GDN_ERR_SHAPE, "decode: unsupported head size");
 }

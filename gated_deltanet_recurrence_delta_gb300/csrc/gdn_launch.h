@@ -57,6 +57,10 @@ size_t prefill_workspace_bytes(int B, int T, int nk, int nv, int D, bool packed)
 gdn_status launch_prefill(const LayerArgs &A, void *workspace, size_t workspace_bytes, cudaStream_t stream);
 size_t prefill_tc_workspace_bytes(int B, int T, int nk, int nv, bool packed);
 gdn_status launch_prefill_tc(const LayerArgs &A, void *workspace, cudaStream_t stream);
+gdn_status launch_commit(const float *ckpt_state, const bf16 *ckpt_conv, float *pool_state, bf16 *pool_conv,
+                         const int32_t *accept_len, const int32_t *dst_slot, int32_t *winner, int B, int T,
+                         int paths, int n_layers, int n_slots, size_t state_floats, size_t conv_elems,
+                         cudaStream_t stream);
 gdn_status launch_state_copy(const float *src_state, const bf16 *src_conv, float *dst_state, bf16 *dst_conv,
                              const int32_t *src_slot, const int32_t *dst_slot, int n, int n_src, int n_dst,
                              size_t state_floats, size_t conv_elems, cudaStream_t stream);

@@ -10,9 +10,10 @@
 //   1. front: depthwise conv + SiLU over [saved tail ; tokens] and the q/k L2
 //      norm, for every (token block, head channel group); results to the
 //      workspace (fp32). Reads the saved tail, writes nothing in place.
-//   2. recur: one CTA per (row, value head): the conv-tail update for the
-//      channels it owns, then the delta rule token by token with the state in
-//      registers, the gated RMSNorm epilogue and the final state in place.
+//   2. recur: one CTA per (row, value head): the delta rule token by token
+//      with the state in registers, the gated RMSNorm epilogue, requested
+//      checkpoints, the final state in place, then the conv-tail update of the
+//      channels it owns.
 // Kernel 2 starts only after kernel 1 has read every saved tail (stream order),
 // so the in-place tail update cannot race with the conv.
 #include "gdn_launch.h"
@@ -158,26 +159,12 @@ __global__ void __launch_bounds__(256, 2) prefill_recur_kernel(LayerArgs A, int 
     return;
   }
 
-  // ---- conv tail: xin rows Lr .. Lr+2 (old rows when Lr < 3), own channels only
-  {
-    bf16 *cs = A.conv_state + (size_t)slot * KC * C;
-    const bool qk = (h % A.G) == 0;
-    const int nch = qk ? 3 * D : D;
-    for (int e = tid; e < nch; e += 256) {
-      const int which = qk ? e / D : 2, cc = e % D;
-      const int ch = which == 0 ? kh * D + cc : (which == 1 ? kd + kh * D + cc : 2 * kd + h * D + cc);
-      const bf16 *src = which == 0 ? A.q + kh * D + cc : (which == 1 ? A.k + kh * D + cc : A.v + h * D + cc);
-      const size_t rstride = which == 2 ? (size_t)A.nv * D : (size_t)kd;
-      bf16 nv3[KC];
-#pragma unroll
-      for (int r = 0; r < KC; ++r) {
-        const int xi = Lr + r;
-        nv3[r] = xi < KC ? cs[(size_t)xi * C + ch] : src[(size_t)(start + xi - KC) * rstride];
-      }
-#pragma unroll
-      for (int r = 0; r < KC; ++r) cs[(size_t)r * C + ch] = nv3[r];
-    }
+  __shared__ RowCkpts ck;  // checkpoints this row asked for (prefix-cache states inside the call)
+  if (tid == 0) {
+    ck.n = 0;
+    if (A.n_ckpt > 0) gather_row_ckpts(A, b, h, Lr, ck);
   }
+  bf16 *cs = A.conv_state + (size_t)slot * KC * C;
 
   // ---- the delta rule, token by token
   const int cq = tid % L::TPR, grp = tid / L::TPR;
@@ -228,11 +215,22 @@ __global__ void __launch_bounds__(256, 2) prefill_recur_kernel(LayerArgs A, int 
     state_step<D>(s, F[par][0], F[par][1], F[par][2], s_gate[0], s_gate[1], s_gate[2], red, tid, o, SyncAll());
     if (warp == 0)
       rmsnorm_store_smem<D>(o, lane, F[par][3], fw, A.rms_eps, A.out + ((size_t)start + t) * A.nv * D + h * D);
+    for (int e = 0; e < ck.n; ++e) {  // checkpoints after this token: the state and the conv tail there
+      if (ck.pos[e] != t + 1) continue;
+      float4 *cS = reinterpret_cast<float4 *>(A.ckpt_state + ((size_t)ck.slot[e] * A.nv + h) * D * D);
+#pragma unroll
+      for (int i = 0; i < L::RPT; ++i) cS[(grp + i * L::NG) * L::TPR + cq] = s[i];
+      conv_tail_at<D>(A, start, h, t + 1, cs, A.ckpt_conv + (size_t)ck.slot[e] * KC * C);
+    }
     __syncthreads();  // s_gate is rewritten by the next token
   }
   for (int t = Lr; t < len; ++t) zero_head<D>(A.out + ((size_t)start + t) * A.nv * D + h * D, tid);
 #pragma unroll
   for (int i = 0; i < L::RPT; ++i) gs[(grp + i * L::NG) * L::TPR + cq] = s[i];
+  // conv tail: xin rows Lr .. Lr+2 (old rows when Lr < 3), own channels only,
+  // after the checkpoints have read the saved rows
+  __syncthreads();
+  conv_tail_at<D>(A, start, h, Lr, cs, cs);
 }
 
 template <int D>

@@ -914,34 +914,11 @@ __device__ __forceinline__ bool chain_prologue(const LayerArgs &A, const Rows &R
 }
 
 // After the (row b, value head h) chain completed: the conv-tail update of the
-// head's own channels (its value channels, and the q / k channels of its key
-// head when h is the first value head of the group), xin rows Lr .. Lr+2 (old
-// rows when Lr < 3). A chain that stopped leaves them as they were.
+// head's own channels, xin rows Lr .. Lr+2 (old rows when Lr < 3), in place.
+// A chain that stopped leaves them as they were.
 __device__ __forceinline__ void chain_tail(const LayerArgs &A, const Rows &R, int b, int h, int Lr) {
-  const int tid = threadIdx.x;
-  const int kh = h / A.G;
-  const int kd = A.nk * HD, C = A.C;
-  const int start = R.start(b);
-  const int slot = row_slot(A, b);
-  {
-    bf16 *cs = A.conv_state + (size_t)slot * KC * C;
-    const bool qk = (h % A.G) == 0;
-    const int nch = qk ? 3 * HD : HD;
-    for (int e = tid; e < nch; e += 256) {
-      const int which = qk ? e / HD : 2, cc = e % HD;
-      const int ch = which == 0 ? kh * HD + cc : (which == 1 ? kd + kh * HD + cc : 2 * kd + h * HD + cc);
-      const bf16 *src = which == 0 ? A.q + kh * HD + cc : (which == 1 ? A.k + kh * HD + cc : A.v + h * HD + cc);
-      const size_t rstride = which == 2 ? (size_t)A.nv * HD : (size_t)kd;
-      bf16 nv3[KC];
-#pragma unroll
-      for (int rr = 0; rr < KC; ++rr) {
-        const int xi = Lr + rr;
-        nv3[rr] = xi < KC ? cs[(size_t)xi * C + ch] : src[(size_t)(start + xi - KC) * rstride];
-      }
-#pragma unroll
-      for (int rr = 0; rr < KC; ++rr) cs[(size_t)rr * C + ch] = nv3[rr];
-    }
-  }
+  bf16 *cs = A.conv_state + (size_t)row_slot(A, b) * KC * A.C;
+  conv_tail_at<HD>(A, R.start(b), h, Lr, cs, cs);
 }
 
 // The sequential pass of one (row b, value head h) chain, after its
@@ -952,7 +929,7 @@ __device__ __forceinline__ void chain_tail(const LayerArgs &A, const Rows &R, in
 // chunk's loads wait for its unit's flag. Returns false when a bounded wait
 // ran out.
 __device__ __forceinline__ bool state_chain(unsigned char *sm, uint64_t *bar_ld, uint64_t *bar_mma,
-                                            const LayerArgs &A, const Rows &R, const Ws &W, int b, int h,
+                                            const LayerArgs &A, const Rows &R, const Ws &W, int b, int h, int Lr,
                                             uint32_t tmem, bool wait_units) {
   unsigned char *SI = sm + kSOffS;
   unsigned char *UP = sm + kSOffUP;
@@ -961,6 +938,11 @@ __device__ __forceinline__ bool state_chain(unsigned char *sm, uint64_t *bar_ld,
   const int len = R.len(b), slot = row_slot(A, b);
   const int n_chunks = (len + CH - 1) / CH;
   const int s0 = R.slot0(b);
+  __shared__ RowCkpts ck;  // checkpoints this row asked for (prefix-cache states inside the call)
+  if (tid == 0) {
+    ck.n = 0;
+    if (A.n_ckpt > 0) gather_row_ckpts(A, b, h, Lr, ck);
+  }
 
   // chunk ci's W rows (rows 0-63 of each column block of the W|Q' image),
   // the fp16 K image (hi) of the key head, U and exp(G_C - G)
@@ -1122,6 +1104,16 @@ __device__ __forceinline__ bool state_chain(unsigned char *sm, uint64_t *bar_ld,
 #pragma unroll
       for (int e = 0; e < 32; ++e) Sv[32 * half + e] = fmaf(gC, Sv[32 * half + e], d[e]);
     }
+    // checkpoints inside this chunk: the state at a chunk end, or at the real
+    // end Lr (the padded tokens after it change nothing), and the conv tail there
+    for (int e = 0; e < ck.n; ++e) {
+      if ((ck.pos[e] - 1) / CH != ci) continue;
+      float *cS = A.ckpt_state + ((size_t)ck.slot[e] * A.nv + h) * HD * HD;
+#pragma unroll
+      for (int k = 0; k < 64; ++k) cS[(size_t)(64 * hh + k) * HD + v] = Sv[k];
+      conv_tail_at<HD>(A, R.start(b), h, ck.pos[e], A.conv_state + (size_t)slot * KC * A.C,
+                       A.ckpt_conv + (size_t)ck.slot[e] * KC * A.C);
+    }
     write_simg();
     tc_fence_before();
     __syncthreads();
@@ -1164,8 +1156,8 @@ __global__ void __launch_bounds__(256, 1) state_kernel(LayerArgs A, Rows R, int 
   const uint32_t tmem = *tmem_slot;
   const int b = blockIdx.x / A.nv, h = blockIdx.x % A.nv;
   int Lr = 0;
-  if (chain_prologue(A, R, Ttot, W, b, h, false, Lr)) chain_finish(A, R, W, b, h, Lr,
-                                                                  state_chain(sm, bar, bar + 2, A, R, W, b, h, tmem, false));
+  if (chain_prologue(A, R, Ttot, W, b, h, false, Lr))
+    chain_finish(A, R, W, b, h, Lr, state_chain(sm, bar, bar + 2, A, R, W, b, h, Lr, tmem, false));
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x < 32) tmem_dealloc(tmem, 256);
@@ -1221,7 +1213,7 @@ __global__ void __launch_bounds__(256, 1) chunk_state_kernel(LayerArgs A, Rows R
   griddep_trigger();
   if (chain)
     chain_finish(A, R, W, j / A.nv, j % A.nv, Lr,
-                 ok && state_chain(sm, bar + 3, bar + 5, A, R, W, j / A.nv, j % A.nv, tmem, true));
+                 ok && state_chain(sm, bar + 3, bar + 5, A, R, W, j / A.nv, j % A.nv, Lr, tmem, true));
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x < 32) tmem_dealloc(tmem, 256);

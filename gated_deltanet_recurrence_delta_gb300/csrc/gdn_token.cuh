@@ -191,6 +191,67 @@ __device__ __forceinline__ void rmsnorm_store_smem(float4 o, int lane, const flo
   }
 }
 
+// The conv tail of a prefill row after its first `pos` tokens of the call, for
+// value head h's own channels: its value channels, and the q / k channels of
+// its key head when h is the first value head of the group (so every channel
+// has one writer). xin rows pos .. pos+2: rows of the saved tail `old`
+// ([3][C]) while pos + r < 3, else tokens pos + r - 3 of the row (which starts
+// at packed token `start`). Written to dst ([3][C]; may be `old` itself: each
+// thread reads its channel's three rows before writing them). All threads of
+// the CTA take part.
+template <int D>
+__device__ __forceinline__ void conv_tail_at(const LayerArgs &A, int start, int h, int pos, const bf16 *old,
+                                             bf16 *dst) {
+  const int kh = h / A.G, kd = A.nk * D, C = A.C;
+  const bool qk = (h % A.G) == 0;
+  const int nch = qk ? 3 * D : D;
+  for (int e = threadIdx.x; e < nch; e += blockDim.x) {
+    const int which = qk ? e / D : 2, cc = e % D;
+    const int ch = which == 0 ? kh * D + cc : (which == 1 ? kd + kh * D + cc : 2 * kd + h * D + cc);
+    const bf16 *src = which == 0 ? A.q + kh * D + cc : (which == 1 ? A.k + kh * D + cc : A.v + h * D + cc);
+    const size_t rstride = which == 2 ? (size_t)A.nv * D : (size_t)kd;
+    bf16 nv3[KC];
+#pragma unroll
+    for (int r = 0; r < KC; ++r) {
+      const int xi = pos + r;
+      nv3[r] = xi < KC ? old[(size_t)xi * C + ch] : src[(size_t)(start + xi - KC) * rstride];
+    }
+#pragma unroll
+    for (int r = 0; r < KC; ++r) dst[(size_t)r * C + ch] = nv3[r];
+  }
+}
+
+// The checkpoints a prefill row requested (A.ckpt triples naming row b), for
+// the chain of (row b, value head h); built by thread 0 into shared memory.
+// A triple is kept when 0 < position <= Lr, position is a multiple of 64 or
+// Lr itself, and 0 <= slot < n_ckpt_slots; otherwise, or past kMaxRowCkpt
+// per row, it is a recorded index error and skipped. The chain of (row 0,
+// head 0) also records triples whose row lies outside [0, B).
+struct RowCkpts {
+  int n;
+  int pos[kMaxRowCkpt], slot[kMaxRowCkpt];
+};
+__device__ __forceinline__ void gather_row_ckpts(const LayerArgs &A, int b, int h, int Lr, RowCkpts &L) {
+  int n = 0;
+  for (int i = 0; i < A.n_ckpt; ++i) {
+    const int r = A.ckpt[3 * i], p = A.ckpt[3 * i + 1], sl = A.ckpt[3 * i + 2];
+    if (r < 0 || r >= A.B) {
+      if (b == 0 && h == 0) set_status(A.status, GDN_ERR_INDEX);
+      continue;
+    }
+    if (r != b) continue;
+    const bool ok = p > 0 && p <= Lr && (p % 64 == 0 || p == Lr) && sl >= 0 && sl < A.n_ckpt_slots;
+    if (!ok || n == kMaxRowCkpt) {
+      set_status(A.status, GDN_ERR_INDEX);
+      continue;
+    }
+    L.pos[n] = p;
+    L.slot[n] = sl;
+    ++n;
+  }
+  L.n = n;
+}
+
 // Zero one head's bf16 output (padded tokens, skipped rows).
 template <int D>
 __device__ __forceinline__ void zero_head(bf16 *out, int tid) {

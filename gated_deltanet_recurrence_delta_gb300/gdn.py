@@ -20,7 +20,8 @@ STATUS = {0: "GDN_OK", 1: "GDN_ERR_ARG", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_MASK", 
           5: "GDN_ERR_CUDA", 6: "GDN_ERR_WORKSPACE", 7: "GDN_ERR_TIMEOUT"}
 EXPORTS = ("gdn_decode_step", "gdn_verify_with_checkpoints", "gdn_prefill_chunked",
            "gdn_prefill_workspace_size", "gdn_state_copy", "gdn_check_status", "gdn_last_error",
-           "gdn_prefill_chunked_static_scratch")
+           "gdn_prefill_chunked_static_scratch", "gdn_commit_accepted", "gdn_decode_step_mxfp8",
+           "gdn_prefill_chunked_ckpt")
 
 
 class GdnError(RuntimeError):
@@ -38,6 +39,11 @@ class Dims(ctypes.Structure):
 class Inputs(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("q", "k", "v", "z", "a", "b", "A_log", "dt_bias", "conv_w",
                                                "norm_w", "mask", "cu_seqlens", "state_idx")]
+
+
+class InputsMxfp8(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("q", "k", "v", "z", "q_scale", "k_scale", "v_scale", "z_scale", "a",
+                                               "b", "A_log", "dt_bias", "conv_w", "norm_w", "mask", "state_idx")]
 
 
 _lib = None
@@ -62,10 +68,15 @@ def load_library(path: Path | str | None = None):
     lib.gdn_prefill_workspace_size.argtypes = [DP, ctypes.c_int]
     lib.gdn_prefill_workspace_size.restype = ctypes.c_size_t
     lib.gdn_state_copy.argtypes = [DP, P, P, P, P, P, P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, P]
+    lib.gdn_prefill_chunked_ckpt.argtypes = [DP, IP, P, P, P, P, ctypes.c_size_t, P, ctypes.c_int32, P, P,
+                                             ctypes.c_int32, P]
+    lib.gdn_decode_step_mxfp8.argtypes = [DP, ctypes.POINTER(InputsMxfp8), P, P, P, P]
+    lib.gdn_commit_accepted.argtypes = [DP, ctypes.c_int32, ctypes.c_int32, P, P, P, P, P, P, P, P]
     lib.gdn_check_status.argtypes = [P]
     lib.gdn_last_error.restype = ctypes.c_char_p
     for name in ("gdn_decode_step", "gdn_verify_with_checkpoints", "gdn_prefill_chunked", "gdn_state_copy",
-                 "gdn_check_status", "gdn_prefill_chunked_static_scratch"):
+                 "gdn_check_status", "gdn_prefill_chunked_static_scratch", "gdn_commit_accepted",
+                 "gdn_decode_step_mxfp8", "gdn_prefill_chunked_ckpt"):
         getattr(lib, name).restype = ctypes.c_int
     if path is None:
         _lib = lib
@@ -113,6 +124,21 @@ def make_inputs(q, k, v, z, a, b, A_log, dt_bias, conv_w, norm_w, mask=None, cu_
     return inp
 
 
+def make_inputs_mxfp8(q, k, v, z, q_scale, k_scale, v_scale, z_scale, a, b, A_log, dt_bias, conv_w, norm_w,
+                      mask=None, state_idx=None) -> InputsMxfp8:
+    """The MXFP8 inputs struct (e4m3 q/k/v/z as uint8 tensors, their E8M0
+    block scales as uint8 tensors); keeps references to the tensors."""
+    t = (q, k, v, z, q_scale, k_scale, v_scale, z_scale, a, b, A_log, dt_bias, conv_w, norm_w, mask, state_idx)
+    inp = InputsMxfp8(*(_ptr(x) for x in t))
+    inp._tensors = t
+    return inp
+
+
+def decode_step_mxfp8(dims: Dims, inputs: InputsMxfp8, conv_state, recurrent_state, out, stream=None):
+    _check(load_library().gdn_decode_step_mxfp8(ctypes.byref(dims), ctypes.byref(inputs), _ptr(conv_state),
+                                                _ptr(recurrent_state), _ptr(out), _stream(stream)))
+
+
 def decode_step(dims: Dims, inputs: Inputs, conv_state, recurrent_state, out, stream=None):
     _check(load_library().gdn_decode_step(ctypes.byref(dims), ctypes.byref(inputs), _ptr(conv_state),
                                           _ptr(recurrent_state), _ptr(out), _stream(stream)))
@@ -139,6 +165,19 @@ def prefill_chunked(dims: Dims, inputs: Inputs, conv_state, recurrent_state, out
                                               int(workspace_bytes), _stream(stream)))
 
 
+def prefill_chunked_ckpt(dims: Dims, inputs: Inputs, conv_state, recurrent_state, out, workspace, ckpt, ckpt_state,
+                         ckpt_conv, workspace_bytes=None, stream=None):
+    """gdn_prefill_chunked_ckpt: ckpt is a device int32 [n, 3] tensor of (row,
+    position, slot); ckpt_state / ckpt_conv the checkpoint slots."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    n = 0 if ckpt is None else int(ckpt.shape[0])
+    _check(load_library().gdn_prefill_chunked_ckpt(
+        ctypes.byref(dims), ctypes.byref(inputs), _ptr(conv_state), _ptr(recurrent_state), _ptr(out),
+        _ptr(workspace), int(workspace_bytes), _ptr(ckpt), n, _ptr(ckpt_state), _ptr(ckpt_conv),
+        int(ckpt_state.shape[0]) if ckpt_state is not None else 0, _stream(stream)))
+
+
 def prefill_chunked_static_scratch(dims: Dims, inputs: Inputs, conv_state, recurrent_state, out, stream=None):
     """gdn_prefill_chunked with the library's own 64 MiB static scratch (for
     callers that cannot allocate device memory)."""
@@ -152,6 +191,14 @@ def state_copy(dims: Dims, src_state, src_conv, dst_state, dst_conv, src_slot, d
     _check(load_library().gdn_state_copy(ctypes.byref(dims), _ptr(src_state), _ptr(src_conv), _ptr(dst_state),
                                          _ptr(dst_conv), _ptr(src_slot), _ptr(dst_slot), int(n),
                                          int(n_src_slots), int(n_dst_slots), _stream(stream)))
+
+
+def commit_accepted(dims: Dims, n_layers, paths, ckpt_state, ckpt_conv, state_pool, conv_pool, accept_len, dst_slot,
+                    winner=None, stream=None):
+    """gdn_commit_accepted: every layer's winning checkpoint into its pool, one launch."""
+    _check(load_library().gdn_commit_accepted(ctypes.byref(dims), int(n_layers), int(paths), _ptr(ckpt_state),
+                                              _ptr(ckpt_conv), _ptr(state_pool), _ptr(conv_pool), _ptr(accept_len),
+                                              _ptr(dst_slot), _ptr(winner), _stream(stream)))
 
 
 def commit_source_slot(accept_len, T: int) -> tuple[int, int]:

@@ -180,3 +180,19 @@ def varlen_layer(layer: int, seed: int = 4, n_rows: int = 32, shape: Shape = QWE
         mask[0, cu[r]:cu[r] + real[r]] = 1.0
     d["mask"] = mask.to(device)
     return d
+
+
+def mxfp8(x: torch.Tensor, block: int = 32):
+    """MXFP8 encoding of x [..., n] (n a multiple of `block`): e4m3 elements and
+    one E8M0 scale byte per block of `block` consecutive values (OCP
+    microscaling): the block's scale is 2^(floor(log2 amax) - 8), 8 being the
+    largest e4m3 exponent, the elements are x / scale rounded to e4m3 and
+    clamped to its largest finite value (448). Returns (elements as uint8,
+    scales as uint8), both on x's device. An all-zero block gets scale 2^-127."""
+    *lead, n = x.shape
+    xb = x.float().reshape(*lead, n // block, block)
+    amax = xb.abs().amax(-1, keepdim=True)
+    e = torch.where(amax > 0, torch.floor(torch.log2(torch.where(amax > 0, amax, torch.ones_like(amax)))) - 8,
+                    torch.full_like(amax, -127.0)).clamp(-127, 127)
+    q = (xb / torch.exp2(e)).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
+    return q.view(torch.uint8).reshape(*lead, n), (e + 127).to(torch.uint8).reshape(*lead, n // block)

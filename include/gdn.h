@@ -39,6 +39,14 @@
  *     zeros, a slot index outside [0, n_slots)) are recorded in a device status
  *     word; the offending row is skipped (its state, conv tail and outputs are
  *     not written). gdn_check_status() reports and clears it.
+ *   - Every wait inside a kernel is bounded; one that runs out records
+ *     GDN_ERR_TIMEOUT (the GPU stalled far beyond any normal latency). In a
+ *     prefill call a (row, value head) whose chain stopped keeps its state, the
+ *     value channels of its conv tail and its outputs, while the row's other
+ *     heads complete; the q / k channels of the tail are written by the first
+ *     value head of each key head's group. In decode and verify a timeout may
+ *     leave the rows of the stalled CTA partly written: treat the call as
+ *     failed and restore those rows (for example from verify checkpoints).
  *   - Rows of one decode or prefill call must name distinct state slots (they
  *     are updated in place). Verify only reads the state, so its rows may share
  *     one slot.
@@ -116,6 +124,35 @@ typedef struct gdn_inputs {
 gdn_status gdn_decode_step(const gdn_dims *dims, const gdn_inputs *in, void *conv_state,
                            float *recurrent_state, void *out, void *stream);
 
+/* Token channels in MXFP8 (OCP microscaling FP8): q, k, v and z as e4m3
+ * elements (FP8 E4M3, one byte each) with one E8M0 scale byte s per block of
+ * 32 consecutive channels of a token; an element e stands for
+ * e * 2^(s - 127) (s = 255 is NaN). Shapes as in gdn_inputs:
+ *   q, k        e4m3 [B][T][nk*dk]   q_scale, k_scale  E8M0 [B][T][nk*dk/32]
+ *   v, z        e4m3 [B][T][nv*dv]   v_scale, z_scale  E8M0 [B][T][nv*dv/32]
+ * a, b, the weights, mask and state_idx are as in gdn_inputs (bf16 / fp32). */
+typedef struct gdn_inputs_mxfp8 {
+  const void *q, *k, *v, *z;
+  const void *q_scale, *k_scale, *v_scale, *z_scale;
+  const void *a, *b;
+  const float *A_log, *dt_bias;
+  const void *conv_w, *norm_w;
+  const float *mask;
+  const int32_t *state_idx;
+} gdn_inputs_mxfp8;
+
+/* gdn_decode_step with the token channels in MXFP8: uni_engine.py
+ * (Qwen3.5-9B-SpeedX9-GDN32) decodes with an FP8 model while the recurrent
+ * state stays exact ("state-safe": nothing that writes the fp32 state is
+ * quantized); here the layer's inputs arrive in FP8 and everything after their
+ * dequantization -- conv, norms, gates, the fp32 state update, the gated
+ * RMSNorm, the bf16 conv tail and outputs -- is the bf16 path's arithmetic,
+ * bit for bit: the call equals gdn_decode_step on the dequantized inputs
+ * (each dequantized element is exact in bf16 while it lies in bf16's normal
+ * range). The conv tail keeps the dequantized inputs in bf16. */
+gdn_status gdn_decode_step_mxfp8(const gdn_dims *dims, const gdn_inputs_mxfp8 *in, void *conv_state,
+                                 float *recurrent_state, void *out, void *stream);
+
 /* Speculative verify of T <= 8 draft tokens per row with per-token checkpoints.
  * generate.py (sparkle, mlx_streaming/mtp), tree_verify_step and the verify
  * forward with per-token gated-delta checkpoints: the state after every token
@@ -154,6 +191,30 @@ gdn_status gdn_verify_with_checkpoints(const gdn_dims *dims, const gdn_inputs *i
 gdn_status gdn_prefill_chunked(const gdn_dims *dims, const gdn_inputs *in, void *conv_state,
                                float *recurrent_state, void *out, void *workspace,
                                size_t workspace_bytes, void *stream);
+
+/* gdn_prefill_chunked that also keeps states from inside the call: the
+ * checkpoints of a prefix state cache. statecache.py (squad-0.8b, StateCache):
+ * a row's forward runs in chunks continued from a saved state, and the state at
+ * chosen positions of its prefix -- per GDN layer the fp32 recurrent state and
+ * the last K-1 conv inputs before the position -- is kept for later rows that
+ * share those tokens; the positions are chunk ends (multiples of 64, fla's
+ * delta-rule chunk) and the real end of the row.
+ * Everything gdn_prefill_chunked does, plus, for each i < n_ckpt:
+ *   ckpt       DEVICE int32 [n_ckpt][3]: (row, position, slot)
+ *   the recurrent state of `row` after its first `position` tokens of this call
+ *   -> ckpt_state[slot] (fp32 [n_ckpt_slots][nv][dk][dv]), and its conv tail
+ *   there (the last K-1 inputs before the position, old tail rows when
+ *   position < K-1) -> ckpt_conv[slot] (bf16 [n_ckpt_slots][conv_k-1][C]).
+ * A position must satisfy 0 < position <= Lr (the row's real length in this
+ * call) and be a multiple of 64 or Lr itself; a row may ask for at most 64.
+ * Any other triple (bad row, position or slot) is a device error
+ * (GDN_ERR_INDEX) and is skipped; the call itself completes. Slots must be
+ * distinct, and disjoint from the state and conv tail the call updates.
+ * n_ckpt == 0 is exactly gdn_prefill_chunked. */
+gdn_status gdn_prefill_chunked_ckpt(const gdn_dims *dims, const gdn_inputs *in, void *conv_state,
+                                    float *recurrent_state, void *out, void *workspace, size_t workspace_bytes,
+                                    const int32_t *ckpt, int32_t n_ckpt, float *ckpt_state, void *ckpt_conv,
+                                    int32_t n_ckpt_slots, void *stream);
 
 /* Workspace bytes gdn_prefill_chunked needs for these dimensions and layout
  * (0 on invalid dims).
@@ -208,6 +269,39 @@ gdn_status gdn_state_copy(const gdn_dims *dims, const float *src_state, const vo
                           float *dst_state, void *dst_conv, const int32_t *src_slot,
                           const int32_t *dst_slot, int32_t n, int32_t n_src_slots,
                           int32_t n_dst_slots, void *stream);
+
+/* Commit the accepted prefix of a speculative verify for every layer of a
+ * stack in one launch, with the winning path chosen on the device (no host
+ * round trip, so a verify + commit step can be one captured CUDA graph).
+ * generate.py (sparkle, mlx_streaming/mtp): after tree_verify_step the first
+ * candidate path with the longest accepted prefix wins and commit_tree_row
+ * makes its state after those tokens the sequence's state; uni_engine.py
+ * (Qwen3.5-9B-SpeedX9-GDN32), copy_cache_: the copy is in place, addresses
+ * preserved.
+ *   dims        B verify rows = n_groups * paths (each group: the candidate
+ *               paths of one sequence, consecutive rows), T draft tokens per
+ *               row (1 <= T <= 8), head sizes, conv_k, n_slots = pool slots
+ *               per layer
+ *   ckpt_state  fp32 [n_layers][B][T][nv][dk][dv]  the verify checkpoints of
+ *               each layer (gdn_verify_with_checkpoints), layers consecutive
+ *   ckpt_conv   bf16 [n_layers][B][T][conv_k-1][C], or NULL (states only)
+ *   state_pool  fp32 [n_layers][n_slots][nv][dk][dv]  in/out
+ *   conv_pool   bf16 [n_layers][n_slots][conv_k-1][C] in/out, NULL iff
+ *               ckpt_conv is NULL
+ *   accept_len  DEVICE int32 [B], each in [0, T]: accepted draft tokens of
+ *               each row
+ *   dst_slot    DEVICE int32 [B / paths]: the pool slot of each group
+ *   winner      DEVICE int32 [B / paths] or NULL: receives each group's winning
+ *               row (the lowest-index row with the longest accept length)
+ * Per group and layer: L = accept_len[winner]; L > 0 copies checkpoint
+ * (winner, L-1) of that layer into slot dst_slot[group] of that layer's pool;
+ * L = 0 copies nothing. An accept length outside [0, T] or a slot outside
+ * [0, n_slots) is a device error (GDN_ERR_INDEX): that group is not committed
+ * and its winner reads -1. (B / paths) * n_layers must be <= 65535. */
+gdn_status gdn_commit_accepted(const gdn_dims *dims, int32_t n_layers, int32_t paths, const float *ckpt_state,
+                               const void *ckpt_conv, float *state_pool, void *conv_pool,
+                               const int32_t *accept_len, const int32_t *dst_slot, int32_t *winner,
+                               void *stream);
 
 /* Synchronise `stream`, then return (and clear) a device-detected error
  * recorded on the current device since the last check (GDN_ERR_MASK,

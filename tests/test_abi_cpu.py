@@ -179,6 +179,33 @@ def test_state_copy_validation(lib):
     assert f(ctypes.byref(d), P, None, P, None, P, P, 0, 1, 1, None) == 0  # nothing to copy
 
 
+def test_commit_accepted_validation(lib):
+    f = lib.gdn_commit_accepted
+    d = _good_dims(B=8, T=4, n_slots=3)
+    ok = (P, P, P, P, P, P, None, None)  # ckpt_state, ckpt_conv, pools, accept_len, dst_slot, winner, stream
+    assert gdn.STATUS[f(ctypes.byref(d), 2, 3, *ok)] == "GDN_ERR_SHAPE"  # 8 rows are not groups of 3
+    assert gdn.STATUS[f(ctypes.byref(d), 0, 4, *ok)] == "GDN_ERR_SHAPE"  # no layers
+    assert gdn.STATUS[f(ctypes.byref(_good_dims(B=8, T=9)), 2, 4, *ok)] == "GDN_ERR_SHAPE"  # T > 8
+    assert gdn.STATUS[f(ctypes.byref(d), 2, 4, P, P, P, P, None, P, None, None)] == "GDN_ERR_ARG"  # accept_len
+    assert gdn.STATUS[f(ctypes.byref(d), 2, 4, P, None, P, P, P, P, None, None)] == "GDN_ERR_ARG"  # conv pair
+    assert gdn.STATUS[f(ctypes.byref(d), 2, 4, P, P, P, P, P, P, P + 2, None)] == "GDN_ERR_ARG"  # winner alignment
+    assert f(ctypes.byref(_good_dims(B=0, T=4)), 2, 4, *ok) == 0  # nothing to commit
+
+
+def test_decode_mxfp8_validation(lib):
+    f = lib.gdn_decode_step_mxfp8
+    names = [n for n, _ in gdn.InputsMxfp8._fields_]
+    good = {n: (1 << 20) + 256 * i for i, n in enumerate(names)}
+    good["mask"] = good["state_idx"] = None
+    d = _good_dims()
+    inp = gdn.InputsMxfp8(**dict(good, q_scale=None))
+    assert gdn.STATUS[f(ctypes.byref(d), ctypes.byref(inp), P, P, P, None)] == "GDN_ERR_ARG"
+    inp = gdn.InputsMxfp8(**good)
+    assert gdn.STATUS[f(ctypes.byref(_good_dims(T=2)), ctypes.byref(inp), P, P, P, None)] == "GDN_ERR_SHAPE"
+    assert gdn.STATUS[f(ctypes.byref(d), ctypes.byref(inp), P, P, None, None)] == "GDN_ERR_ARG"
+    assert f(ctypes.byref(_good_dims(B=0)), ctypes.byref(inp), P, P, P, None) == 0
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError):
         gdn.load_library(tmp_path / "missing" / "libgdn.so")

@@ -1,0 +1,82 @@
+"""GPU parity of gdn_decode_step_mxfp8 (the decode step with its token channels
+q / k / v / z in MXFP8: e4m3 elements, one power-of-two E8M0 scale per 32
+channels), through the C-ABI:
+
+  - bit for bit equal to gdn_decode_step on the dequantized inputs (outputs,
+    fp32 state and bf16 conv tail): everything after dequantization is the
+    bf16 path's arithmetic;
+  - against the oracle on the dequantized inputs within the spec bars;
+  - against the oracle on the original bf16 inputs (before quantization): the
+    error FP8 itself brings (e4m3 keeps 4 significant bits, so each input
+    moves by up to ~6%), recorded, with loose sanity bounds on the relative
+    Frobenius errors of the outputs and of the state after the token."""
+import numpy as np
+import pytest
+import torch
+
+from gated_deltanet_recurrence_delta_gb300 import gdn
+from gated_deltanet_recurrence_delta_gb300 import inputs as I
+from tests.gpu_cases import ACTS, WEIGHTS, assert_out, assert_state, dev, dims, inputs, oracle_layer, record, rel_fro
+
+pytestmark = pytest.mark.gpu
+
+MX = ("q", "k", "v", "z")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from gated_deltanet_recurrence_delta_gb300 import build
+    build.build()
+    gdn.load_library()
+
+
+def dequant(e, s, block=32):
+    """The value an MXFP8 element stands for: e4m3 times 2^(scale - 127)."""
+    f = e.view(torch.float8_e4m3fn).float()
+    sc = torch.exp2(s.float() - 127.0)
+    return (f.reshape(*f.shape[:-1], -1, block) * sc.unsqueeze(-1)).reshape(f.shape)
+
+
+@pytest.mark.parametrize("shape,B", [(I.QWEN35_9B, 16), (I.TINY, 3), (I.Shape(nk=1, nv=4, dk=64, dv=64), 2)])
+def test_mxfp8_decode(oracle_mod, shape, B):
+    d = I.decode_batch(seed=140 + B, B=B, shape=shape)
+    enc = {n: I.mxfp8(d[n]) for n in MX}
+    deq = {n: dequant(*enc[n]).to(torch.bfloat16) for n in MX}
+    for n in MX:  # every dequantized element is exact in bf16
+        assert torch.equal(deq[n].float(), dequant(*enc[n]))
+    acts_deq = {**{n: d[n] for n in ACTS}, **deq}
+    w = {n: dev(d[n]) for n in WEIGHTS}
+    dm = dims(shape, B, 1, B)
+
+    # the MXFP8 call
+    conv8, S8 = dev(d["conv_state"]).clone(), dev(d["state"]).clone()
+    out8 = torch.empty((B, 1, shape.nv, shape.dv), dtype=torch.bfloat16, device="cuda")
+    mx = {n: (dev(enc[n][0]), dev(enc[n][1])) for n in MX}
+    inp8 = gdn.make_inputs_mxfp8(mx["q"][0], mx["k"][0], mx["v"][0], mx["z"][0], mx["q"][1], mx["k"][1],
+                                 mx["v"][1], mx["z"][1], dev(d["a"]), dev(d["b"]), w["A_log"], w["dt_bias"],
+                                 w["conv_w"], w["norm_w"])
+    gdn.decode_step_mxfp8(dm, inp8, conv8, S8, out8)
+    # the bf16 call on the dequantized inputs
+    convb, Sb = dev(d["conv_state"]).clone(), dev(d["state"]).clone()
+    outb = torch.empty_like(out8)
+    gdn.decode_step(dm, inputs(w, {n: dev(a) for n, a in acts_deq.items()}), convb, Sb, outb)
+    gdn.check_status()
+    assert torch.equal(out8, outb) and torch.equal(S8, Sb) and torch.equal(conv8, convb)
+
+    # the oracle on the dequantized inputs: the spec bars
+    ref = oracle_layer(oracle_mod, shape, d, acts_deq, d["conv_state"], d["state"])
+    assert_out(out8, ref["out"])
+    assert_state(S8, ref["state"])
+    assert torch.equal(conv8.cpu().double(), torch.from_numpy(ref["conv_state"]))
+
+    # the oracle on the original bf16 inputs: what FP8 itself costs
+    ref0 = oracle_layer(oracle_mod, shape, d, d, d["conv_state"], d["state"])
+    e_out = rel_fro(out8, ref0["out"])
+    e_state = rel_fro(S8, ref0["state"])
+    record("fp8_vs_bf16_inputs_out_rel_fro", e_out)
+    record("fp8_vs_bf16_inputs_state_rel_fro", e_state)
+    assert e_out <= 0.15, f"outputs {e_out:.3e} off the bf16-input result (relative Frobenius)"
+    assert e_state <= 0.1, f"state {e_state:.3e} off the bf16-input result (relative Frobenius)"
+    assert np.isfinite(e_out) and np.isfinite(e_state)
