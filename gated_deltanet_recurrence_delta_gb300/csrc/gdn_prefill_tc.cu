@@ -63,7 +63,11 @@ struct Ws {
   __half *kimg, *qimg;  // [S][nk][2 hi|lo][2][64][64]  K, Q as swizzled [token][dk] images (2 x 16 KiB)
   __half *vimg;         // [S][nv][2 hi|lo][2][64][64]  V as a swizzled [token][dv] image
   __half *wq;           // [S][nv][2][128][64]  W (rows 0-63) | Q' (rows 64-127) image (32 KiB)
-  float *sec;           // [S][nv][68]          exp(G_C - G_j) per token j < 64, then gamma_C (and 3 pad)
+  float *gate;          // [S][nv][324]         per token j < 64: g, beta, G (inclusive prefix of g), exp(G),
+                        //                      exp(G_C - G); then gamma_C (and 3 pad). Written by the front
+                        //                      kernel when the chunk and state passes are separate kernels
+                        //                      (else the chunk unit forms the gates and writes the last 68,
+                        //                      which the state pass reads)
   float *ut, *ot;       // [S][nv][64][128]     U and O_local, token-major fp32, 16-byte chunk c of
                         //                      row i stored at c ^ (i % 8) (32 KiB each)
   __half *simg;         // [S][nv][2][128][64]  fp16 image of the state at the chunk's start (32 KiB)
@@ -76,7 +80,10 @@ struct Ws {
 constexpr size_t kImg = 64 * 128;    // halves in a 64x128 image
 constexpr size_t kWQ = 128 * 128;    // halves in the W|Q' image
 constexpr size_t kRowF = 128 * 64;   // floats in U / O_local
-constexpr int kSecRec = 68;          // floats in one exp(G_C - G) | gamma_C record (a multiple of 16 bytes)
+constexpr int kGateRec = 324;        // floats in one gate record (a multiple of 16 bytes)
+constexpr int kGateLd = 320;         // floats of it a chunk unit loads (g, beta, G, exp(G), exp(G_C - G))
+constexpr int kSecOff = 256;         // exp(G_C - G) | gamma_C: the state pass's 68 floats
+constexpr int kSecRec = 68;
 
 size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -87,7 +94,7 @@ size_t slots_total(int B, int T, bool packed) {
 size_t ws_bytes(int B, int T, int nk, int nv, bool packed) {
   const size_t S = slots_total(B, T, packed);
   return 2 * a256(S * nk * kImg * 4) + a256(S * nv * kImg * 4) + a256(S * nv * kWQ * 2) +
-         a256(S * nv * kSecRec * 4) + 2 * a256(S * nv * kRowF * 4) +
+         a256(S * nv * kGateRec * 4) + 2 * a256(S * nv * kRowF * 4) +
          a256(S * nv * kWQ * 2) + a256((size_t)B * nv * 4) + a256(S * nv * 4) + a256(S * 8);
 }
 
@@ -103,8 +110,8 @@ Ws carve(void *ws, int B, int T, int nk, int nv, bool packed) {
   p += a256(S * nv * kImg * 4);
   w.wq = reinterpret_cast<__half *>(p);
   p += a256(S * nv * kWQ * 2);
-  w.sec = reinterpret_cast<float *>(p);
-  p += a256(S * nv * kSecRec * 4);
+  w.gate = reinterpret_cast<float *>(p);
+  p += a256(S * nv * kGateRec * 4);
   w.ut = reinterpret_cast<float *>(p);
   p += a256(S * nv * kRowF * 4);
   w.ot = reinterpret_cast<float *>(p);
@@ -253,6 +260,10 @@ __device__ __forceinline__ void umma_tile_split_bmn(uint32_t tmem_d, uint32_t a_
 // so its L2 norm is a 16-lane butterfly, and each thread's 16-byte chunks of
 // the [token][d] image are stored straight from registers (a warp writes
 // whole lines).
+// GATES: the value-head CTAs also form the chunk's gates (for calls whose chunk
+// pass runs as its own kernel, where the units are the critical path; a
+// compile-time choice, so the other instantiation carries none of that code).
+template <bool GATES>
 __global__ void __launch_bounds__(256, 4) front_kernel(LayerArgs A, Rows R, int Ttot, Ws W) {
   griddep_wait();  // the kernel before this call (a previous layer call) is complete
   griddep_trigger();
@@ -267,6 +278,26 @@ __global__ void __launch_bounds__(256, 4) front_kernel(LayerArgs A, Rows R, int 
   const int which = gi < A.nk ? 0 : (gi < 2 * A.nk ? 1 : 2);
   const int head = which == 0 ? gi : (which == 1 ? gi - A.nk : gi - 2 * A.nk);
   const int slot = row_slot(A, r);
+  // value heads: warp 0 also forms the chunk's gates (gdn_gates: g = -exp(A_log)
+  // softplus(a + dt_bias), beta = sigmoid(b); g = beta = 0 on padding and past
+  // the row end), two tokens per lane. Their inputs are loaded now and used
+  // after the images are stored: these CTAs skip the L2 norm, so they have the
+  // time the q / k CTAs spend on it.
+  const bool gate_warp = GATES && which == 2 && tid < 32;
+  float ga[2] = {0.f, 0.f}, gb[2] = {0.f, 0.f};
+  bool greal[2] = {false, false};
+  if (gate_warp) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int i = 2 * tid + e;
+      if (c * CH + i < len) {
+        const size_t p = (size_t)start + c * CH + i;
+        greal[e] = !A.mask || A.mask[p] == 1.0f;
+        ga[e] = ldbf(A.a + p * A.nv + head);
+        gb[e] = ldbf(A.b + p * A.nv + head);
+      }
+    }
+  }
   const int cb = tid & 15, tb = tid >> 4, pos0 = c * CH + 4 * tb;
   const int ch0 = which == 0 ? head * HD : (which == 1 ? kd + head * HD : 2 * kd + head * HD);
   const bf16 *src = which == 0 ? A.q + head * HD : (which == 1 ? A.k + head * HD : A.v + head * HD);
@@ -330,6 +361,35 @@ __global__ void __launch_bounds__(256, 4) front_kernel(LayerArgs A, Rows R, int 
     *reinterpret_cast<uint4 *>(img + off) = hi;
     *reinterpret_cast<uint4 *>(img + kImg * 2 + off) = lo;
   }
+  if (gate_warp) {
+    // the gates, then G = the inclusive prefix of g, exp(G), exp(G_C - G) and
+    // gamma_C = exp(G_C): the same arithmetic as the chunk unit's
+    const int lane = tid;
+    float g[2], be[2];
+    const float eA = -expf(A.A_log[head]), dtb = A.dt_bias[head];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      g[e] = greal[e] ? __fmul_rn(eA, softplus_f(__fadd_rn(ga[e], dtb))) : 0.f;
+      be[e] = greal[e] ? sigmoid_f(gb[e]) : 0.f;
+    }
+    const float v0 = g[0], v1 = v0 + g[1];
+    float run = v1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float t = __shfl_up_sync(0xffffffffu, run, o);
+      if (lane >= o) run += t;
+    }
+    const float G0 = run - v1 + v0, G1 = run;
+    const float GC = __shfl_sync(0xffffffffu, run, 31);
+    float *rec = W.gate + ((size_t)s * A.nv + head) * kGateRec;
+    reinterpret_cast<float2 *>(rec)[lane] = make_float2(g[0], g[1]);
+    reinterpret_cast<float2 *>(rec + 64)[lane] = make_float2(be[0], be[1]);
+    reinterpret_cast<float2 *>(rec + 128)[lane] = make_float2(G0, G1);
+    const float gam1 = __expf(G1);
+    reinterpret_cast<float2 *>(rec + 192)[lane] = make_float2(__expf(G0), gam1);
+    reinterpret_cast<float2 *>(rec + 256)[lane] = make_float2(__expf(GC - G0), __expf(GC - G1));
+    if (lane == 31) rec[320] = gam1;  // gamma_C
+  }
 }
 
 // ------------------------------------------------------------ chunk-local
@@ -349,9 +409,10 @@ constexpr int kOffTRL = 147456;  // [T; R] image (lo)
 constexpr int kOffPTH = 163840;  // [128 rows][128 B]: P rows 0-63 | T^T rows 64-127 (hi)
 constexpr int kOffPTL = 180224;  // the same, lo parts
 constexpr int kOffSCR = 196608;  // fp32 [1024] solve scratch
-constexpr int kOffSm = 200704;   // g, beta, G, exp(G), exp(G_C - G): fp32 [5][64]; barriers; tmem base
-constexpr int kOffBar = kOffSm + 5 * 64 * 4;  // [0..2] chunk-local loads and products, [3..5] the chain's, TMEM base
-constexpr int kChunkSmem = kOffSm + 2048 + 1024;  // + alignment slack
+constexpr int kOffSm = 200704;   // 2 x the unit's gates g, beta, G, exp(G), exp(G_C - G): fp32 [5][64]
+                                 // (unit parity p uses buffer p); barriers; tmem base
+constexpr int kOffBar = kOffSm + 2 * kGateLd * 4;  // [0..2] chunk-local loads and products, [3..5] the chain's, TMEM base
+constexpr int kChunkSmem = kOffBar + 64 + 1024;     // + alignment slack
 
 __device__ __forceinline__ void store_split8(unsigned char *hi_img, unsigned char *lo_img, uint32_t off,
                                              const float *x) {
@@ -377,16 +438,20 @@ struct UnitPhase {
 // unit's K|Q tiles were requested that way by the unit before. The caller has
 // initialised the barriers at kOffBar, holds 256 TMEM columns at `tmem`
 // and has synchronised the CTA since any earlier use of shared memory or TMEM.
+// gates_ready: the front kernel formed the gates; they arrive with the K|Q
+// tiles (else the unit forms them and stores exp(G_C - G), gamma_C for the
+// state pass).
 // publish: once the unit's outputs are complete in global memory, set its
 // flag (release, GPU scope) for a chain pass of the same grid. Without
 // publish the unit returns with its output stores possibly still reading
 // shared memory; the next unit waits for them before it reuses those regions,
 // and the caller before the CTA exits. Returns false when a bounded wait ran
 // out (the status word is set).
-template <class FindNext>
+template <bool GATES_READY, class FindNext>
 __device__ __forceinline__ bool chunk_unit(unsigned char *sm, const LayerArgs &A, const Rows &R, const Ws &W, int s,
                                            int h, int r, int c, int parity, bool kq_issued, FindNext find_next,
                                            uint32_t tmem, UnitPhase &ph, bool publish) {
+  constexpr bool gates_ready = GATES_READY;
   const int xo = parity ? kOffAF : kOffKQH, yo = parity ? kOffKQH : kOffAF;  // K|Q region, A/T/P region
   unsigned char *KQH = sm + xo, *KQL = sm + xo + (kOffKQL - kOffKQH);
   unsigned char *B2H = sm + kOffB2H;
@@ -394,7 +459,7 @@ __device__ __forceinline__ bool chunk_unit(unsigned char *sm, const LayerArgs &A
   unsigned char *TRH = sm + yo, *TRL = sm + yo + (kOffTRL - kOffAF);
   unsigned char *PTH = sm + yo + (kOffPTH - kOffAF), *PTL = sm + yo + (kOffPTL - kOffAF);
   float *SCR = reinterpret_cast<float *>(sm + kOffSCR);
-  float *sg = reinterpret_cast<float *>(sm + kOffSm);  // g
+  float *sg = reinterpret_cast<float *>(sm + kOffSm) + parity * kGateLd;  // g
   float *sb = sg + 64;                                   // beta
   float *sG = sb + 64;                                   // inclusive prefix of g
   float *sgam = sG + 64;                                 // exp(G_j)
@@ -408,9 +473,13 @@ __device__ __forceinline__ bool chunk_unit(unsigned char *sm, const LayerArgs &A
   const int nvalid = min(CH, len - c * CH);
 
   // thread 0: the K|Q tiles of (slot s2, key head kh2) into the region at
-  // dstH (hi) / dstH + 32 KiB (lo)
-  auto issue_kq = [&](int s2, int kh2, unsigned char *dstH) {
-    mbar_arrive_expect_tx(&bar_ld[0], 65536);
+  // dstH (hi) / dstH + 32 KiB (lo), and with gates_ready the gates of (slot
+  // s2, value head h2) into the gate buffer of parity par2
+  auto issue_kq = [&](int s2, int kh2, unsigned char *dstH, int h2, int par2) {
+    mbar_arrive_expect_tx(&bar_ld[0], 65536 + (gates_ready ? kGateLd * 4 : 0));
+    if (gates_ready)
+      bulk_g2s(reinterpret_cast<float *>(sm + kOffSm) + par2 * kGateLd, W.gate + ((size_t)s2 * A.nv + h2) * kGateRec,
+               kGateLd * 4, &bar_ld[0]);
     for (int part = 0; part < 2; ++part) {
       const __half *ki = W.kimg + ((size_t)s2 * A.nk + kh2) * 2 * kImg + part * kImg;
       const __half *qi = W.qimg + ((size_t)s2 * A.nk + kh2) * 2 * kImg + part * kImg;
@@ -430,11 +499,11 @@ __device__ __forceinline__ bool chunk_unit(unsigned char *sm, const LayerArgs &A
   // the V region and from the region this unit's A / P tiles go to: V is
   // requested, and those tiles written, once its stores have read them.
   if (tid == 0) {  // the K|Q tiles first (the first product needs them), then V
-    if (!kq_issued) issue_kq(s, kh, KQH);
+    if (!kq_issued) issue_kq(s, kh, KQH, h, parity);
     if (publish) issue_v();
   }
   // gates of the chunk's tokens; padding and tokens past the row end get g = beta = 0
-  if (tid < CH) {
+  if (!gates_ready && tid < CH) {
     float g = 0.f, beta = 0.f;
     if (tid < nvalid) {
       const size_t p = (size_t)start + c * CH + tid;
@@ -448,7 +517,7 @@ __device__ __forceinline__ bool chunk_unit(unsigned char *sm, const LayerArgs &A
     sb[tid] = beta;
   }
   __syncthreads();
-  if (warp == 0) {  // inclusive prefix over 64 values, two per lane
+  if (!gates_ready && warp == 0) {  // inclusive prefix over 64 values, two per lane
     const float v0 = sg[2 * lane], v1 = v0 + sg[2 * lane + 1];
     float run = v1;
 #pragma unroll
@@ -479,8 +548,8 @@ __device__ __forceinline__ bool chunk_unit(unsigned char *sm, const LayerArgs &A
     umma_commit(bar_mma);
     nx = find_next();
   }
-  if (tid < CH) {  // per-token factors for the state pass: exp(G_C - G_j)
-    float *rec = W.sec + ((size_t)s * A.nv + h) * kSecRec;
+  if (!gates_ready && tid < CH) {  // per-token factors for the state pass: exp(G_C - G_j)
+    float *rec = W.gate + ((size_t)s * A.nv + h) * kGateRec + kSecOff;
     rec[tid] = sec[tid];
     if (tid == 0) rec[CH] = sgam[CH - 1];  // gamma_C
   }
@@ -671,7 +740,7 @@ __device__ __forceinline__ bool chunk_unit(unsigned char *sm, const LayerArgs &A
   ph.mma ^= 1;
   tc_fence_after();
   // the A / T / [T; R] / P tiles are consumed: that region takes the next unit's K|Q
-  if (tid == 0 && nx.x >= 0) issue_kq(nx.x, nx.y / A.G, sm + yo);
+  if (tid == 0 && nx.x >= 0) issue_kq(nx.x, nx.y / A.G, sm + yo, nx.y, parity ^ 1);
   {
     // W / Q' into the K|Q image (plain fp16); U / O_local rows, fp32, staged in
     // the free B2 tiles in the row-swizzled layout of the workspace (16-byte
@@ -784,7 +853,7 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
       return make_int2(n.x < 0 ? -1 : n.x / A.nv, n.x < 0 ? 0 : n.x % A.nv);
     };
     const bool ok =
-        chunk_unit(sm, A, R, W, cur.x / A.nv, cur.x % A.nv, cur.y, cur.z, parity, kq, find_next, tmem, ph, false);
+        chunk_unit<true>(sm, A, R, W, cur.x / A.nv, cur.x % A.nv, cur.y, cur.z, parity, kq, find_next, tmem, ph, false);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -956,7 +1025,7 @@ __device__ __forceinline__ bool state_chain(unsigned char *sm, uint64_t *bar_ld,
     bulk_g2s(wdst + 8192, wq + 16384, 8192, &bar_ld[buf]);
     bulk_g2s(sm + kSOffKT + buf * 16384, W.kimg + ((size_t)s * A.nk + kh) * 2 * kImg, 16384, &bar_ld[buf]);
     bulk_g2s(sm + kSOffUT + buf * 32768, W.ut + sh * kRowF, 32768, &bar_ld[buf]);
-    bulk_g2s(sm + kSOffSec + buf * kSecRec * 4, W.sec + sh * kSecRec, kSecRec * 4, &bar_ld[buf]);
+    bulk_g2s(sm + kSOffSec + buf * kSecRec * 4, W.gate + sh * kGateRec + kSecOff, kSecRec * 4, &bar_ld[buf]);
   };
   // thread 0: the last chunk whose loads are issued, and the last chunk up to
   // which every unit is known published and acquired; gave_up: a unit's flag
@@ -1202,8 +1271,8 @@ __global__ void __launch_bounds__(256, 1) chunk_state_kernel(LayerArgs A, Rows R
       const int v = u + (int)gridDim.x, c2 = v / BH, rh2 = v % BH;
       return v < n_units ? make_int2((rh2 / A.nv) * R.cpr + c2, rh2 % A.nv) : make_int2(-1, 0);
     };
-    ok = chunk_unit(sm, A, R, W, r * R.cpr + c, rh % A.nv, r, c, parity, u != (int)blockIdx.x, find_next, tmem, ph,
-                    true);
+    ok = chunk_unit<false>(sm, A, R, W, r * R.cpr + c, rh % A.nv, r, c, parity, u != (int)blockIdx.x, find_next, tmem,
+                           ph, true);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1432,18 +1501,21 @@ gdn_status launch_prefill_tc(const LayerArgs &A, void *ws, cudaStream_t stream) 
       return fail(GDN_ERR_CUDA, "prefill: cannot reserve shared memory");
     attr_set[dev.id].store(true, std::memory_order_release);
   }
-  if (launch_pdl(tc::front_kernel, dim3(S, 2 * A.nk + A.nv), dim3(256), 0, stream, A, R, Ttot, W) != cudaSuccess)
+  // Few chains (dense rows, at most half a grid of one CTA per SM): chunk units
+  // and chains in one grid, so that the chains start while late chunks are
+  // still being prepared; the chains are that grid's critical path and the
+  // units form their own gates. Otherwise two kernels, and the front kernel
+  // forms the gates (the chunk pass is the critical path there).
+  const int n_units = S * A.nv, grid = n_units < dev.sms ? n_units : dev.sms;
+  const bool merged = !packed && 2 * A.B * A.nv <= grid;
+  if (launch_pdl(merged ? tc::front_kernel<false> : tc::front_kernel<true>, dim3(S, 2 * A.nk + A.nv), dim3(256), 0,
+                 stream, A, R, Ttot, W) != cudaSuccess)
     return check_launch("prefill front");
   // every kernel starts early (programmatic dependent launch) and waits for
   // its predecessor inside the kernel
   CUtensorMap omap, zmap;
   if (gdn_status st = tc::encode_rows_map(&omap, A.out, Ttot, A.nv * tc::HD, tc::CH / 2)) return st;
   if (gdn_status st = tc::encode_rows_map(&zmap, A.z, Ttot, A.nv * tc::HD, tc::CH)) return st;
-  // Few chains (dense rows, at most half a grid of one CTA per SM): chunk units
-  // and chains in one grid, so that the chains start while late chunks are
-  // still being prepared. Otherwise two kernels.
-  const int n_units = S * A.nv, grid = n_units < dev.sms ? n_units : dev.sms;
-  const bool merged = !packed && 2 * A.B * A.nv <= grid;
   if (merged) {
     if (launch_pdl(tc::chunk_state_kernel, dim3(grid), dim3(256), tc::kChunkSmem, stream, A, R, Ttot, W) !=
         cudaSuccess)
