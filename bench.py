@@ -66,8 +66,11 @@ KERNEL_SOURCES = {
     "decode_kernel": ("gdn_decode.cu", "gdn_token.cuh") + _COMMON_SOURCES,
     "verify_split_kernel": ("gdn_verify.cu", "gdn_token.cuh") + _COMMON_SOURCES,
     "state_copy_kernel": ("gdn_state_copy.cu",) + _COMMON_SOURCES,
+    "decode_kernel_mxfp8": ("gdn_decode.cu", "gdn_token.cuh") + _COMMON_SOURCES,
+    "commit_kernel": ("gdn_state_copy.cu",) + _COMMON_SOURCES,
     **{k: _PREFILL_SOURCES for k in ("front_kernel", "chunk_state_kernel", "output_kernel", "chunk_kernel",
-                                     "state_kernel", "prefill_call_512")},
+                                     "state_kernel", "front_kernel_gates", "output_kernel_varlen", "prefill_call_512",
+                                     "varlen_layer")},
 }
 
 
@@ -87,17 +90,22 @@ def csrc_hash(kernel: str | None = None) -> str:
     return h.hexdigest()[:16]
 
 
-def dram_traffic(kernel: str):
-    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, or None
+def dram_traffic(kernel: str, field: str = "bytes_per_launch"):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary (or, with
+    field="l2_write_bytes_per_launch", the bytes its SMs wrote into L2), or None
     when absent or taken on other kernel sources."""
     p = ROOT / "profiles" / "dram_traffic.json"
     if not p.exists():
         return None
     d = json.loads(p.read_text())
     e = d.get(kernel)
-    if not e or e.get("csrc_hash") != csrc_hash(kernel):
+    if not e or e.get("csrc_hash") != csrc_hash(kernel) or field not in e:
         return None
-    return float(e["bytes_per_launch"])
+    return float(e[field])
+
+
+def scaled(x, k):
+    return None if x is None else x * k
 
 
 class ClockSampler:
@@ -264,6 +272,7 @@ def phase_decode(gdn, world, steps, warmup, peak_hbm, local=0, e2e=True):
            "roofline": {"bound": "hbm", "achieved": nbytes / (kms * 1e-3) / 1e9, "peak": peak_hbm,
                         "unit": "GB/s", "frac": nbytes / (kms * 1e-3) / 1e9 / peak_hbm,
                         "traffic": dram_traffic("decode_kernel"), "traffic_note": TRAFFIC_NOTE,
+                        "l2_write_bytes": dram_traffic("decode_kernel", "l2_write_bytes_per_launch"),
                         "algorithmic_bytes": nbytes},
            "l2": f"inputs larger than L2: {n_sets} rotating layer buffer sets of {per_set / 2**20:.0f} MiB state",
            "clocks": clk.summary()}
@@ -345,7 +354,8 @@ def phase_decode_mxfp8(gdn, world, steps, warmup, peak_hbm):
     res = {"tokens_per_s": B * world / (ms * 1e-3), "ms_per_step": ms, "tokens_per_step": B, "launches_per_step": 1,
            "roofline": {"bound": "hbm", "kernel": "decode_kernel (MXFP8 inputs)",
                         "achieved": nbytes / (ms * 1e-3) / 1e9, "peak": peak_hbm, "unit": "GB/s",
-                        "frac": nbytes / (ms * 1e-3) / 1e9 / peak_hbm, "algorithmic_bytes": nbytes},
+                        "frac": nbytes / (ms * 1e-3) / 1e9 / peak_hbm, "algorithmic_bytes": nbytes,
+                        "traffic": dram_traffic("decode_kernel_mxfp8"), "traffic_note": TRAFFIC_NOTE},
            "l2": f"inputs larger than L2: {n_sets} rotating layer buffer sets of {per_set / 2**20:.0f} MiB state"}
     del sets
     torch.cuda.empty_cache()
@@ -396,7 +406,8 @@ def phase_verify(gdn, world, steps, warmup, peak_hbm):
            "step_hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peak_hbm,
            "roofline": {"bound": "hbm", "kernel": "verify_split_kernel", "achieved": vbytes / (kms * 1e-3) / 1e9,
                         "peak": peak_hbm, "unit": "GB/s", "frac": vbytes / (kms * 1e-3) / 1e9 / peak_hbm,
-                        "traffic": dram_traffic("verify_split_kernel"), "traffic_note": TRAFFIC_NOTE}}
+                        "traffic": dram_traffic("verify_split_kernel"), "traffic_note": TRAFFIC_NOTE,
+                        "l2_write_bytes": dram_traffic("verify_split_kernel", "l2_write_bytes_per_launch")}}
     del sets
     torch.cuda.empty_cache()
     return res
@@ -475,7 +486,8 @@ def phase_prefill(gdn, world, steps, warmup, peak_tf):
            "ms_per_512_call": ms / (T // call), "launches_per_step": 3 * (T // call),
            "roofline": {"bound": "tensor", "kernel": "front+chunk_state+output", "achieved": flops / (kms * 1e-3) / 1e12, "peak": peak_tf,
                         "unit": "TFLOP/s", "frac": flops / (kms * 1e-3) / 1e12 / peak_tf,
-                        "traffic": dram_traffic("prefill_call_512"), "traffic_scope": "one 512-token call (three kernels)",
+                        "traffic": scaled(dram_traffic("prefill_call_512"), T // call),
+                        "traffic_scope": "16 512-token calls (three kernels each)",
                         "traffic_note": TRAFFIC_NOTE,
                         "algorithmic_flops_per_token": prefill_flops_per_token(s)}}
     del d, calls, ws
@@ -509,7 +521,9 @@ def phase_varlen(gdn, world, steps, warmup, peak_tf, n_layers=24):
            "layer_tokens_per_s": real * n_layers * world / (ms * 1e-3), "ms_per_step": ms,
            "real_tokens": real, "padded_tokens": padded, "layers": n_layers, "launches_per_step": 4 * n_layers,
            "roofline": {"bound": "tensor", "kernel": "front+chunk+state+output", "achieved": flops / (kms * 1e-3) / 1e12, "peak": peak_tf,
-                        "unit": "TFLOP/s", "frac": flops / (kms * 1e-3) / 1e12 / peak_tf, "traffic": None}}
+                        "unit": "TFLOP/s", "frac": flops / (kms * 1e-3) / 1e12 / peak_tf,
+                        "traffic": scaled(dram_traffic("varlen_layer"), n_layers),
+                        "traffic_scope": f"{n_layers} layers (four kernels each)", "traffic_note": TRAFFIC_NOTE}}
     del layers, ws
     torch.cuda.empty_cache()
     return res
@@ -639,6 +653,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
     ap.add_argument("--phases", default="decode,verify,decode_mxfp8,stack,prefill,varlen")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--stack-layers", type=int, default=24, help="layers of the captured stack phase")
     ap.add_argument("--oracle-varlen-layers", type=int, default=3,
                     help="varlen layers the oracle baseline runs in full (24 = the whole stack)")
     args = ap.parse_args()
@@ -687,7 +702,7 @@ def main():
     if "decode_mxfp8" in phases:
         results["decode_mxfp8"] = phase_decode_mxfp8(gdn, world, steps, warmup, peak_hbm)
     if "stack" in phases:
-        results["stack"] = phase_stack(gdn, world, max(3, steps // 40), warmup, peak_hbm)
+        results["stack"] = phase_stack(gdn, world, max(3, steps // 40), warmup, peak_hbm, n_layers=args.stack_layers)
     if "prefill" in phases:
         results["prefill"] = phase_prefill(gdn, world, max(3, steps // 400), warmup, peak_tf)
     if "varlen" in phases:
