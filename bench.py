@@ -10,7 +10,7 @@ per-token checkpoints, commit of the winner), chunked prefill (one row of
 (32 rows U{16..2048} padded to chunk buckets, 24 independent layers).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--phases decode,verify,decode_mxfp8,stack,prefill,varlen]
+                  [--phases decode,verify,decode_mxfp8,stack,proj,prefill,varlen]
 
 --impl reference times the fp64 CPU oracle (the reference implementation of
 this path) on the same decode workload, on the host's cores.
@@ -454,6 +454,56 @@ def phase_stack(gdn, world, steps, warmup, peak_hbm, n_layers=24):
     return res
 
 
+def phase_proj(gdn, world, steps, warmup, peak_hbm, peak_tf):
+    """The layer's projections (tcgen05 GEMMs) at the Qwen3.5-9B-like layer's
+    sizes (hidden 4096): the in-projection, split into the layer's six input
+    tensors in its epilogue (12352 output features), and the out-projection
+    (4096 x 4096). Decode-sized calls (64 tokens) stream their weights: HBM
+    roofline over rotating weight sets larger than L2. Prefill-sized calls
+    (8192 tokens): tensor roofline."""
+    s, H = I.QWEN35_9B, 4096
+    N = 2 * s.kd + 2 * s.vd + 2 * s.nv
+    g = torch.Generator(device="cuda").manual_seed(12)
+    res = {}
+    for M in (64, 8192):
+        n_sets = max(2, math.ceil(3 * L2_BYTES / (N * H * 2))) if M == 64 else 1
+        w_in = [(torch.randn((N, H), generator=g, device="cuda") * H ** -0.5).to(torch.bfloat16) for _ in range(n_sets)]
+        w_out = [(torch.randn((H, s.vd), generator=g, device="cuda") * s.vd ** -0.5).to(torch.bfloat16)
+                 for _ in range(max(1, math.ceil(3 * L2_BYTES / (H * s.vd * 2))) if M == 64 else 1)]
+        hidden = torch.randn((M, H), generator=g, device="cuda").to(torch.bfloat16)
+        o = torch.randn((M, s.vd), generator=g, device="cuda").to(torch.bfloat16)
+        outs = {n: torch.empty((M, w), dtype=torch.bfloat16, device="cuda")
+                for n, w in (("q", s.kd), ("k", s.kd), ("v", s.vd), ("z", s.vd), ("a", s.nv), ("b", s.nv))}
+        y = torch.empty((M, H), dtype=torch.bfloat16, device="cuda")
+        dm = _dims(gdn, s, 1, 1, 1)
+
+        def step_in(i, _):
+            gdn.in_proj(dm, hidden, w_in[i % len(w_in)], outs["q"], outs["k"], outs["v"], outs["z"], outs["a"],
+                        outs["b"])
+
+        def step_out(i, _):
+            gdn.out_proj(o, w_out[i % len(w_out)], y)
+
+        k = steps if M == 64 else max(3, steps // 20)
+        ms_in = timed(world, k, warmup, step_in)
+        ms_out = timed(world, k, warmup, step_out)
+        for name, ms, nout, kk in (("in_proj", ms_in, N, H), ("out_proj", ms_out, H, s.vd)):
+            nbytes = (nout * kk + M * kk + M * nout) * 2
+            flops = 2.0 * M * nout * kk
+            key = f"{name}_{'decode' if M == 64 else 'prefill'}"
+            if M == 64:
+                roof = {"bound": "hbm", "achieved": nbytes / (ms * 1e-3) / 1e9, "peak": peak_hbm, "unit": "GB/s",
+                        "frac": nbytes / (ms * 1e-3) / 1e9 / peak_hbm, "algorithmic_bytes": nbytes}
+            else:
+                roof = {"bound": "tensor", "achieved": flops / (ms * 1e-3) / 1e12, "peak": peak_tf, "unit": "TFLOP/s",
+                        "frac": flops / (ms * 1e-3) / 1e12 / peak_tf, "algorithmic_flops": flops}
+            res[key] = {"tokens": M, "features": nout, "k": kk, "ms_per_call": ms, "tokens_per_s": M * world / (ms * 1e-3),
+                        "roofline": roof}
+        del w_in, w_out, hidden, o, outs, y
+        torch.cuda.empty_cache()
+    return res
+
+
 def prefill_flops_per_token(s, C=64):
     d = s.dk
     return s.nv * (10 * C * d + 6 * d * d + (2 / 3) * C * C)
@@ -651,7 +701,7 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
-    ap.add_argument("--phases", default="decode,verify,decode_mxfp8,stack,prefill,varlen")
+    ap.add_argument("--phases", default="decode,verify,decode_mxfp8,stack,proj,prefill,varlen")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--stack-layers", type=int, default=24, help="layers of the captured stack phase")
     ap.add_argument("--oracle-varlen-layers", type=int, default=3,
@@ -703,6 +753,8 @@ def main():
         results["decode_mxfp8"] = phase_decode_mxfp8(gdn, world, steps, warmup, peak_hbm)
     if "stack" in phases:
         results["stack"] = phase_stack(gdn, world, max(3, steps // 40), warmup, peak_hbm, n_layers=args.stack_layers)
+    if "proj" in phases:
+        results["proj"] = phase_proj(gdn, world, max(20, steps // 10), warmup, peak_hbm, peak_tf)
     if "prefill" in phases:
         results["prefill"] = phase_prefill(gdn, world, max(3, steps // 400), warmup, peak_tf)
     if "varlen" in phases:

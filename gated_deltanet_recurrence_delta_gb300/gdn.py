@@ -21,7 +21,7 @@ STATUS = {0: "GDN_OK", 1: "GDN_ERR_ARG", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_MASK", 
 EXPORTS = ("gdn_decode_step", "gdn_verify_with_checkpoints", "gdn_prefill_chunked",
            "gdn_prefill_workspace_size", "gdn_state_copy", "gdn_check_status", "gdn_last_error",
            "gdn_prefill_chunked_static_scratch", "gdn_commit_accepted", "gdn_decode_step_mxfp8",
-           "gdn_prefill_chunked_ckpt")
+           "gdn_prefill_chunked_ckpt", "gdn_in_proj", "gdn_out_proj")
 
 
 class GdnError(RuntimeError):
@@ -70,13 +70,15 @@ def load_library(path: Path | str | None = None):
     lib.gdn_state_copy.argtypes = [DP, P, P, P, P, P, P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, P]
     lib.gdn_prefill_chunked_ckpt.argtypes = [DP, IP, P, P, P, P, ctypes.c_size_t, P, ctypes.c_int32, P, P,
                                              ctypes.c_int32, P]
+    lib.gdn_in_proj.argtypes = [DP, ctypes.c_int32, ctypes.c_int32, P, P, P, P, P, P, P, P, P]
+    lib.gdn_out_proj.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, P, P, P, P]
     lib.gdn_decode_step_mxfp8.argtypes = [DP, ctypes.POINTER(InputsMxfp8), P, P, P, P]
     lib.gdn_commit_accepted.argtypes = [DP, ctypes.c_int32, ctypes.c_int32, P, P, P, P, P, P, P, P]
     lib.gdn_check_status.argtypes = [P]
     lib.gdn_last_error.restype = ctypes.c_char_p
     for name in ("gdn_decode_step", "gdn_verify_with_checkpoints", "gdn_prefill_chunked", "gdn_state_copy",
                  "gdn_check_status", "gdn_prefill_chunked_static_scratch", "gdn_commit_accepted",
-                 "gdn_decode_step_mxfp8", "gdn_prefill_chunked_ckpt"):
+                 "gdn_decode_step_mxfp8", "gdn_prefill_chunked_ckpt", "gdn_in_proj", "gdn_out_proj"):
         getattr(lib, name).restype = ctypes.c_int
     if path is None:
         _lib = lib
@@ -215,6 +217,21 @@ def commit_source_slot(accept_len, T: int) -> tuple[int, int]:
         raise ValueError("accept lengths must lie in [0, T] and there must be at least one path")
     win = max(range(len(L)), key=lambda p: (L[p], -p))
     return win, (win * T + L[win] - 1 if L[win] > 0 else -1)
+
+
+def in_proj(dims: Dims, hidden, w_in, q, k, v, z, a, b, stream=None):
+    """gdn_in_proj: hidden [M, H] x w_in [N, H]^T split into q, k, v, z, a, b."""
+    H = int(hidden.shape[-1])
+    M = hidden.numel() // H
+    _check(load_library().gdn_in_proj(ctypes.byref(dims), M, H, _ptr(hidden), _ptr(w_in), _ptr(q), _ptr(k), _ptr(v),
+                                      _ptr(z), _ptr(a), _ptr(b), _stream(stream)))
+
+
+def out_proj(o, w_out, y, stream=None):
+    """gdn_out_proj: y [M, H] = o [M, V] x w_out [H, V]^T."""
+    V, H = int(o.shape[-1]), int(w_out.shape[0])
+    M = o.numel() // V
+    _check(load_library().gdn_out_proj(M, H, V, _ptr(o), _ptr(w_out), _ptr(y), _stream(stream)))
 
 
 def check_status(stream=None):

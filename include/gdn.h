@@ -303,6 +303,28 @@ gdn_status gdn_commit_accepted(const gdn_dims *dims, int32_t n_layers, int32_t p
                                const int32_t *accept_len, const int32_t *dst_slot, int32_t *winner,
                                void *stream);
 
+/* The layer's in-projection, split into the layer's inputs in its epilogue.
+ * statecache.py (squad-0.8b), CacheQwen35._gdn: the hidden state times in_proj
+ * is split along the features into [mixed (2*kd + vd), z (vd), b (nv), a (nv)],
+ * and mixed into q (kd), k (kd), v (vd) channels: here one tcgen05 GEMM whose
+ * epilogue writes each feature straight into its tensor.
+ *   dims     nk, nv, dk, dv of the layer (kd = nk*dk, vd = nv*dv); other fields unused
+ *   M        tokens; H hidden size, a multiple of 64
+ *   hidden   bf16 [M][H]
+ *   w_in     bf16 [N][H], N = 2*kd + 2*vd + 2*nv rows in the order q | k | v | z | b | a
+ *   q, k     bf16 [M][kd];  v, z  bf16 [M][vd];  a, b  bf16 [M][nv]   (the gdn_inputs layouts)
+ * fp32 accumulation, each output rounded once to bf16. Every pointer 16-byte
+ * aligned; H*2 bytes a multiple of 16. A bounded wait that expires records
+ * GDN_ERR_TIMEOUT and the tile is not written. */
+gdn_status gdn_in_proj(const gdn_dims *dims, int32_t M, int32_t H, const void *hidden, const void *w_in, void *q,
+                       void *k, void *v, void *z, void *a, void *b, void *stream);
+
+/* The layer's out-projection after the gated RMSNorm: y = o W_out^T.
+ *   o      bf16 [M][V] (the layer's output rows, V = nv*dv, a multiple of 64)
+ *   w_out  bf16 [H][V];  y  bf16 [M][H]   (H a multiple of 8)
+ * Same GEMM and precision as gdn_in_proj. */
+gdn_status gdn_out_proj(int32_t M, int32_t H, int32_t V, const void *o, const void *w_out, void *y, void *stream);
+
 /* Synchronise `stream`, then return (and clear) a device-detected error
  * recorded on the current device since the last check (GDN_ERR_MASK,
  * GDN_ERR_INDEX, GDN_ERR_TIMEOUT; the lowest code wins when several were

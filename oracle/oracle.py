@@ -160,3 +160,23 @@ def layer(*, q, k, v, z, a, b, A_log, dt_bias, conv_w, norm_w, conv_state, state
         res["ckpt_state"] = cks
         res["ckpt_conv"] = ckc
     return res
+
+
+def in_proj(hidden, w_in, nk, nv, dk, dv):
+    """The layer's in-projection and its split (statecache.py, CacheQwen35._gdn:
+    the features of hidden x in_proj^T in the order [mixed (2 kd + vd), z (vd),
+    b (nv), a (nv)], mixed = [q (kd), k (kd), v (vd)]). hidden [M, H], w_in [N, H].
+    Returns the six float64 arrays, each [M, width]. The product is numpy's fp64
+    matmul of the exact inputs."""
+    x, w = _f64(hidden), _f64(w_in)
+    y = x.reshape(-1, x.shape[-1]) @ w.T
+    kd, vd = nk * dk, nv * dv
+    cuts = np.cumsum([kd, kd, vd, vd, nv])
+    q, k, v, z, b, a = np.split(y, cuts, axis=1)
+    return {"q": q, "k": k, "v": v, "z": z, "b": b, "a": a}
+
+
+def out_proj(o, w_out):
+    """The layer's out-projection: o [M, V] x w_out [H, V]^T in fp64."""
+    x, w = _f64(o), _f64(w_out)
+    return x.reshape(-1, x.shape[-1]) @ w.T
