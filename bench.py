@@ -70,8 +70,7 @@ KERNEL_SOURCES = {
     "commit_kernel": ("gdn_state_copy.cu",) + _COMMON_SOURCES,
     **{k: ("gdn_proj.cu", "gdn_umma.cuh") + _COMMON_SOURCES for k in ("gemm_in_proj_prefill", "gemm_in_proj_decode")},
     **{k: _PREFILL_SOURCES for k in ("front_kernel", "chunk_state_kernel", "output_kernel", "chunk_kernel",
-                                     "state_kernel", "front_kernel_gates", "output_kernel_varlen", "prefill_call_512",
-                                     "varlen_layer")},
+                                     "state_kernel", "front_kernel_gates", "prefill_call_512", "varlen_layer")},
 }
 
 
@@ -534,7 +533,7 @@ def phase_prefill(gdn, world, steps, warmup, peak_tf):
             gdn.prefill_chunked(dm, inp, d["conv_state"], d["state"], out, ws)
 
     ms = timed(world, steps, warmup, step)
-    kms = ms  # the roofline covers the whole call (front, chunk, state and output kernels)
+    kms = ms  # the roofline covers the whole call (front, chunk+state and output kernels)
     flops = prefill_flops_per_token(s) * T
     res = {"tokens_per_s": T * world / (ms * 1e-3), "ms_per_step": ms, "tokens_per_step": T,
            "ms_per_512_call": ms / (T // call), "launches_per_step": 3 * (T // call),
@@ -573,11 +572,11 @@ def phase_varlen(gdn, world, steps, warmup, peak_tf, n_layers=24):
     flops = prefill_flops_per_token(s) * real * n_layers
     res = {"real_tokens_per_s": real * world / (ms * 1e-3),
            "layer_tokens_per_s": real * n_layers * world / (ms * 1e-3), "ms_per_step": ms,
-           "real_tokens": real, "padded_tokens": padded, "layers": n_layers, "launches_per_step": 4 * n_layers,
-           "roofline": {"bound": "tensor", "kernel": "front+chunk+state+output", "achieved": flops / (kms * 1e-3) / 1e12, "peak": peak_tf,
+           "real_tokens": real, "padded_tokens": padded, "layers": n_layers, "launches_per_step": 3 * n_layers,
+           "roofline": {"bound": "tensor", "kernel": "front+chunk+state", "achieved": flops / (kms * 1e-3) / 1e12, "peak": peak_tf,
                         "unit": "TFLOP/s", "frac": flops / (kms * 1e-3) / 1e12 / peak_tf,
                         "traffic": scaled(dram_traffic("varlen_layer"), n_layers),
-                        "traffic_scope": f"{n_layers} layers (four kernels each)", "traffic_note": TRAFFIC_NOTE}}
+                        "traffic_scope": f"{n_layers} layers (three kernels each)", "traffic_note": TRAFFIC_NOTE}}
     del layers, ws
     torch.cuda.empty_cache()
     return res

@@ -13,9 +13,9 @@
 //   S_C = gamma_C S_0 + (K * exp(G_C - G))^T U'
 // (S on the stored transpose St[k][v]). exp(-G) is never formed.
 //
-// Passes (one call = front -> chunk -> state -> output, stream ordered; the
-// chunk and state passes are one grid when there are few chains, two kernels
-// otherwise):
+// Passes, stream ordered. Few (row, head) chains: front -> chunk + state in
+// one grid -> output. Otherwise: front -> chunk -> state, the state pass
+// forming the outputs itself:
 //   front  conv + SiLU + q/k L2 norm per (chunk slot, q/k/v head), written
 //          as split fp16 tiles, 128B-swizzled [token][d] images of Q, K and V
 //          (K-major operands where d is the contraction, MN-major ones where
@@ -27,25 +27,29 @@
 //          tcgen05 products [T; R] diag(beta gamma) K and [T; R] diag(beta) V
 //          (M=128,N=128,K=64 each; the factors ride on the columns of two
 //          [T; R] images) yield W, P W (-> Q'), U and P U (= O_local). Writes
-//          W|Q' as one swizzled image, U and O_local fp32, exp(G_C - G).
+//          W|Q' as one swizzled image, U in fp16, O_local in fp32, and
+//          exp(G_C - G).
 //   state  per (row, value head), sequential over its chunks with the state
 //          in registers (fp32) and an fp16 copy in shared memory:
 //          X = S_math W^T (tcgen05 M=128,N=64,K=128) -> U' = U - X,
 //          dS = (U' exp(G_C - G))^T-image x K-image (tcgen05 M=128,N=128,
-//          K=64, K read MN-major) ->
-//          S = gamma_C S + dS; the fp16 state image at every chunk start
-//          is copied out.
-//   output per (chunk slot, value head), all chunks in parallel:
-//          O = Q' S + O_local from that image (tcgen05 M=128,N=64,K=128),
-//          gated RMSNorm epilogue with z loaded by the TMA, bf16 rows out
-//          through the TMA.
+//          K=64, K read MN-major), S = gamma_C S + dS. With many chains the
+//          same product also yields O_S = Q' S (N=128: [W; Q']) and, while
+//          the tensor cores form dS, O = O_S + O_local, the gated RMSNorm
+//          and the bf16 rows go out. With few chains the fp16 state image
+//          at every chunk start is copied out instead, for
+//   output per (chunk slot, value head), all chunks in parallel on the SMs
+//          the chains leave idle: O = Q' S + O_local from that image
+//          (tcgen05 M=128,N=64,K=128), gated RMSNorm, bf16 rows through the
+//          TMA.
 // Operand tiles move between HBM and shared memory with bulk copies (TMA).
 // Precision: accumulators are fp32. The chunk kernel runs every product in
 // split fp16 (x = hi + lo, hi = fp16(x), lo = fp16(x - hi); a*b ~ hi*hi +
-// hi*lo + lo*hi, ~21 significant bits), so W, U, Q', O_local reach the state
-// kernel nearly exact; the state kernel's two products take plain fp16
-// operands (10-bit mantissa; bf16 would leave the final state ~3e-3 off in
-// relative Frobenius norm). With every product in plain fp16 the normalised
+// hi*lo + lo*hi, ~21 significant bits), so W, Q', O_local reach the state
+// kernel nearly exact (U in fp16: it only enters U' = U - X, which the state
+// product takes in fp16 anyway); the state kernel's two products take plain
+// fp16 operands (10-bit mantissa; bf16 would leave the final state ~3e-3 off
+// in relative Frobenius norm). With every product in plain fp16 the normalised
 // outputs of badly conditioned tokens drift by ~1e-2.
 #include "gdn_launch.h"
 #include "gdn_token.cuh"
@@ -68,9 +72,11 @@ struct Ws {
                         //                      kernel when the chunk and state passes are separate kernels
                         //                      (else the chunk unit forms the gates and writes the last 68,
                         //                      which the state pass reads)
-  float *ut, *ot;       // [S][nv][64][128]     U and O_local, token-major fp32, 16-byte chunk c of
-                        //                      row i stored at c ^ (i % 8) (32 KiB each)
-  __half *simg;         // [S][nv][2][128][64]  fp16 image of the state at the chunk's start (32 KiB)
+  __half *ut;           // [S][nv][64][128]     U, token-major fp16, 16-byte chunk c of row i
+                        //                      stored at c ^ (i % 8) (16 KiB)
+  float *ot;            // [S][nv][64][128]     O_local, token-major fp32, the same chunk order (32 KiB)
+  __half *simg;         // [S][nv][2][128][64]  fp16 image of the state at the chunk's start (32 KiB;
+                        //                      dense rows only: the grid of few chains)
   int *lr;              // [B][nv]              real length of each row, per value head; -1 = the
                         //                      row was rejected or the head's chain stopped
   int *flag;            // [S][nv]              chunk unit published (chunk + state in one grid)
@@ -79,7 +85,7 @@ struct Ws {
 
 constexpr size_t kImg = 64 * 128;    // halves in a 64x128 image
 constexpr size_t kWQ = 128 * 128;    // halves in the W|Q' image
-constexpr size_t kRowF = 128 * 64;   // floats in U / O_local
+constexpr size_t kRowF = 128 * 64;   // floats in O_local (and halves in U)
 constexpr int kGateRec = 324;        // floats in one gate record (a multiple of 16 bytes)
 constexpr int kGateLd = 320;         // floats of it a chunk unit loads (g, beta, G, exp(G), exp(G_C - G))
 constexpr int kSecOff = 256;         // exp(G_C - G) | gamma_C: the state pass's 68 floats
@@ -94,8 +100,8 @@ size_t slots_total(int B, int T, bool packed) {
 size_t ws_bytes(int B, int T, int nk, int nv, bool packed) {
   const size_t S = slots_total(B, T, packed);
   return 2 * a256(S * nk * kImg * 4) + a256(S * nv * kImg * 4) + a256(S * nv * kWQ * 2) +
-         a256(S * nv * kGateRec * 4) + 2 * a256(S * nv * kRowF * 4) +
-         a256(S * nv * kWQ * 2) + a256((size_t)B * nv * 4) + a256(S * nv * 4) + a256(S * 8);
+         a256(S * nv * kGateRec * 4) + a256(S * nv * kRowF * 2) + a256(S * nv * kRowF * 4) +
+         (packed ? 0 : a256(S * nv * kWQ * 2)) + a256((size_t)B * nv * 4) + a256(S * nv * 4) + a256(S * 8);
 }
 
 Ws carve(void *ws, int B, int T, int nk, int nv, bool packed) {
@@ -112,12 +118,12 @@ Ws carve(void *ws, int B, int T, int nk, int nv, bool packed) {
   p += a256(S * nv * kWQ * 2);
   w.gate = reinterpret_cast<float *>(p);
   p += a256(S * nv * kGateRec * 4);
-  w.ut = reinterpret_cast<float *>(p);
-  p += a256(S * nv * kRowF * 4);
+  w.ut = reinterpret_cast<__half *>(p);
+  p += a256(S * nv * kRowF * 2);
   w.ot = reinterpret_cast<float *>(p);
   p += a256(S * nv * kRowF * 4);
-  w.simg = reinterpret_cast<__half *>(p);
-  p += a256(S * nv * kWQ * 2);
+  w.simg = packed ? nullptr : reinterpret_cast<__half *>(p);
+  if (!packed) p += a256(S * nv * kWQ * 2);
   w.lr = reinterpret_cast<int *>(p);
   p += a256((size_t)B * nv * 4);
   w.flag = reinterpret_cast<int *>(p);
@@ -411,7 +417,7 @@ constexpr int kOffPTL = 180224;  // the same, lo parts
 constexpr int kOffSCR = 196608;  // fp32 [1024] solve scratch
 constexpr int kOffSm = 200704;   // 2 x the unit's gates g, beta, G, exp(G), exp(G_C - G): fp32 [5][64]
                                  // (unit parity p uses buffer p); barriers; tmem base
-constexpr int kOffBar = kOffSm + 2 * kGateLd * 4;  // [0..2] chunk-local loads and products, [3..5] the chain's, TMEM base
+constexpr int kOffBar = kOffSm + 2 * kGateLd * 4;  // chunk-local loads and products, TMEM base
 constexpr int kChunkSmem = kOffBar + 64 + 1024;     // + alignment slack
 
 __device__ __forceinline__ void store_split8(unsigned char *hi_img, unsigned char *lo_img, uint32_t off,
@@ -438,6 +444,7 @@ struct UnitPhase {
 // unit's K|Q tiles were requested that way by the unit before. The caller has
 // initialised the barriers at kOffBar, holds 256 TMEM columns at `tmem`
 // and has synchronised the CTA since any earlier use of shared memory or TMEM.
+// bars: the unit's barriers (two loads, the products).
 // gates_ready: the front kernel formed the gates; they arrive with the K|Q
 // tiles (else the unit forms them and stores exp(G_C - G), gamma_C for the
 // state pass).
@@ -450,7 +457,7 @@ struct UnitPhase {
 template <bool GATES_READY, class FindNext>
 __device__ __forceinline__ bool chunk_unit(unsigned char *sm, const LayerArgs &A, const Rows &R, const Ws &W, int s,
                                            int h, int r, int c, int parity, bool kq_issued, FindNext find_next,
-                                           uint32_t tmem, UnitPhase &ph, bool publish) {
+                                           uint32_t tmem, uint64_t *bars, UnitPhase &ph, bool publish) {
   constexpr bool gates_ready = GATES_READY;
   const int xo = parity ? kOffAF : kOffKQH, yo = parity ? kOffKQH : kOffAF;  // K|Q region, A/T/P region
   unsigned char *KQH = sm + xo, *KQL = sm + xo + (kOffKQL - kOffKQH);
@@ -464,8 +471,8 @@ __device__ __forceinline__ bool chunk_unit(unsigned char *sm, const LayerArgs &A
   float *sG = sb + 64;                                   // inclusive prefix of g
   float *sgam = sG + 64;                                 // exp(G_j)
   float *sec = sgam + 64;                                // exp(G_C - G_j)
-  uint64_t *bar_ld = reinterpret_cast<uint64_t *>(sm + kOffBar);  // [0]: K|Q tiles, [1]: V tiles
-  uint64_t *bar_mma = bar_ld + 2;
+  uint64_t *bar_ld = bars;  // [0]: K|Q tiles, [1]: V tiles
+  uint64_t *bar_mma = bars + 2;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int kh = h / A.G;
@@ -742,13 +749,14 @@ __device__ __forceinline__ bool chunk_unit(unsigned char *sm, const LayerArgs &A
   // the A / T / [T; R] / P tiles are consumed: that region takes the next unit's K|Q
   if (tid == 0 && nx.x >= 0) issue_kq(nx.x, nx.y / A.G, sm + yo, nx.y, parity ^ 1);
   {
-    // W / Q' into the K|Q image (plain fp16); U / O_local rows, fp32, staged in
-    // the free B2 tiles in the row-swizzled layout of the workspace (16-byte
-    // chunk c of row i at c ^ (i % 8)), then bulk-stored
+    // W / Q' into the K|Q image (plain fp16); U rows (fp16) and O_local rows
+    // (fp32) staged in the free B2 tiles in the row-swizzled layout of the
+    // workspace (16-byte chunk c of row i at c ^ (i % 8)), then bulk-stored
     const int q = warp & 3, hh = warp >> 2, row = 32 * q + lane, i = row & (CH - 1);
     const bool upper = row >= CH;
     const float gam = sgam[i];
-    float4 *stage = reinterpret_cast<float4 *>(sm + kOffB2H + (upper ? 32768 : 0)) + (size_t)i * 32;
+    float4 *stage = reinterpret_cast<float4 *>(sm + kOffB2H + 32768) + (size_t)i * 32;  // O_local row i
+    uint4 *stage_u = reinterpret_cast<uint4 *>(sm + kOffB2H) + (size_t)i * 16;          // U row i
 #pragma unroll 1
     for (int cb = 0; cb < 4; ++cb) {
       float v[32];
@@ -774,10 +782,16 @@ __device__ __forceinline__ bool chunk_unit(unsigned char *sm, const LayerArgs &A
           }
           *dst = make_uint4(pack_h2(y[0], y[1]), pack_h2(y[2], y[3]), pack_h2(y[4], y[5]), pack_h2(y[6], y[7]));
         }
-      } else {
+      } else if (upper) {
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4)
           stage[(8 * cb + c4) ^ (i & 7)] = make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
+      } else {
+#pragma unroll
+        for (int c2 = 0; c2 < 4; ++c2)
+          stage_u[(4 * cb + c2) ^ (i & 7)] =
+              make_uint4(pack_h2(v[8 * c2], v[8 * c2 + 1]), pack_h2(v[8 * c2 + 2], v[8 * c2 + 3]),
+                         pack_h2(v[8 * c2 + 4], v[8 * c2 + 5]), pack_h2(v[8 * c2 + 6], v[8 * c2 + 7]));
       }
     }
     fence_proxy_async_smem();
@@ -789,7 +803,7 @@ __device__ __forceinline__ bool chunk_unit(unsigned char *sm, const LayerArgs &A
       if (hh == 0) {
         bulk_s2g(W.wq + sh * kWQ, KQH, 32768);
       } else {
-        bulk_s2g(W.ut + sh * kRowF, sm + kOffB2H, 32768);
+        bulk_s2g(W.ut + sh * kRowF, sm + kOffB2H, 16384);
         bulk_s2g(W.ot + sh * kRowF, sm + kOffB2H + 32768, 32768);
       }
       bulk_commit();
@@ -853,7 +867,8 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
       return make_int2(n.x < 0 ? -1 : n.x / A.nv, n.x < 0 ? 0 : n.x % A.nv);
     };
     const bool ok =
-        chunk_unit<true>(sm, A, R, W, cur.x / A.nv, cur.x % A.nv, cur.y, cur.z, parity, kq, find_next, tmem, ph, false);
+        chunk_unit<true>(sm, A, R, W, cur.x / A.nv, cur.x % A.nv, cur.y, cur.z, parity, kq, find_next, tmem, bar, ph,
+                         false);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -870,22 +885,34 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
 
 // ------------------------------------------------------------ state pass
 //
-// The sequential part only: per (row, value head), over its chunks,
-//   X = S_math W^T (tcgen05 M=128 v, N=64 tokens, K=128) -> U' = U - X,
-//   dS = (U' * exp(G_C - G))^T-image x K-image (M=128, N=128, K=64, K read MN-major) ->
-//   S = gamma_C S + dS,
-// with the state in registers (fp32) and an fp16 copy in shared memory. The
-// fp16 image of the state at the start of every chunk is copied out (bulk
-// store) for the output kernel, which does O = Q' S + O_local off this path.
+// The sequential part, per (row, value head) over its chunks, with the state
+// in registers (fp32) and its fp16 image in shared memory:
+//   [X | O_S] = S_math [W; Q']^T (tcgen05 M=128 v, N=128 tokens, K=128),
+//   U' = U - X, dS = (U' * exp(G_C - G))^T-image x K-image (M=128, N=128,
+//   K=64, K read MN-major), S = gamma_C S + dS,
+// and the chunk's outputs O = O_S + O_local (O_S = Q' S from the state at the
+// chunk's start) with the gated RMSNorm (statecache.py, gated_rmsnorm), formed
+// while the tensor cores compute dS. Padded tokens of the row get zeros.
 
 constexpr int kSOffS = 0;         // S_math fp16 image [2 kb][128 rows][128 B] (32 KiB)
-constexpr int kSOffW = 32768;     // 2 x W image [2 kb][64 rows][128 B] (16 KiB each)
-constexpr int kSOffKT = 65536;    // 2 x K image (hi) [2 kb][64 rows][128 B] (16 KiB each), read MN-major
-constexpr int kSOffUT = 98304;    // 2 x U fp32 [64 tokens][128 v] (32 KiB each)
-constexpr int kSOffUP = 163840;   // U'^T image [128 rows][128 B] (16 KiB)
-constexpr int kSOffSec = 180224;  // 2 x the exp(G_C - G_j) | gamma_C record, fp32 [68]
-constexpr int kSOffBar = 180800;  // barriers, TMEM base
+constexpr int kSOffWQ = 32768;    // 2 x W|Q' image [2 kb][128 rows][128 B] (32 KiB each)
+constexpr int kSOffKT = 98304;    // 2 x K image (hi) [2 kb][64 rows][128 B] (16 KiB each), read MN-major
+constexpr int kSOffUT = 131072;   // 2 x U fp16 [64 tokens][128 v] (16 KiB each)
+constexpr int kSOffOL = 163840;   // O_local fp32 [64 tokens][128 v] (32 KiB; one chunk at a time)
+constexpr int kSOffUP = 196608;   // U'^T image [128 rows][128 B] (16 KiB)
+constexpr int kSOffSec = 212992;  // 2 x the exp(G_C - G_j) | gamma_C record, fp32 [68]
+constexpr int kSOffBar = kSOffSec + 2 * kSecRec * 4;  // the chain's barriers (4), TMEM base
 constexpr int kStateSmem = kSOffBar + 64 + 1024;
+// The outputs of a chunk are formed in buffers free at that time: o (fp32
+// [64 tokens][128 v], the O_local layout) in the state image, which the first
+// product has read and the step rewrites at its end; the RMS partials (fp32
+// [4][64], then [64] rstd) in the chunk's U buffer, consumed before them, whose
+// next loads are requested after they are read.
+// chunk + state in one grid: the units' layout below kOffBar, the chain's above; barriers past both
+constexpr int kMOffBar = kSOffBar > kOffBar ? kSOffBar : kOffBar;  // [0..2] units, [3..6] the chain, TMEM base
+constexpr int kMergedSmem = kMOffBar + 64 + 1024;
+static_assert(kStateSmem + 1024 <= 232448 && kMergedSmem + 1024 <= 232448,
+              "shared memory of one CTA (with room for the static shared variables)");
 
 // Polls of a unit flag before a blocking wait gives up (about a quarter of a
 // second with the 64 ns sleeps between polls).
@@ -933,11 +960,11 @@ __device__ __forceinline__ bool unit_ready(const int *flag, bool block, unsigned
 
 // What the (row b, value head h) chain needs before its chunks, and nothing
 // of theirs: the row's checks (slot, mask of ones then zeros -> real length
-// Lr, recorded per head for the output pass). False when the row is rejected
+// Lr, recorded per head for an output pass). False when the row is rejected
 // (its status is set). With prefetch_state the head's fp32 state is fetched
 // into L2 for the chain.
-__device__ __forceinline__ bool chain_prologue(const LayerArgs &A, const Rows &R, int Ttot, const Ws &W, int b,
-                                               int h, bool prefetch_state, int &Lr_out) {
+__device__ __forceinline__ bool chain_prologue(const LayerArgs &A, const Rows &R, int Ttot, const Ws &W, int b, int h,
+                                               bool prefetch_state, int &Lr_out) {
   __shared__ int s_min_zero, s_max_one, s_bad;
   const int tid = threadIdx.x;
   const int start = R.start(b), len = R.len(b);
@@ -972,7 +999,7 @@ __device__ __forceinline__ bool chain_prologue(const LayerArgs &A, const Rows &R
     }
     return false;
   }
-  if (tid == 0) W.lr[(size_t)b * A.nv + h] = Lr;  // read by the output kernel
+  if (tid == 0) W.lr[(size_t)b * A.nv + h] = Lr;  // read by an output pass
   Lr_out = Lr;
   if (prefetch_state) {  // 64 KiB: two 128-byte lines per thread
     const char *gS = reinterpret_cast<const char *>(A.state + ((size_t)slot * A.nv + h) * HD * HD);
@@ -982,29 +1009,40 @@ __device__ __forceinline__ bool chain_prologue(const LayerArgs &A, const Rows &R
   return true;
 }
 
-// After the (row b, value head h) chain completed: the conv-tail update of the
-// head's own channels, xin rows Lr .. Lr+2 (old rows when Lr < 3), in place.
-// A chain that stopped leaves them as they were.
-__device__ __forceinline__ void chain_tail(const LayerArgs &A, const Rows &R, int b, int h, int Lr) {
-  bf16 *cs = A.conv_state + (size_t)row_slot(A, b) * KC * A.C;
-  conv_tail_at<HD>(A, R.start(b), h, Lr, cs, cs);
+// The end of an accepted (row b, value head h) chain: when it completed, the
+// conv-tail update of the head's own channels, xin rows Lr .. Lr+2 (old rows
+// when Lr < 3), in place; when it stopped (a wait expired, or this grid's
+// units did not complete), the head is marked so that an output pass writes
+// nothing for it, and its state and conv-tail channels stay as they were.
+__device__ __forceinline__ void chain_finish(const LayerArgs &A, const Rows &R, const Ws &W, int b, int h, int Lr,
+                                             bool completed) {
+  if (completed) {
+    bf16 *cs = A.conv_state + (size_t)row_slot(A, b) * KC * A.C;
+    conv_tail_at<HD>(A, R.start(b), h, Lr, cs, cs);
+  } else if (threadIdx.x == 0) {
+    W.lr[(size_t)b * A.nv + h] = -1;
+  }
 }
 
 // The sequential pass of one (row b, value head h) chain, after its
-// chain_prologue accepted the row. The caller has initialised the two load
-// barriers `bar_ld` and the product barrier `bar_mma`, holds 256 TMEM columns
-// at `tmem` and has synchronised the CTA since any earlier use of shared
-// memory or TMEM. wait_units: the chunk units run in this grid, so each
-// chunk's loads wait for its unit's flag. Returns false when a bounded wait
-// ran out.
-__device__ __forceinline__ bool state_chain(unsigned char *sm, uint64_t *bar_ld, uint64_t *bar_mma,
-                                            const LayerArgs &A, const Rows &R, const Ws &W, int b, int h, int Lr,
-                                            uint32_t tmem, bool wait_units) {
+// chain_prologue accepted the row. bars: the chain's barriers (two loads, the
+// products, O_local). The caller holds 256 TMEM columns at `tmem` and has
+// synchronised the CTA since any earlier use of shared memory or TMEM.
+// OUT: the chain forms the chunks' outputs (else it copies out the state image
+// at every chunk start, for the output kernel). wait_units: the chunk units run
+// in this grid, so each chunk's loads wait for its unit's flag. Returns false
+// when a bounded wait ran out (with OUT the outputs of the chunks before it are
+// written).
+template <bool OUT>
+__device__ __forceinline__ bool state_chain(unsigned char *sm, uint64_t *bars, const LayerArgs &A, const Rows &R,
+                                            const Ws &W, int b, int h, int Lr, uint32_t tmem, bool wait_units) {
+  uint64_t *bar_ld = bars, *bar_mma = bars + 2, *bar_ol = bars + 3;
   unsigned char *SI = sm + kSOffS;
   unsigned char *UP = sm + kSOffUP;
+  float *OL = reinterpret_cast<float *>(sm + kSOffOL);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int kh = h / A.G;
-  const int len = R.len(b), slot = row_slot(A, b);
+  const int start = R.start(b), len = R.len(b), slot = row_slot(A, b);
   const int n_chunks = (len + CH - 1) / CH;
   const int s0 = R.slot0(b);
   __shared__ RowCkpts ck;  // checkpoints this row asked for (prefix-cache states inside the call)
@@ -1013,18 +1051,14 @@ __device__ __forceinline__ bool state_chain(unsigned char *sm, uint64_t *bar_ld,
     if (A.n_ckpt > 0) gather_row_ckpts(A, b, h, Lr, ck);
   }
 
-  // chunk ci's W rows (rows 0-63 of each column block of the W|Q' image),
-  // the fp16 K image (hi) of the key head, U and exp(G_C - G)
+  // chunk ci's W|Q' image, the fp16 K image (hi) of the key head, U and exp(G_C - G)
   auto issue_loads = [&](int ci) {  // thread 0
     const int buf = ci & 1, s = s0 + ci;
     const size_t sh = (size_t)s * A.nv + h;
-    const unsigned char *wq = reinterpret_cast<const unsigned char *>(W.wq + sh * kWQ);
-    unsigned char *wdst = sm + kSOffW + buf * 16384;
-    mbar_arrive_expect_tx(&bar_ld[buf], 16384 + 16384 + 32768 + kSecRec * 4);
-    bulk_g2s(wdst, wq, 8192, &bar_ld[buf]);
-    bulk_g2s(wdst + 8192, wq + 16384, 8192, &bar_ld[buf]);
+    mbar_arrive_expect_tx(&bar_ld[buf], 32768 + 16384 + 16384 + kSecRec * 4);
+    bulk_g2s(sm + kSOffWQ + buf * 32768, W.wq + sh * kWQ, 32768, &bar_ld[buf]);
     bulk_g2s(sm + kSOffKT + buf * 16384, W.kimg + ((size_t)s * A.nk + kh) * 2 * kImg, 16384, &bar_ld[buf]);
-    bulk_g2s(sm + kSOffUT + buf * 32768, W.ut + sh * kRowF, 32768, &bar_ld[buf]);
+    bulk_g2s(sm + kSOffUT + buf * 16384, W.ut + sh * kRowF, 16384, &bar_ld[buf]);
     bulk_g2s(sm + kSOffSec + buf * kSecRec * 4, W.gate + sh * kGateRec + kSecOff, kSecRec * 4, &bar_ld[buf]);
   };
   // thread 0: the last chunk whose loads are issued, and the last chunk up to
@@ -1032,12 +1066,24 @@ __device__ __forceinline__ bool state_chain(unsigned char *sm, uint64_t *bar_ld,
   // wait expired (no load of that chunk is in flight), the chain stops
   int issued = -1, acquired = wait_units ? -1 : n_chunks - 1;
   bool gave_up = false;
+  // thread 0: O_local has one buffer: chunk ci's is requested once chunk
+  // ci - 1's outputs have read theirs and chunk ci's unit is acquired
+  int ol_issued = -1, ol_done = -1;
+  auto try_issue_ol = [&]() {
+    const int ci = ol_issued + 1;
+    if (OUT && ci < n_chunks && ol_done == ol_issued && issued >= ci) {
+      mbar_arrive_expect_tx(bar_ol, 32768);
+      bulk_g2s(sm + kSOffOL, W.ot + ((size_t)(s0 + ci) * A.nv + h) * kRowF, 32768, bar_ol);
+      ol_issued = ci;
+    }
+  };
   auto issue_when_ready = [&](int ci, bool block) {  // thread 0
     if (gave_up) return;
     if (ci <= acquired || unit_ready(W.flag + (size_t)(s0 + ci) * A.nv + h, block, A.status, true)) {
       if (ci > acquired) acquired = ci;
       issue_loads(ci);
       issued = ci;
+      try_issue_ol();
     } else if (block) {
       gave_up = true;
     }
@@ -1089,14 +1135,33 @@ __device__ __forceinline__ bool state_chain(unsigned char *sm, uint64_t *bar_ld,
   if (!wait_units && tid == 0 && n_chunks > 0) issue_when_ready(0, true);
   tc_fence_before();
   __syncthreads();
-  if (tid == 0 && n_chunks > 0) {  // the state image at the start of chunk 0
+  if (!OUT && tid == 0 && n_chunks > 0) {  // the state image at the start of chunk 0
     bulk_s2g(W.simg + ((size_t)s0 * A.nv + h) * kWQ, SI, 32768);
     bulk_commit();
   }
+  // the output rows' layout: thread r = tid % 128 of warp group hh takes values
+  // 8c .. 8c+7 (c = r % 16) of tokens 32hh + r / 16 + 8k, k = 0..3
+  const int orow = 32 * hh + ((tid & 127) >> 4), oc = tid & 15;
+  float wn[8];  // the RMSNorm weights of those values
+#pragma unroll
+  for (int e = 0; e < 8; ++e) wn[e] = OUT ? ldbf(A.norm_w + 8 * oc + e) : 0.0f;
+  // z at those places (16-byte loads), for the chunk ahead of the outputs
+  uint4 z8[4];
+  auto load_z = [&](int ci) {
+    const int zreal = min(CH, Lr - ci * CH);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int i = orow + 8 * k;
+      z8[k] = i < zreal ? __ldg(reinterpret_cast<const uint4 *>(A.z + ((size_t)(start + ci * CH + i) * A.nv + h) * HD) + oc)
+                        : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  if (OUT && n_chunks > 0) load_z(0);
 
   bool ok = true;
   for (int ci = 0; ci < n_chunks; ++ci) {
-    const int buf = ci & 1, s = s0 + ci;
+    const int buf = ci & 1, t0 = ci * CH;
+    const int ntok = min(CH, len - t0), nreal = max(0, min(CH, Lr - t0));
     int seen = -1;  // thread 0: the last chunk up to which the units read as published (unordered reads)
     if (tid == 0) {  // a chunk not prefetched is waited for; the next one is prefetched when ready
       if (issued < ci) issue_when_ready(ci, true);
@@ -1116,8 +1181,9 @@ __device__ __forceinline__ bool state_chain(unsigned char *sm, uint64_t *bar_ld,
     const float gC = reinterpret_cast<const float *>(sm + kSOffSec + buf * kSecRec * 4)[CH];
     if (tid == 0) {
       tc_fence_after();
-      umma_tile(tmem, smem_u32(SI), 128, smem_u32(sm + kSOffW + buf * 16384), 64, 128, umma_idesc_f16(128, 64),
-                false);
+      // rows 0-63 of the W|Q' image are W (N=64), all 128 rows [W; Q'] (N=128)
+      umma_tile(tmem, smem_u32(SI), 128, smem_u32(sm + kSOffWQ + buf * 32768), 128, 128,
+                umma_idesc_f16(128, OUT ? 128 : 64), false);
       umma_commit(bar_mma);
       if (seen > ci) {  // published: one acquire for all of them (off the product's path), then the loads
         fence_acq_rel_gpu();
@@ -1134,21 +1200,20 @@ __device__ __forceinline__ bool state_chain(unsigned char *sm, uint64_t *bar_ld,
     tc_fence_after();
     {
       // (U - W S) * exp(G_C - G) for tokens 32hh .. 32hh+31 of value row v -> fp16 image row v
-      const float *ut = reinterpret_cast<const float *>(sm + kSOffUT + buf * 32768);
+      const __half *ut = reinterpret_cast<const __half *>(sm + kSOffUT + buf * 16384);
       const float *sec = reinterpret_cast<const float *>(sm + kSOffSec + buf * kSecRec * 4) + 32 * hh;
       float x[32];
       tmem_ld32(tmem_at(tmem, q, 32 * hh), x);
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        float y[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int i = 32 * hh + 8 * c4 + e;  // token; element (i, v) sits in chunk (v / 4) ^ (i % 8) of row i
-          y[e] = (ut[i * HD + ((((v >> 2) ^ (i & 7))) << 2) + (v & 3)] - x[8 * c4 + e]) * sec[8 * c4 + e];
-        }
-        *reinterpret_cast<uint4 *>(UP + sw128_chunk(128, v, 4 * hh + c4)) =
-            make_uint4(pack_h2(y[0], y[1]), pack_h2(y[2], y[3]), pack_h2(y[4], y[5]), pack_h2(y[6], y[7]));
+      for (int e = 0; e < 32; ++e) {  // every read before the first store (see the output rows)
+        const int i = 32 * hh + e;     // token; element (i, v) sits in chunk (v / 8) ^ (i % 8) of row i
+        x[e] = (__half2float(ut[i * HD + ((((v >> 3) ^ (i & 7))) << 3) + (v & 7)]) - x[e]) * sec[e];
       }
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4)
+        *reinterpret_cast<uint4 *>(UP + sw128_chunk(128, v, 4 * hh + c4)) =
+            make_uint4(pack_h2(x[8 * c4], x[8 * c4 + 1]), pack_h2(x[8 * c4 + 2], x[8 * c4 + 3]),
+                       pack_h2(x[8 * c4 + 4], x[8 * c4 + 5]), pack_h2(x[8 * c4 + 6], x[8 * c4 + 7]));
       fence_proxy_async_smem();
     }
     tc_fence_before();
@@ -1158,7 +1223,86 @@ __device__ __forceinline__ bool state_chain(unsigned char *sm, uint64_t *bar_ld,
       umma_tile_bmn(tmem + 128, smem_u32(UP), 128, smem_u32(sm + kSOffKT + buf * 16384), 8192, 64,
                     umma_idesc_f16_bmn(128, 128), false);
       umma_commit(bar_mma);
-      bulk_wait_read_all();  // the copy of the previous state image has left shared memory
+      if (!OUT) bulk_wait_read_all();  // the copy of the previous state image has left shared memory
+    }
+    // ---- the chunk's outputs while dS forms: O = O_S + O_local (value row v =
+    //      TMEM lane, tokens 32hh .. 32hh+31 = TMEM columns 64 + 32hh ..), then
+    //      the gated RMSNorm over the 128 value rows of each token
+    if (OUT && !cta_wait(bar_ol, (uint32_t)(ci & 1), A.status)) {
+      ok = false;
+      break;
+    }
+    if (OUT) {
+      float *red = reinterpret_cast<float *>(sm + kSOffUT + buf * 16384);  // [4][64] (see kStateSmem)
+      float *rstd = red + 256;                                            // [64]
+      float *OS = reinterpret_cast<float *>(SI);                         // o, in the O_local layout
+      float o[32];
+      tmem_ld32(tmem_at(tmem, q, 64 + 32 * hh), o);
+      // o += O_local (element (i, v) sits in chunk (v / 4) ^ (i % 8) of row i), kept in OS
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int i = 32 * hh + e;
+        o[e] += OL[i * HD + ((((v >> 2) ^ (i & 7))) << 2) + (v & 3)];
+      }
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int i = 32 * hh + e;
+        OS[i * HD + ((((v >> 2) ^ (i & 7))) << 2) + (v & 3)] = o[e];
+      }
+      // sum over the warp's 32 rows of o^2 for each of the 32 tokens: after the
+      // transposing butterfly lane l holds token l's partial
+#pragma unroll
+      for (int e = 0; e < 32; ++e) o[e] *= o[e];
+#pragma unroll
+      for (int w = 16; w >= 1; w >>= 1) {
+        const bool up = (lane & w) != 0;
+#pragma unroll
+        for (int e = 0; e < w; ++e) {
+          const float send = up ? o[e] : o[e + w];
+          const float keep = up ? o[e + w] : o[e];
+          o[e] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+        }
+      }
+      red[q * 64 + 32 * hh + lane] = o[0];
+      __syncthreads();
+      if (tid == 0) {  // every thread has read this chunk's O_local: the next chunk's may come
+        ol_done = ci;
+        try_issue_ol();
+      }
+      if (q == 0) {
+        const int t = 32 * hh + lane;
+        const float ss = red[t] + red[64 + t] + red[128 + t] + red[192 + t];
+        rstd[t] = rsqrtf(ss / (float)HD + A.rms_eps);
+      }
+      named_sync(3 + hh, 128);
+      // the bf16 rows, 16 bytes per access; padded tokens of the row get zeros
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int i = orow + 8 * k;
+        if (i < ntok) {
+          uint4 res = make_uint4(0u, 0u, 0u, 0u);
+          if (i < nreal) {
+            const float4 oa = *reinterpret_cast<const float4 *>(OS + i * HD + (((2 * oc) ^ (i & 7)) << 2));
+            const float4 ob = *reinterpret_cast<const float4 *>(OS + i * HD + (((2 * oc + 1) ^ (i & 7)) << 2));
+            const float rs = rstd[i];
+            const float ov[8] = {oa.x, oa.y, oa.z, oa.w, ob.x, ob.y, ob.z, ob.w};
+            const uint4 zk = z8[k];
+            const uint32_t zw[4] = {zk.x, zk.y, zk.z, zk.w};
+            uint32_t pw[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float z0 = __uint_as_float(zw[e] << 16), z1 = __uint_as_float(zw[e] & 0xffff0000u);
+              const float y0 = ov[2 * e] * rs * (wn[2 * e] * silu_fast(z0));
+              const float y1 = ov[2 * e + 1] * rs * (wn[2 * e + 1] * silu_fast(z1));
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(y0, y1);
+              pw[e] = *reinterpret_cast<const uint32_t *>(&b2);
+            }
+            res = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+          }
+          reinterpret_cast<uint4 *>(A.out + ((size_t)(start + t0 + i) * A.nv + h) * HD)[oc] = res;
+        }
+      }
+      if (ci + 1 < n_chunks) load_z(ci + 1);
     }
     if (!cta_wait(bar_mma, 1, A.status)) {
       ok = false;
@@ -1186,26 +1330,16 @@ __device__ __forceinline__ bool state_chain(unsigned char *sm, uint64_t *bar_ld,
     write_simg();
     tc_fence_before();
     __syncthreads();
-    if (tid == 0 && ci + 1 < n_chunks) {  // the state image at the start of chunk ci + 1
-      bulk_s2g(W.simg + ((size_t)(s + 1) * A.nv + h) * kWQ, SI, 32768);
+    if (!OUT && tid == 0 && ci + 1 < n_chunks) {  // the state image at the start of chunk ci + 1
+      bulk_s2g(W.simg + ((size_t)(s0 + ci + 1) * A.nv + h) * kWQ, SI, 32768);
       bulk_commit();
     }
   }
-  if (tid == 0) bulk_wait_read_all();  // no bulk store may still read this CTA's shared memory
+  if (!OUT && tid == 0) bulk_wait_read_all();  // no bulk store may still read this CTA's shared memory
   if (!ok) return false;
 #pragma unroll
   for (int k = 0; k < 64; ++k) gS[(size_t)(64 * hh + k) * HD + v] = Sv[k];
   return true;
-}
-
-// The end of an accepted chain: when it completed, the conv-tail update of the
-// head's channels; when it stopped (a wait expired, or this grid's units did
-// not complete), the head is marked so that the output pass writes nothing
-// for it: its state, conv-tail channels and outputs stay as they were.
-__device__ __forceinline__ void chain_finish(const LayerArgs &A, const Rows &R, const Ws &W, int b, int h, int Lr,
-                                             bool completed) {
-  if (completed) chain_tail(A, R, b, h, Lr);
-  else if (threadIdx.x == 0) W.lr[(size_t)b * A.nv + h] = -1;
 }
 
 __global__ void __launch_bounds__(256, 1) state_kernel(LayerArgs A, Rows R, int Ttot, Ws W) {
@@ -1213,9 +1347,9 @@ __global__ void __launch_bounds__(256, 1) state_kernel(LayerArgs A, Rows R, int 
   const uint32_t raw = smem_u32(smem_raw);
   unsigned char *sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   uint64_t *bar = reinterpret_cast<uint64_t *>(sm + kSOffBar);
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 3);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 4);
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 3; ++i) mbar_init(&bar[i], 1);
+    for (int i = 0; i < 4; ++i) mbar_init(&bar[i], 1);
     fence_mbar_init();
   }
   if (threadIdx.x < 32) tmem_alloc(tmem_slot, 256);
@@ -1226,7 +1360,7 @@ __global__ void __launch_bounds__(256, 1) state_kernel(LayerArgs A, Rows R, int 
   const int b = blockIdx.x / A.nv, h = blockIdx.x % A.nv;
   int Lr = 0;
   if (chain_prologue(A, R, Ttot, W, b, h, false, Lr))
-    chain_finish(A, R, W, b, h, Lr, state_chain(sm, bar, bar + 2, A, R, W, b, h, Lr, tmem, false));
+    chain_finish(A, R, W, b, h, Lr, state_chain<true>(sm, bar, A, R, W, b, h, Lr, tmem, false));
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x < 32) tmem_dealloc(tmem, 256);
@@ -1246,10 +1380,10 @@ __global__ void __launch_bounds__(256, 1) chunk_state_kernel(LayerArgs A, Rows R
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   unsigned char *sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  uint64_t *bar = reinterpret_cast<uint64_t *>(sm + kOffBar);  // [0..2] units, [3..5] the chain
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 6);
+  uint64_t *bar = reinterpret_cast<uint64_t *>(sm + kMOffBar);  // [0..2] units, [3..6] the chain
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 7);
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 6; ++i) mbar_init(&bar[i], 1);
+    for (int i = 0; i < 7; ++i) mbar_init(&bar[i], 1);
     fence_mbar_init();
   }
   if (threadIdx.x < 32) tmem_alloc(tmem_slot, 256);
@@ -1272,7 +1406,7 @@ __global__ void __launch_bounds__(256, 1) chunk_state_kernel(LayerArgs A, Rows R
       return v < n_units ? make_int2((rh2 / A.nv) * R.cpr + c2, rh2 % A.nv) : make_int2(-1, 0);
     };
     ok = chunk_unit<false>(sm, A, R, W, r * R.cpr + c, rh % A.nv, r, c, parity, u != (int)blockIdx.x, find_next, tmem,
-                           ph, true);
+                           bar, ph, true);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1282,7 +1416,7 @@ __global__ void __launch_bounds__(256, 1) chunk_state_kernel(LayerArgs A, Rows R
   griddep_trigger();
   if (chain)
     chain_finish(A, R, W, j / A.nv, j % A.nv, Lr,
-                 ok && state_chain(sm, bar + 3, bar + 5, A, R, W, j / A.nv, j % A.nv, Lr, tmem, true));
+                 ok && state_chain<false>(sm, bar + 3, A, R, W, j / A.nv, j % A.nv, Lr, tmem, true));
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x < 32) tmem_dealloc(tmem, 256);
@@ -1290,7 +1424,8 @@ __global__ void __launch_bounds__(256, 1) chunk_state_kernel(LayerArgs A, Rows R
 
 // ------------------------------------------------------------ outputs
 //
-// Per (chunk slot, value head), all chunks in parallel: O^T = S_img Q'^T
+// For the grid of few chains. Per (chunk slot, value head), all chunks in
+// parallel: O^T = S_img Q'^T
 // (tcgen05 M=128 v, N=64 tokens, K=128) from the state image at the chunk's
 // start, + O_local, then the gated RMSNorm (statecache.py, gated_rmsnorm)
 // and bf16 rows out through the TMA. Padded tokens of the row get zeros.
@@ -1305,16 +1440,14 @@ constexpr int kOutSmem = kOOffBar + 64 + 1024;
 
 // omap: out viewed as [Ttot][nv*dv] bf16, box [32 tokens][128 values];
 // zmap: z viewed the same way, box [64 tokens][128 values].
-// early: 1 = Q' and O_local were complete before the kernel this one follows
-// started (separate chunk and state kernels): they load before the wait.
-// 0 = they come from the grid this one follows, which published each chunk
-// unit with a flag: the unit's flag is acquired, then they load, still before
-// the wait (the state images load after it). That grid triggers this launch
-// only after all its units are published, so the flag is set when read: the
-// acquire orders memory, it does not wait for a running producer.
+// Q' and O_local come from the grid this one follows, which published each
+// chunk unit with a flag: the unit's flag is acquired, then they load before
+// the wait for that grid (the state images load after it). That grid triggers
+// this launch only after all its units are published, so the flag is set when
+// read: the acquire orders memory, it does not wait for a running producer.
 __global__ void __launch_bounds__(256, 2) output_kernel(LayerArgs A, Rows R, int Ttot, Ws W,
                                                         const __grid_constant__ CUtensorMap omap,
-                                                        const __grid_constant__ CUtensorMap zmap, int early) {
+                                                        const __grid_constant__ CUtensorMap zmap) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   unsigned char *sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -1354,7 +1487,7 @@ __global__ void __launch_bounds__(256, 2) output_kernel(LayerArgs A, Rows R, int
   };
   bool issued = false;  // thread 0: Q', O_local and z were requested (else its flag wait expired)
   if (tid == 0) {
-    issued = early || unit_ready(W.flag + sh, true, A.status, false);
+    issued = unit_ready(W.flag + sh, true, A.status, false);
     if (issued) issue_qoz();
   }
   griddep_wait();  // the state pass's images and row lengths are complete
@@ -1497,7 +1630,7 @@ gdn_status launch_prefill_tc(const LayerArgs &A, void *ws, cudaStream_t stream) 
         cudaFuncSetAttribute(tc::output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kOutSmem) !=
             cudaSuccess ||
         cudaFuncSetAttribute(tc::chunk_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             tc::kChunkSmem) != cudaSuccess)
+                             tc::kMergedSmem) != cudaSuccess)
       return fail(GDN_ERR_CUDA, "prefill: cannot reserve shared memory");
     attr_set[dev.id].store(true, std::memory_order_release);
   }
@@ -1505,33 +1638,33 @@ gdn_status launch_prefill_tc(const LayerArgs &A, void *ws, cudaStream_t stream) 
   // and chains in one grid, so that the chains start while late chunks are
   // still being prepared; the chains are that grid's critical path and the
   // units form their own gates. Otherwise two kernels, and the front kernel
-  // forms the gates (the chunk pass is the critical path there).
+  // forms the gates (the chunk pass is the critical path there). Every kernel
+  // starts early (programmatic dependent launch) and waits for its
+  // predecessor inside the kernel.
   const int n_units = S * A.nv, grid = n_units < dev.sms ? n_units : dev.sms;
   const bool merged = !packed && 2 * A.B * A.nv <= grid;
   if (launch_pdl(merged ? tc::front_kernel<false> : tc::front_kernel<true>, dim3(S, 2 * A.nk + A.nv), dim3(256), 0,
                  stream, A, R, Ttot, W) != cudaSuccess)
     return check_launch("prefill front");
-  // every kernel starts early (programmatic dependent launch) and waits for
-  // its predecessor inside the kernel
-  CUtensorMap omap, zmap;
-  if (gdn_status st = tc::encode_rows_map(&omap, A.out, Ttot, A.nv * tc::HD, tc::CH / 2)) return st;
-  if (gdn_status st = tc::encode_rows_map(&zmap, A.z, Ttot, A.nv * tc::HD, tc::CH)) return st;
   if (merged) {
-    if (launch_pdl(tc::chunk_state_kernel, dim3(grid), dim3(256), tc::kChunkSmem, stream, A, R, Ttot, W) !=
+    CUtensorMap omap, zmap;
+    if (gdn_status st = tc::encode_rows_map(&omap, A.out, Ttot, A.nv * tc::HD, tc::CH / 2)) return st;
+    if (gdn_status st = tc::encode_rows_map(&zmap, A.z, Ttot, A.nv * tc::HD, tc::CH)) return st;
+    if (launch_pdl(tc::chunk_state_kernel, dim3(grid), dim3(256), tc::kMergedSmem, stream, A, R, Ttot, W) !=
         cudaSuccess)
       return check_launch("prefill chunk+state");
-  } else {
-    if (launch_pdl(tc::chunk_kernel, dim3(grid), dim3(256), tc::kChunkSmem, stream, A, R, Ttot, W, n_units) !=
+    if (launch_pdl(tc::output_kernel, dim3(S, A.nv), dim3(256), tc::kOutSmem, stream, A, R, Ttot, W, omap, zmap) !=
         cudaSuccess)
-      return check_launch("prefill chunk");
-    if (launch_pdl(tc::state_kernel, dim3(A.B * A.nv), dim3(256), tc::kStateSmem, stream, A, R, Ttot, W) !=
-        cudaSuccess)
-      return check_launch("prefill state");
-  }
-  if (launch_pdl(tc::output_kernel, dim3(S, A.nv), dim3(256), tc::kOutSmem, stream, A, R, Ttot, W, omap, zmap,
-                 merged ? 0 : 1) != cudaSuccess)
+      return check_launch("prefill output");
     return check_launch("prefill output");
-  return check_launch("prefill output");
+  }
+  if (launch_pdl(tc::chunk_kernel, dim3(grid), dim3(256), tc::kChunkSmem, stream, A, R, Ttot, W, n_units) !=
+      cudaSuccess)
+    return check_launch("prefill chunk");
+  if (launch_pdl(tc::state_kernel, dim3(A.B * A.nv), dim3(256), tc::kStateSmem, stream, A, R, Ttot, W) !=
+      cudaSuccess)
+    return check_launch("prefill state");
+  return check_launch("prefill state");
 }
 
 }  // namespace gdn

@@ -41,10 +41,13 @@
  *     not written). gdn_check_status() reports and clears it.
  *   - Every wait inside a kernel is bounded; one that runs out records
  *     GDN_ERR_TIMEOUT (the GPU stalled far beyond any normal latency). In a
- *     prefill call a (row, value head) whose chain stopped keeps its state, the
- *     value channels of its conv tail and its outputs, while the row's other
- *     heads complete; the q / k channels of the tail are written by the first
- *     value head of each key head's group. In decode and verify a timeout may
+ *     prefill call a (row, value head) whose chain stopped keeps its state and
+ *     the value channels of its conv tail, while the row's other heads
+ *     complete; the q / k channels of the tail are written by the first value
+ *     head of each key head's group. Its outputs stay as they were when the
+ *     call has few chains (dense rows, B * nv at most half the SM count, head
+ *     size 128), else they are written for the chunks before the one where it
+ *     stopped. In decode and verify a timeout may
  *     leave the rows of the stalled CTA partly written: treat the call as
  *     failed and restore those rows (for example from verify checkpoints).
  *   - Rows of one decode or prefill call must name distinct state slots (they
