@@ -409,8 +409,9 @@ constexpr int kOffKQL = 32768;   // the same, lo parts
 constexpr int kOffB2H = 65536;   // V image [2 kb][64 rows][128 B] (hi), then the lo parts at +16 KiB;
                                  // at the end the U | O_local staging (64 KiB)
 constexpr int kOffAF = 131072;   // fp32 [64][kLD]: A, then T in place; later the [T; R] image (hi)
-constexpr int kLD = 65;          // padded row stride: column-wise accesses hit distinct banks
-                                 // (the 256 bytes past 16 KiB overlap the [T; R] lo image, unused until then)
+constexpr int kLD = 68;          // padded row stride: 16-byte aligned rows, and a 16-byte chunk of rows
+                                 // i .. i+7 in eight different bank groups (the 1 KiB past 16 KiB
+                                 // overlaps the [T; R] lo image, unused until then)
 constexpr int kOffTRL = 147456;  // [T; R] image (lo)
 constexpr int kOffPTH = 163840;  // [128 rows][128 B]: P rows 0-63 | T^T rows 64-127 (hi)
 constexpr int kOffPTL = 180224;  // the same, lo parts
@@ -585,8 +586,9 @@ __device__ __forceinline__ bool chunk_unit(unsigned char *sm, const LayerArgs &A
         y[e] = arow ? (j < i ? bi * v[e] * gam : 0.0f) : (j <= i ? v[e] * gam : 0.0f);
       }
       if (arow) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) AF[i * kLD + 32 * hh + 8 * g8 + e] = y[e];
+        float4 *dst = reinterpret_cast<float4 *>(AF + i * kLD + 32 * hh + 8 * g8);
+        dst[0] = make_float4(y[0], y[1], y[2], y[3]);
+        dst[1] = make_float4(y[4], y[5], y[6], y[7]);
       } else {
         store_split8(PTH, PTL, sw128_chunk(128, i, 4 * hh + g8), y);
       }
@@ -599,7 +601,9 @@ __device__ __forceinline__ bool chunk_unit(unsigned char *sm, const LayerArgs &A
   //      inv([[X, 0], [Y, Z]]) = [[X^-1, 0], [-Z^-1 Y X^-1, Z^-1]]:
   //      the four diagonal 16x16 blocks by forward substitution, then the two
   //      16x16 off-diagonal blocks of the 32x32 diagonal blocks, then the
-  //      lower-left 32x32 block. Each product runs over all 256 threads.
+  //      lower-left 32x32 block. The off-diagonal products run on two / four
+  //      warps, each thread accumulating a register block of the result from
+  //      16-byte loads (few shared-memory loads per FMA); the other warps wait.
   float t16[16];  // T row i = tid / 4, columns 16 (tid % 4) .. +15 (kept for the second image)
   {
     if (tid < 64) {
@@ -619,53 +623,106 @@ __device__ __forceinline__ bool chunk_unit(unsigned char *sm, const LayerArgs &A
       for (int rr = 0; rr < 16; ++rr) Tb[rr * kLD + cc] = x[rr];
     }
     __syncthreads();
-    {
-      // level 1: blocks (1,0) and (3,2): X = A_rc T_cc, then T_rc = -T_rr X
-      const int pr = tid >> 7, rem = tid & 127, rr = rem >> 3, m0 = (rem & 7) * 2;
+    if (tid < 64) {
+      // level 1: blocks (1,0) and (3,2), one warp each: X = A_rc T_cc, then
+      // T_rc = -T_rr X; thread = a 4x2 block (rows 4bi.., columns 2bm..)
+      const int pr = tid >> 5, bi = (tid >> 3) & 3, bm = tid & 7;
       const int r0 = 16 + 32 * pr, c0 = 32 * pr;
-      float x0 = 0.0f, x1 = 0.0f;
+      float x[4][2];
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const float a = AF[(r0 + rr) * kLD + c0 + k];
-        x0 = fmaf(a, AF[(c0 + k) * kLD + c0 + m0], x0);
-        x1 = fmaf(a, AF[(c0 + k) * kLD + c0 + m0 + 1], x1);
-      }
-      SCR[pr * 256 + rr * 16 + m0] = x0;
-      SCR[pr * 256 + rr * 16 + m0 + 1] = x1;
-      __syncthreads();
-      float y0 = 0.0f, y1 = 0.0f;
+      for (int j = 0; j < 4; ++j) x[j][0] = x[j][1] = 0.0f;
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const float t = AF[(r0 + rr) * kLD + r0 + k];
-        y0 = fmaf(t, SCR[pr * 256 + k * 16 + m0], y0);
-        y1 = fmaf(t, SCR[pr * 256 + k * 16 + m0 + 1], y1);
+      for (int k4 = 0; k4 < 4; ++k4) {
+        float4 a[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) a[j] = *reinterpret_cast<const float4 *>(AF + (r0 + 4 * bi + j) * kLD + c0 + 4 * k4);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const float2 t = *reinterpret_cast<const float2 *>(AF + (c0 + 4 * k4 + kk) * kLD + c0 + 2 * bm);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float av = kk == 0 ? a[j].x : kk == 1 ? a[j].y : kk == 2 ? a[j].z : a[j].w;
+            x[j][0] = fmaf(av, t.x, x[j][0]);
+            x[j][1] = fmaf(av, t.y, x[j][1]);
+          }
+        }
       }
-      AF[(r0 + rr) * kLD + c0 + m0] = -y0;
-      AF[(r0 + rr) * kLD + c0 + m0 + 1] = -y1;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<float2 *>(SCR + pr * 256 + (4 * bi + j) * 16 + 2 * bm) = make_float2(x[j][0], x[j][1]);
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < 4; ++j) x[j][0] = x[j][1] = 0.0f;
+#pragma unroll
+      for (int k4 = 0; k4 < 4; ++k4) {
+        float4 t[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) t[j] = *reinterpret_cast<const float4 *>(AF + (r0 + 4 * bi + j) * kLD + r0 + 4 * k4);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const float2 xk = *reinterpret_cast<const float2 *>(SCR + pr * 256 + (4 * k4 + kk) * 16 + 2 * bm);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float tv = kk == 0 ? t[j].x : kk == 1 ? t[j].y : kk == 2 ? t[j].z : t[j].w;
+            x[j][0] = fmaf(tv, xk.x, x[j][0]);
+            x[j][1] = fmaf(tv, xk.y, x[j][1]);
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<float2 *>(AF + (r0 + 4 * bi + j) * kLD + c0 + 2 * bm) = make_float2(-x[j][0], -x[j][1]);
     }
     __syncthreads();
-    {
-      // level 2: block rows 32-63, columns 0-31: Y = A_BA T_A, then T_BA = -T_B Y
-      const int r = tid >> 3, m0 = (tid & 7) * 4;
-      float y[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (tid < 128) {
+      // level 2: block rows 32-63, columns 0-31: Y = A_BA T_A, then T_BA = -T_B Y;
+      // thread = a 4x2 block (rows 4bi.., columns 2bm..) of each 32x32 product
+      const int bi = tid >> 4, bm = tid & 15;
+      float y[4][2];
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        const float a = AF[(32 + r) * kLD + k];
+      for (int j = 0; j < 4; ++j) y[j][0] = y[j][1] = 0.0f;
+#pragma unroll 2
+      for (int k4 = 0; k4 < 8; ++k4) {
+        float4 a[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) y[e] = fmaf(a, AF[k * kLD + m0 + e], y[e]);
+        for (int j = 0; j < 4; ++j) a[j] = *reinterpret_cast<const float4 *>(AF + (32 + 4 * bi + j) * kLD + 4 * k4);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const float2 t = *reinterpret_cast<const float2 *>(AF + (4 * k4 + kk) * kLD + 2 * bm);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float av = kk == 0 ? a[j].x : kk == 1 ? a[j].y : kk == 2 ? a[j].z : a[j].w;
+            y[j][0] = fmaf(av, t.x, y[j][0]);
+            y[j][1] = fmaf(av, t.y, y[j][1]);
+          }
+        }
       }
 #pragma unroll
-      for (int e = 0; e < 4; ++e) SCR[r * 32 + m0 + e] = y[e];
-      __syncthreads();
-      float z[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<float2 *>(SCR + (4 * bi + j) * 32 + 2 * bm) = make_float2(y[j][0], y[j][1]);
+      named_sync(5, 128);  // Y complete; A_BA is read
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        const float t = AF[(32 + r) * kLD + 32 + k];
+      for (int j = 0; j < 4; ++j) y[j][0] = y[j][1] = 0.0f;
+#pragma unroll 2
+      for (int k4 = 0; k4 < 8; ++k4) {
+        float4 t[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) z[e] = fmaf(t, SCR[k * 32 + m0 + e], z[e]);
+        for (int j = 0; j < 4; ++j)
+          t[j] = *reinterpret_cast<const float4 *>(AF + (32 + 4 * bi + j) * kLD + 32 + 4 * k4);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const float2 yk = *reinterpret_cast<const float2 *>(SCR + (4 * k4 + kk) * 32 + 2 * bm);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float tv = kk == 0 ? t[j].x : kk == 1 ? t[j].y : kk == 2 ? t[j].z : t[j].w;
+            y[j][0] = fmaf(tv, yk.x, y[j][0]);
+            y[j][1] = fmaf(tv, yk.y, y[j][1]);
+          }
+        }
       }
 #pragma unroll
-      for (int e = 0; e < 4; ++e) AF[(32 + r) * kLD + m0 + e] = -z[e];
+      for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<float2 *>(AF + (32 + 4 * bi + j) * kLD + 2 * bm) = make_float2(-y[j][0], -y[j][1]);
     }
     __syncthreads();
     // T (fp32, in AF) -> rows 0-63 of the split image [T; R] diag(beta gamma)
@@ -673,7 +730,13 @@ __device__ __forceinline__ bool chunk_unit(unsigned char *sm, const LayerArgs &A
     // row j = column j of T, gathered by column)
     const int i = tid >> 2, q4 = tid & 3;
 #pragma unroll
-    for (int k = 0; k < 16; ++k) t16[k] = AF[i * kLD + 16 * q4 + k];
+    for (int c4 = 0; c4 < 4; ++c4) {
+      const float4 t4 = *reinterpret_cast<const float4 *>(AF + i * kLD + 16 * q4 + 4 * c4);
+      t16[4 * c4] = t4.x;
+      t16[4 * c4 + 1] = t4.y;
+      t16[4 * c4 + 2] = t4.z;
+      t16[4 * c4 + 3] = t4.w;
+    }
     const int jc = tid & 63, ip = tid >> 6;  // T^T row jc, tokens 16 ip .. +15
     float tc16[16];
 #pragma unroll
@@ -861,8 +924,16 @@ __global__ void __launch_bounds__(256, 1) chunk_kernel(LayerArgs A, Rows R, int 
   int parity = 0;
   bool kq = false;
   while (cur.x >= 0) {
+    // thread 0: the (row, chunk) of the next candidate unit's slot, requested
+    // now (packed rows: a load through L2) and used once the unit's first
+    // product is issued
+    const int cand = cur.x + (int)gridDim.x;
+    int2 cand_rc = make_int2(-1, 0);
+    if (threadIdx.x == 0 && R.cu && cand < n_units) cand_rc = __ldcg(W.slot_rc + cand / A.nv);
     auto find_next = [&]() {  // thread 0, during the unit: published for the CTA in s_next
-      const int3 n = first_unit(cur.x + gridDim.x);
+      int3 n;
+      if (R.cu && cand < n_units && cand_rc.x >= 0) n = make_int3(cand, cand_rc.x, cand_rc.y);
+      else n = first_unit(cand);
       s_next = n;
       return make_int2(n.x < 0 ? -1 : n.x / A.nv, n.x < 0 ? 0 : n.x % A.nv);
     };
