@@ -1174,14 +1174,12 @@ __device__ __forceinline__ bool state_chain(unsigned char *sm, uint64_t *bars, c
     return seen;
   };
   if (wait_units && tid == 0 && n_chunks > 0) {  // same grid: the first chunks' loads before the state's
-    const int seen = scan_published(0);
-    if (seen >= 0) {  // one acquire for every unit published so far
+    issue_when_ready(0, true);  // chunk 0 alone first (one acquire of its flag), then the units after it
+    const int seen = n_chunks > 1 && !gave_up ? scan_published(1) : 0;
+    if (seen >= 1) {  // one acquire for every unit published so far
       fence_acq_rel_gpu();
       fence_proxy_async_global();
       acquired = seen;
-    }
-    issue_when_ready(0, true);
-    if (n_chunks > 1 && acquired >= 1) {
       issue_loads(1);
       issued = 1;
     }
