@@ -577,12 +577,16 @@ __device__ __forceinline__ bool chunk_unit(unsigned char *sm, const LayerArgs &A
     const float Gi = sG[i], bi = sb[i];
 #pragma unroll 1
     for (int g8 = 0; g8 < 4; ++g8) {
+      // G_j of the 8 columns first: their load overlaps the TMEM load's
+      const float4 ga = *reinterpret_cast<const float4 *>(sG + 32 * hh + 8 * g8);
+      const float4 gb = *reinterpret_cast<const float4 *>(sG + 32 * hh + 8 * g8 + 4);
+      const float Gj[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
       float v[8], y[8];
       tmem_ld8(tmem_at(tmem, q, 32 * hh + 8 * g8), v);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const int j = 32 * hh + 8 * g8 + e;
-        const float gam = __expf(Gi - sG[j]);
+        const float gam = __expf(Gi - Gj[e]);
         y[e] = arow ? (j < i ? bi * v[e] * gam : 0.0f) : (j <= i ? v[e] * gam : 0.0f);
       }
       if (arow) {
@@ -777,14 +781,20 @@ __device__ __forceinline__ bool chunk_unit(unsigned char *sm, const LayerArgs &A
     const int q = warp & 3, hh = warp >> 2, i = 32 * q + lane;
 #pragma unroll 1
     for (int g8 = 0; g8 < 4; ++g8) {
-      float v[8], y[8];
-      tmem_ld8(tmem_at(tmem, q, 32 * hh + 8 * g8), v);
       const int j0 = 32 * hh + 8 * g8;
+      // beta_j and gamma_j first: their loads overlap the TMEM load's
+      const float4 b0 = *reinterpret_cast<const float4 *>(sb + j0), b1 = *reinterpret_cast<const float4 *>(sb + j0 + 4);
+      const float4 m0 = *reinterpret_cast<const float4 *>(sgam + j0);
+      const float4 m1 = *reinterpret_cast<const float4 *>(sgam + j0 + 4);
+      const float bj[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+      const float mj[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+      float v[8], y[8];
+      tmem_ld8(tmem_at(tmem, q, j0), v);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) y[e] = v[e] * (sb[j0 + e] * sgam[j0 + e]);
+      for (int e = 0; e < 8; ++e) y[e] = v[e] * (bj[e] * mj[e]);
       store_split8(TRH, TRL, sw128_chunk(128, CH + i, 4 * hh + g8), y);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) y[e] = v[e] * sb[j0 + e];
+      for (int e = 0; e < 8; ++e) y[e] = v[e] * bj[e];
       store_split8(PTH, PTL, sw128_chunk(128, CH + i, 4 * hh + g8), y);
     }
   }
@@ -822,6 +832,17 @@ __device__ __forceinline__ bool chunk_unit(unsigned char *sm, const LayerArgs &A
     uint4 *stage_u = reinterpret_cast<uint4 *>(sm + kOffB2H) + (size_t)i * 16;          // U row i
 #pragma unroll 1
     for (int cb = 0; cb < 4; ++cb) {
+      // Q' rows: this block's Q (hi, lo) first, every read before the first
+      // store and overlapping the TMEM load
+      uint4 qhv[4], qlv[4];
+      if (hh == 0 && upper) {
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          const uint32_t off = sw128_chunk(128, row, 4 * cb + c4);
+          qhv[c4] = *reinterpret_cast<const uint4 *>(KQH + off);
+          qlv[c4] = *reinterpret_cast<const uint4 *>(KQL + off);
+        }
+      }
       float v[32];
       tmem_ld32(tmem_at(tmem, q, 128 * hh + 32 * cb), v);
       if (hh == 0) {
@@ -831,7 +852,7 @@ __device__ __forceinline__ bool chunk_unit(unsigned char *sm, const LayerArgs &A
           uint4 *dst = reinterpret_cast<uint4 *>(KQH + off);
           float y[8];
           if (upper) {
-            const uint4 qh = *dst, ql = *reinterpret_cast<const uint4 *>(KQL + off);
+            const uint4 qh = qhv[c4], ql = qlv[c4];
             const uint32_t hs[4] = {qh.x, qh.y, qh.z, qh.w}, ls[4] = {ql.x, ql.y, ql.z, ql.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
