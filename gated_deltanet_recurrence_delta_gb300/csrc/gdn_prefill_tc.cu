@@ -745,10 +745,20 @@ __device__ __forceinline__ bool chunk_unit(unsigned char *sm, const LayerArgs &A
     float tc16[16];
 #pragma unroll
     for (int k = 0; k < 16; ++k) tc16[k] = AF[(16 * ip + k) * kLD + jc];
+    float bg16[16];  // beta_j gamma_j of this thread's 16 columns
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) {
+      const float4 b4 = *reinterpret_cast<const float4 *>(sb + 16 * q4 + 4 * c4);
+      const float4 g4 = *reinterpret_cast<const float4 *>(sgam + 16 * q4 + 4 * c4);
+      bg16[4 * c4] = b4.x * g4.x;
+      bg16[4 * c4 + 1] = b4.y * g4.y;
+      bg16[4 * c4 + 2] = b4.z * g4.z;
+      bg16[4 * c4 + 3] = b4.w * g4.w;
+    }
     __syncthreads();
     float y16[16];
 #pragma unroll
-    for (int k = 0; k < 16; ++k) y16[k] = t16[k] * (sb[16 * q4 + k] * sgam[16 * q4 + k]);
+    for (int k = 0; k < 16; ++k) y16[k] = t16[k] * bg16[k];
 #pragma unroll
     for (int c2 = 0; c2 < 2; ++c2) store_split8(TRH, TRL, sw128_chunk(128, i, 2 * q4 + c2), y16 + 8 * c2);
 #pragma unroll
