@@ -1002,17 +1002,18 @@ constexpr int kSOffKT = 98304;    // 2 x K image (hi) [2 kb][64 rows][128 B] (16
 constexpr int kSOffUT = 131072;   // 2 x U fp16 [64 tokens][128 v] (16 KiB each)
 constexpr int kSOffOL = 163840;   // O_local fp32 [64 tokens][128 v] (32 KiB; one chunk at a time)
 constexpr int kSOffUP = 196608;   // U'^T image [128 rows][128 B] (16 KiB)
-constexpr int kSOffSec = 212992;  // 2 x the exp(G_C - G_j) | gamma_C record, fp32 [68]
-constexpr int kSOffBar = kSOffSec + 2 * kSecRec * 4;  // the chain's barriers (4), TMEM base
-constexpr int kStateSmem = kSOffBar + 64 + 1024;
+constexpr int kSOffZ = 212992;    // z bf16 [64 tokens][128 v] of the chunk whose outputs are formed (16 KiB)
+constexpr int kSOffSec = 229376;  // 2 x the exp(G_C - G_j) | gamma_C record, fp32 [68]
+constexpr int kSOffBar = kSOffSec + 2 * kSecRec * 4;  // the chain's barriers (5), TMEM base
+constexpr int kStateSmem = kSOffBar + 128 + 1024;
 // The outputs of a chunk are formed in buffers free at that time: o (fp32
 // [64 tokens][128 v], the O_local layout) in the state image, which the first
 // product has read and the step rewrites at its end; the RMS partials (fp32
 // [4][64], then [64] rstd) in the chunk's U buffer, consumed before them, whose
 // next loads are requested after they are read.
 // chunk + state in one grid: the units' layout below kOffBar, the chain's above; barriers past both
-constexpr int kMOffBar = kSOffBar > kOffBar ? kSOffBar : kOffBar;  // [0..2] units, [3..6] the chain, TMEM base
-constexpr int kMergedSmem = kMOffBar + 64 + 1024;
+constexpr int kMOffBar = kSOffBar > kOffBar ? kSOffBar : kOffBar;  // [0..2] units, [3..7] the chain, TMEM base
+constexpr int kMergedSmem = kMOffBar + 128 + 1024;
 static_assert(kStateSmem + 1024 <= 232448 && kMergedSmem + 1024 <= 232448,
               "shared memory of one CTA (with room for the static shared variables)");
 
@@ -1128,7 +1129,8 @@ __device__ __forceinline__ void chain_finish(const LayerArgs &A, const Rows &R, 
 
 // The sequential pass of one (row b, value head h) chain, after its
 // chain_prologue accepted the row. bars: the chain's barriers (two loads, the
-// products, O_local). The caller holds 256 TMEM columns at `tmem` and has
+// products, O_local, z). zmap (with OUT): z viewed as [tokens][nv*dv] bf16,
+// box [64 tokens][128]. The caller holds 256 TMEM columns at `tmem` and has
 // synchronised the CTA since any earlier use of shared memory or TMEM.
 // OUT: the chain forms the chunks' outputs (else it copies out the state image
 // at every chunk start, for the output kernel). wait_units: the chunk units run
@@ -1137,8 +1139,9 @@ __device__ __forceinline__ void chain_finish(const LayerArgs &A, const Rows &R, 
 // written).
 template <bool OUT>
 __device__ __forceinline__ bool state_chain(unsigned char *sm, uint64_t *bars, const LayerArgs &A, const Rows &R,
-                                            const Ws &W, int b, int h, int Lr, uint32_t tmem, bool wait_units) {
-  uint64_t *bar_ld = bars, *bar_mma = bars + 2, *bar_ol = bars + 3;
+                                            const Ws &W, int b, int h, int Lr, uint32_t tmem, bool wait_units,
+                                            const CUtensorMap *zmap) {
+  uint64_t *bar_ld = bars, *bar_mma = bars + 2, *bar_ol = bars + 3, *bar_z = bars + 4;
   unsigned char *SI = sm + kSOffS;
   unsigned char *UP = sm + kSOffUP;
   float *OL = reinterpret_cast<float *>(sm + kSOffOL);
@@ -1245,18 +1248,13 @@ __device__ __forceinline__ bool state_chain(unsigned char *sm, uint64_t *bars, c
   float wn[8];  // the RMSNorm weights of those values
 #pragma unroll
   for (int e = 0; e < 8; ++e) wn[e] = OUT ? ldbf(A.norm_w + 8 * oc + e) : 0.0f;
-  // z at those places (16-byte loads), for the chunk ahead of the outputs
-  uint4 z8[4];
+  // thread 0: chunk ci's z tile (rows past the tensor read as zeros), once
+  // chunk ci - 1's outputs have read theirs
   auto load_z = [&](int ci) {
-    const int zreal = min(CH, Lr - ci * CH);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int i = orow + 8 * k;
-      z8[k] = i < zreal ? __ldg(reinterpret_cast<const uint4 *>(A.z + ((size_t)(start + ci * CH + i) * A.nv + h) * HD) + oc)
-                        : make_uint4(0u, 0u, 0u, 0u);
-    }
+    mbar_arrive_expect_tx(bar_z, 16384);
+    tma_load_2d(sm + kSOffZ, zmap, h * HD, start + ci * CH, bar_z);
   };
-  if (OUT && n_chunks > 0) load_z(0);
+  if (OUT && tid == 0 && n_chunks > 0) load_z(0);
 
   bool ok = true;
   for (int ci = 0; ci < n_chunks; ++ci) {
@@ -1328,7 +1326,7 @@ __device__ __forceinline__ bool state_chain(unsigned char *sm, uint64_t *bars, c
     // ---- the chunk's outputs while dS forms: O = O_S + O_local (value row v =
     //      TMEM lane, tokens 32hh .. 32hh+31 = TMEM columns 64 + 32hh ..), then
     //      the gated RMSNorm over the 128 value rows of each token
-    if (OUT && !cta_wait(bar_ol, (uint32_t)(ci & 1), A.status)) {
+    if (OUT && (!cta_wait(bar_ol, (uint32_t)(ci & 1), A.status) || !cta_wait(bar_z, (uint32_t)(ci & 1), A.status))) {
       ok = false;
       break;
     }
@@ -1386,7 +1384,7 @@ __device__ __forceinline__ bool state_chain(unsigned char *sm, uint64_t *bars, c
             const float4 ob = *reinterpret_cast<const float4 *>(OS + i * HD + (((2 * oc + 1) ^ (i & 7)) << 2));
             const float rs = rstd[i];
             const float ov[8] = {oa.x, oa.y, oa.z, oa.w, ob.x, ob.y, ob.z, ob.w};
-            const uint4 zk = z8[k];
+            const uint4 zk = *reinterpret_cast<const uint4 *>(sm + kSOffZ + (size_t)(i * HD + 8 * oc) * 2);
             const uint32_t zw[4] = {zk.x, zk.y, zk.z, zk.w};
             uint32_t pw[4];
 #pragma unroll
@@ -1402,13 +1400,13 @@ __device__ __forceinline__ bool state_chain(unsigned char *sm, uint64_t *bars, c
           reinterpret_cast<uint4 *>(A.out + ((size_t)(start + t0 + i) * A.nv + h) * HD)[oc] = res;
         }
       }
-      if (ci + 1 < n_chunks) load_z(ci + 1);
     }
     if (!cta_wait(bar_mma, 1, A.status)) {
       ok = false;
       break;
     }
     tc_fence_after();
+    if (OUT && tid == 0 && ci + 1 < n_chunks) load_z(ci + 1);  // every thread has read this chunk's z
     // S = gamma_C S + dS
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
@@ -1442,14 +1440,15 @@ __device__ __forceinline__ bool state_chain(unsigned char *sm, uint64_t *bars, c
   return true;
 }
 
-__global__ void __launch_bounds__(256, 1) state_kernel(LayerArgs A, Rows R, int Ttot, Ws W) {
+__global__ void __launch_bounds__(256, 1) state_kernel(LayerArgs A, Rows R, int Ttot, Ws W,
+                                                       const __grid_constant__ CUtensorMap zmap) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   unsigned char *sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   uint64_t *bar = reinterpret_cast<uint64_t *>(sm + kSOffBar);
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 4);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 5);
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 4; ++i) mbar_init(&bar[i], 1);
+    for (int i = 0; i < 5; ++i) mbar_init(&bar[i], 1);
     fence_mbar_init();
   }
   if (threadIdx.x < 32) tmem_alloc(tmem_slot, 256);
@@ -1460,7 +1459,7 @@ __global__ void __launch_bounds__(256, 1) state_kernel(LayerArgs A, Rows R, int 
   const int b = blockIdx.x / A.nv, h = blockIdx.x % A.nv;
   int Lr = 0;
   if (chain_prologue(A, R, Ttot, W, b, h, false, Lr))
-    chain_finish(A, R, W, b, h, Lr, state_chain<true>(sm, bar, A, R, W, b, h, Lr, tmem, false));
+    chain_finish(A, R, W, b, h, Lr, state_chain<true>(sm, bar, A, R, W, b, h, Lr, tmem, false, &zmap));
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x < 32) tmem_dealloc(tmem, 256);
@@ -1481,9 +1480,9 @@ __global__ void __launch_bounds__(256, 1) chunk_state_kernel(LayerArgs A, Rows R
   const uint32_t raw = smem_u32(smem_raw);
   unsigned char *sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   uint64_t *bar = reinterpret_cast<uint64_t *>(sm + kMOffBar);  // [0..2] units, [3..6] the chain
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 7);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 8);
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 7; ++i) mbar_init(&bar[i], 1);
+    for (int i = 0; i < 8; ++i) mbar_init(&bar[i], 1);
     fence_mbar_init();
   }
   if (threadIdx.x < 32) tmem_alloc(tmem_slot, 256);
@@ -1516,7 +1515,7 @@ __global__ void __launch_bounds__(256, 1) chunk_state_kernel(LayerArgs A, Rows R
   griddep_trigger();
   if (chain)
     chain_finish(A, R, W, j / A.nv, j % A.nv, Lr,
-                 ok && state_chain<false>(sm, bar + 3, A, R, W, j / A.nv, j % A.nv, Lr, tmem, true));
+                 ok && state_chain<false>(sm, bar + 3, A, R, W, j / A.nv, j % A.nv, Lr, tmem, true, nullptr));
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x < 32) tmem_dealloc(tmem, 256);
@@ -1761,7 +1760,9 @@ gdn_status launch_prefill_tc(const LayerArgs &A, void *ws, cudaStream_t stream) 
   if (launch_pdl(tc::chunk_kernel, dim3(grid), dim3(256), tc::kChunkSmem, stream, A, R, Ttot, W, n_units) !=
       cudaSuccess)
     return check_launch("prefill chunk");
-  if (launch_pdl(tc::state_kernel, dim3(A.B * A.nv), dim3(256), tc::kStateSmem, stream, A, R, Ttot, W) !=
+  CUtensorMap zmap;
+  if (gdn_status st = tc::encode_rows_map(&zmap, A.z, Ttot, A.nv * tc::HD, tc::CH)) return st;
+  if (launch_pdl(tc::state_kernel, dim3(A.B * A.nv), dim3(256), tc::kStateSmem, stream, A, R, Ttot, W, zmap) !=
       cudaSuccess)
     return check_launch("prefill state");
   return check_launch("prefill state");
