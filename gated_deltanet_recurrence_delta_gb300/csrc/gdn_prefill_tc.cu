@@ -224,9 +224,10 @@ __device__ __forceinline__ void named_sync(int id, int n) {
 // ------------------------------------------------------------ split fp16
 
 __device__ __forceinline__ void split2(float a, float b, uint32_t &hi, uint32_t &lo) {
-  const __half ha = __float2half_rn(a), hb = __float2half_rn(b);
-  const __half la = __float2half_rn(a - __half2float(ha)), lb = __float2half_rn(b - __half2float(hb));
-  const __half2 h2 = __halves2half2(ha, hb), l2 = __halves2half2(la, lb);
+  // paired conversions (each half rounded to nearest, as one at a time would be)
+  const __half2 h2 = __floats2half2_rn(a, b);
+  const float2 hf = __half22float2(h2);
+  const __half2 l2 = __floats2half2_rn(a - hf.x, b - hf.y);
   hi = *reinterpret_cast<const uint32_t *>(&h2);
   lo = *reinterpret_cast<const uint32_t *>(&l2);
 }
