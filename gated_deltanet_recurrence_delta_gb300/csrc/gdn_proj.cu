@@ -168,8 +168,9 @@ __global__ void __launch_bounds__(128, 1) gemm_kernel(const __grid_constant__ CU
   if (!ok && tid == 0) set_status(status, GDN_ERR_TIMEOUT);
   tc_fence_after();
   if (SPLIT > 1) {
-    // every CTA parks its partial tile [feature][token] (rows padded to BN + 1
-    // floats: conflict-free by rows and by columns) in its own stage ring
+    // every CTA parks its partial tile [token][feature] (feature-contiguous: a
+    // warp's accesses to one token column are one 128-byte line, locally and
+    // across the cluster) in its own stage ring
     float *part = reinterpret_cast<float *>(sm);
     const int row = 32 * warp + lane;
 #pragma unroll 1
@@ -177,7 +178,7 @@ __global__ void __launch_bounds__(128, 1) gemm_kernel(const __grid_constant__ CU
       float v[32];
       tmem_ld32(tmem_at(tmem, warp, 32 * c), v);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) part[row * (BN + 1) + 32 * c + e] = (ok && !s_abort) ? v[e] : 0.0f;
+      for (int e = 0; e < 32; ++e) part[(32 * c + e) * BM + row] = (ok && !s_abort) ? v[e] : 0.0f;
     }
     cluster_sync_all();  // every CTA's partial tile is in place
     const int f = f0 + row;
@@ -193,7 +194,7 @@ __global__ void __launch_bounds__(128, 1) gemm_kernel(const __grid_constant__ CU
     if (dst && ok && !s_abort) {
       uint32_t base[SPLIT];
 #pragma unroll
-      for (int p = 0; p < SPLIT; ++p) base[p] = cluster_addr(part + row * (BN + 1) + (int)rank * CW, (uint32_t)p);
+      for (int p = 0; p < SPLIT; ++p) base[p] = cluster_addr(part + (int)rank * CW * BM + row, (uint32_t)p);
       constexpr int G = 8;  // columns whose SPLIT loads are in flight together
       static_assert(CW % G == 0, "column groups");
 #pragma unroll 1
@@ -202,7 +203,7 @@ __global__ void __launch_bounds__(128, 1) gemm_kernel(const __grid_constant__ CU
 #pragma unroll
         for (int j = 0; j < G; ++j)
 #pragma unroll
-          for (int p = 0; p < SPLIT; ++p) v[j][p] = ld_cluster_f32(base[p] + 4u * (uint32_t)(c0 + j));
+          for (int p = 0; p < SPLIT; ++p) v[j][p] = ld_cluster_f32(base[p] + 4u * (uint32_t)((c0 + j) * BM));
 #pragma unroll
         for (int j = 0; j < G; ++j) {
           float acc = 0.0f;
@@ -272,7 +273,7 @@ gdn_status encode_operand(CUtensorMap *map, const void *base, long long rows, lo
 
 template <int BN, int SPLIT>
 gdn_status launch_t(const void *w, const void *x, int Nout, int M, int K, const Epi &epi, cudaStream_t stream) {
-  static_assert(SPLIT == 1 || (BN + 1) * BM * 4 <= Smem<BN>::kBar, "the partial tile fits in the stage ring");
+  static_assert(SPLIT == 1 || BN * BM * 4 <= Smem<BN>::kBar, "the partial tile fits in the stage ring");
   const DeviceInfo &dev = device_info();
   static std::atomic<bool> attr_set[kMaxDevices];
   if (!attr_set[dev.id].load(std::memory_order_acquire)) {
