@@ -1208,17 +1208,9 @@ __device__ __forceinline__ bool state_chain(unsigned char *sm, uint64_t *bars, c
       if (f[e] && seen == from + e - 1) seen = from + e;
     return seen;
   };
-  if (wait_units && tid == 0 && n_chunks > 0) {  // same grid: the first chunks' loads before the state's
-    issue_when_ready(0, true);  // chunk 0 alone first (one acquire of its flag), then the units after it
-    const int seen = n_chunks > 1 && !gave_up ? scan_published(1) : 0;
-    if (seen >= 1) {  // one acquire for every unit published so far
-      fence_acq_rel_gpu();
-      fence_proxy_async_global();
-      acquired = seen;
-      issue_loads(1);
-      issued = 1;
-    }
-  }
+  // same grid: chunk 0's loads (one acquire of its flag) before the state's;
+  // the later units are scanned by the first step, after its first product
+  if (wait_units && tid == 0 && n_chunks > 0) issue_when_ready(0, true);
   // thread <-> (value row v = TMEM lane, key half / token half hh)
   const int q = warp & 3, hh = warp >> 2, v = 32 * q + lane;
   float Sv[64];
