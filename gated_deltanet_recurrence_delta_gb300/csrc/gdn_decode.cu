@@ -20,7 +20,6 @@
 //     behind the current unit's state stream; row slots are resolved once
 //     into a shared table.
 // The per-token arithmetic is the shared code of gdn_token.cuh.
-#include <cuda_fp8.h>
 
 #include "gdn_launch.h"
 #include "gdn_token.cuh"
@@ -65,12 +64,24 @@ struct UnitGeom {
   }
 };
 
-// One MXFP8 element: e4m3 (exact in half precision) times its block's scale
+// One MXFP8 element: e4m3 times its block's scale
 // 2^(s-127) (s = 0: 2^-127; s = 255: NaN, the format's NaN code). The product
 // is exact in fp32 and, inside bf16's normal range, in bf16, so the conv and
 // the saved conv tail see exactly the dequantized input.
+// e4m3 (OCP FP8): sign, 4 exponent bits (bias 7), 3 mantissa bits; exponent 0
+// holds the subnormals m * 2^-9; S.1111.111 is NaN (no infinities). Decoded
+// exactly into fp32 with integer operations.
+__device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
+  const uint32_t sgn = (b & 0x80u) << 24, ex = (b >> 3) & 15u, m = b & 7u;
+  float v;
+  if ((b & 0x7Fu) == 0x7Fu) v = __int_as_float(0x7fc00000);
+  else if (ex == 0u) v = (float)m * 0.001953125f;  // m * 2^-9, exact
+  else v = __uint_as_float(((ex + 120u) << 23) | (m << 20));
+  return __uint_as_float(__float_as_uint(v) | sgn);
+}
+
 __device__ __forceinline__ bf16 mx_dequant(uint8_t e, uint8_t s) {
-  const float f = __half2float(__half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)e, __NV_E4M3)));
+  const float f = e4m3_to_f32(e);
   const float scale = s == 255 ? __int_as_float(0x7fc00000) : (s == 0 ? __int_as_float(0x00400000)
                                                                        : __int_as_float((int)s << 23));
   return __float2bfloat16_rn(f * scale);
