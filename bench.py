@@ -68,7 +68,8 @@ KERNEL_SOURCES = {
     "state_copy_kernel": ("gdn_state_copy.cu",) + _COMMON_SOURCES,
     "decode_kernel_mxfp8": ("gdn_decode.cu", "gdn_token.cuh") + _COMMON_SOURCES,
     "commit_kernel": ("gdn_state_copy.cu",) + _COMMON_SOURCES,
-    **{k: ("gdn_proj.cu", "gdn_umma.cuh") + _COMMON_SOURCES for k in ("gemm_in_proj_prefill", "gemm_in_proj_decode")},
+    **{k: ("gdn_proj.cu", "gdn_umma.cuh") + _COMMON_SOURCES
+       for k in ("gemm_in_proj_prefill", "gemm_in_proj_decode", "gemm_out_proj_decode")},
     **{k: _PREFILL_SOURCES for k in ("front_kernel", "chunk_state_kernel", "output_kernel", "chunk_kernel",
                                      "state_kernel", "front_kernel_gates", "prefill_call_512", "varlen_layer")},
 }
@@ -497,8 +498,8 @@ def phase_proj(gdn, world, steps, warmup, peak_hbm, peak_tf):
             else:
                 roof = {"bound": "tensor", "achieved": flops / (ms * 1e-3) / 1e12, "peak": peak_tf, "unit": "TFLOP/s",
                         "frac": flops / (ms * 1e-3) / 1e12 / peak_tf, "algorithmic_flops": flops}
-            if name == "in_proj":
-                roof["traffic"] = dram_traffic(f"gemm_in_proj_{'decode' if M == 64 else 'prefill'}")
+            if name == "in_proj" or M == 64:
+                roof["traffic"] = dram_traffic(f"gemm_{name}_{'decode' if M == 64 else 'prefill'}")
                 roof["traffic_note"] = TRAFFIC_NOTE
             res[key] = {"tokens": M, "features": nout, "k": kk, "ms_per_call": ms, "tokens_per_s": M * world / (ms * 1e-3),
                         "roofline": roof}
