@@ -346,12 +346,6 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(LayerArgs A) {
         fz[e] = __bfloat162float(load_z<MX>(A, U, b, kh, e));
       float decay = 0.f, beta = 0.f;
       if (tid < G) gdn_gates(__bfloat162float(R.ga), __bfloat162float(R.gb), R.alog, R.dtb, decay, beta);
-      // next unit's inputs, in flight while this unit's heads stream
-      if (i + 1 < my_units) {
-        const int s1 = unit_slot(i + 1);
-        const int u1 = u + (int)gridDim.x;
-        if (s1 >= 0) load_front<MX>(R, A, U, u1 / A.nk, u1 % A.nk, s1, tid);
-      }
       csync();
       if (warp == 0) warp_l2norm<D>(fq, A.l2_eps, A.scale, lane);
       if (warp == 1) warp_l2norm<D>(fk, A.l2_eps, 1.0f, lane);
@@ -365,6 +359,14 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(LayerArgs A) {
         }
       }
       csync();
+      // next unit's inputs, in flight while this unit's heads stream: issued
+      // after this unit's front end, whose shared-memory work would otherwise
+      // queue behind the global loads and wait out their latency
+      if (i + 1 < my_units) {
+        const int s1 = unit_slot(i + 1);
+        const int u1 = u + (int)gridDim.x;
+        if (s1 >= 0) load_front<MX>(R, A, U, u1 / A.nk, u1 % A.nk, s1, tid);
+      }
     } else if (j == 0 && i + 1 < my_units) {
       // skipped unit: still prefetch the next one
       const int s1 = unit_slot(i + 1);
