@@ -216,3 +216,42 @@ def test_tensor_core_path_rejected_row(oracle_mod):
         assert_out(out[r:r + 1], ref["out"], f"row {r}")
         assert_state(S[r], ref["state"][0], f"row {r}")
         assert torch.equal(conv[r].cpu().double(), torch.from_numpy(ref["conv_state"][0]))
+
+
+def test_many_chains_rejected_and_padded_rows(oracle_mod):
+    """Head size 128, 40 rows x 4 value heads: 160 chains, so the chunk and
+    state passes run as separate kernels and the state pass forms the outputs
+    itself. A row whose mask is not ones then zeros is reported (GDN_ERR_MASK)
+    and skipped -- its state, conv tail and outputs are not written; a padded
+    row gets zeros after its real length; every other row matches the oracle."""
+    shape = I.Shape(nk=2, nv=4, dk=128, dv=128)
+    B, T = 40, 70
+    d = I.decode_batch(seed=95, B=B, shape=shape)
+    acts = I.activations(shape, B, T, torch.Generator().manual_seed(96))
+    mask = torch.ones((B, T))
+    mask[7, 20] = 0   # a hole: not a prefix of ones
+    mask[11, 33:] = 0  # padding after 33 real tokens
+    w = _wd(d)
+    conv, S = dev(d["conv_state"]).clone(), dev(d["state"]).clone()
+    out = torch.full((B, T, shape.nv, shape.dv), 7.0, dtype=torch.bfloat16, device="cuda")
+    dm = dims(shape, B, T, B)
+    ws = gdn.workspace(dm)
+    gdn.prefill_chunked(dm, inputs(w, {n: dev(a) for n, a in acts.items()}, mask=dev(mask)), conv, S, out, ws)
+    with pytest.raises(gdn.GdnError) as e:
+        gdn.check_status()
+    assert e.value.name == "GDN_ERR_MASK"
+    assert torch.equal(S[7].cpu(), d["state"][7]) and torch.equal(conv[7].cpu(), d["conv_state"][7])
+    assert bool(torch.all(out[7].float() == 7.0))
+    keep = [r for r in range(B) if r != 7]
+    ra = {n: a[keep] for n, a in acts.items()}
+    dd = dict(d)
+    ref = oracle_layer(oracle_mod, shape, dd, ra, d["conv_state"][keep], d["state"][keep], mask=mask[keep])
+    o = out[keep]
+    pad = keep.index(11)
+    assert torch.count_nonzero(o[pad, 33:].float()) == 0
+    o_real = torch.cat([o[:pad], o[pad + 1:]])
+    ref_real = np.concatenate([ref["out"][:pad], ref["out"][pad + 1:]])
+    assert_out(o_real, ref_real)
+    assert_out(o[pad, :33], ref["out"][pad, :33])
+    assert_state(S[keep], ref["state"])
+    assert torch.equal(conv[keep].cpu().double(), torch.from_numpy(ref["conv_state"]))
