@@ -144,21 +144,37 @@ struct Rows {
   __device__ __forceinline__ int start(int r) const { return cu ? cu[r] : r * T; }
   __device__ __forceinline__ int len(int r) const { return cu ? cu[r + 1] - cu[r] : T; }
   __device__ __forceinline__ int slot0(int r) const { return cu ? cu[r] / CH + r : r * cpr; }
-  // (row, chunk) of slot s, or row -1 when the slot holds no chunk
+  // (row, chunk) of slot s, or row -1 when the slot holds no chunk. Packed
+  // rows: called by whole warps. The first slots slot0(r) increase with r, so
+  // the rows with slot0(r) <= s form a prefix; each warp reads the row offsets
+  // 32 at a time (one coalesced load instead of a chain of dependent loads)
+  // and counts that prefix with a ballot.
   __device__ __forceinline__ void locate(int s, int Ttot, int &r, int &c) const {
+    int st, ln;
     if (!cu) {
       r = s / cpr;
       c = s % cpr;
+      st = r * T;
+      ln = T;
     } else {
-      int lo = 0, hi = B - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (slot0(mid) <= s) lo = mid; else hi = mid - 1;
+      const int lane = threadIdx.x & 31;
+      int n = 0;
+      for (int base = 0; base < B; base += 32) {
+        const int i = base + lane;
+        const unsigned m = __ballot_sync(0xffffffffu, i < B && __ldg(cu + i) / CH + i <= s);
+        n += __popc(m);
+        if (m != 0xffffffffu) break;
       }
-      r = lo;
-      c = s - slot0(lo);
+      r = n - 1;
+      if (r < 0) {
+        r = -1;
+        c = 0;
+        return;
+      }
+      st = __ldg(cu + r);
+      ln = __ldg(cu + r + 1) - st;
+      c = s - (st / CH + r);
     }
-    const int st = start(r), ln = len(r);
     if (r < 0 || r >= B || c < 0 || st < 0 || ln < 0 || st + ln > Ttot || c * CH >= ln) r = -1;
   }
 };
@@ -358,7 +374,7 @@ __global__ void __launch_bounds__(256, 4) front_kernel(LayerArgs A, Rows R, int 
       for (int e = 0; e < 8; ++e) ss = __fmaf_rn(y[t][e], y[t][e], ss);
 #pragma unroll
       for (int o = 1; o < 16; o <<= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
-      const float rn = __fdiv_rn(sc, sqrtf(__fadd_rn(ss, A.l2_eps)));
+      const float rn = sc * rsqrtf(ss + A.l2_eps);
 #pragma unroll
       for (int e = 0; e < 8; ++e) y[t][e] = __fmul_rn(y[t][e], rn);
     }
@@ -1461,13 +1477,13 @@ __global__ void __launch_bounds__(256, 1) state_kernel(LayerArgs A, Rows R, int 
 // ------------------------------------------------------------ chunk + state in one grid
 //
 // For calls with few (row, head) chains (a 512-token call of one row has 32):
-// the grid is one CTA per SM; CTA i runs chunk units i, i + grid, ... in
-// chunk-major order (all heads' first chunks first) and publishes each unit's
-// flag; then the last B*nv CTAs, which have the fewest units, run one chain
-// each, loading every chunk as soon as its unit is published. The chains'
-// early chunks thus overlap the units of the late chunks. The waiting CTAs are
-// at most half the grid and no CTA that runs units waits on another, so the
-// units always complete; every wait is bounded.
+// the grid is one CTA per SM. The last B*nv CTAs each run the unit of their
+// own chain's first chunk, then the chain, loading every later chunk as soon
+// as its unit is published; the other CTAs run the later chunks' units in
+// chunk-major order (all chains' second chunks first) and publish each unit's
+// flag. The chains' early chunks thus overlap the units of the late chunks.
+// The chain CTAs are at most half the grid, and no CTA waits on another before
+// its units are done, so the units always complete; every wait is bounded.
 __global__ void __launch_bounds__(256, 1) chunk_state_kernel(LayerArgs A, Rows R, int Ttot, Ws W) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -1491,14 +1507,19 @@ __global__ void __launch_bounds__(256, 1) chunk_state_kernel(LayerArgs A, Rows R
   UnitPhase ph{0u, 0u, 0u};
   bool ok = true;
   int parity = 0;
-  for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x, parity ^= 1) {
-    const int c = u / BH, rh = u % BH, r = rh / A.nv;  // chunk-major: unit (chunk c, row r, head rh % nv)
+  // units in chunk-major order, u = chunk * BH + row * nv + head. A chain CTA
+  // runs one unit, the first chunk of its own chain (u = j), so that its first
+  // step waits for no other CTA; the other CTAs share the later chunks' units
+  const int u0 = j < BH ? j : BH + (int)blockIdx.x;
+  const int ustep = j < BH ? n_units : (int)gridDim.x - BH;
+  for (int u = u0; ok && u < n_units; u += ustep, parity ^= 1) {
+    const int c = u / BH, rh = u % BH, r = rh / A.nv;  // unit (chunk c, row r, head rh % nv)
     auto find_next = [&]() {
-      const int v = u + (int)gridDim.x, c2 = v / BH, rh2 = v % BH;
+      const int v = u + ustep, c2 = v / BH, rh2 = v % BH;
       return v < n_units ? make_int2((rh2 / A.nv) * R.cpr + c2, rh2 % A.nv) : make_int2(-1, 0);
     };
-    ok = chunk_unit<false>(sm, A, R, W, r * R.cpr + c, rh % A.nv, r, c, parity, u != (int)blockIdx.x, find_next, tmem,
-                           bar, ph, true);
+    ok = chunk_unit<false>(sm, A, R, W, r * R.cpr + c, rh % A.nv, r, c, parity, u != u0, find_next, tmem, bar, ph,
+                           true);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
