@@ -259,6 +259,18 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(LayerArgs A) {
     }
     fence_mbar_init();
   }
+  // Before the wait: the first NS tasks' states are requested into L2. The
+  // slot index read here is only a hint; the loads after the wait use the one
+  // read then.
+  for (int n = 0; n < NS && n < n_tasks; ++n) {
+    const int u = (int)blockIdx.x + (n / G) * (int)gridDim.x, b = u / A.nk, h = (u % A.nk) * G + n % G;
+    const int s = A.state_idx ? __ldcg(A.state_idx + b) : b;
+    if (s >= 0 && s < A.n_slots) {
+      const char *p = reinterpret_cast<const char *>(A.state + ((size_t)s * A.nv + h) * D * D);
+      for (int off = 128 * tid; off < D * D * 4; off += 128 * (int)blockDim.x)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(p + off));
+    }
+  }
   griddep_wait();  // the kernel before this call (e.g. the previous layer's) is complete
   griddep_trigger();
   for (int i = tid; i < my_units && i < kSlotTable; i += blockDim.x) slot_tab[i] = resolve(i, true);

@@ -237,6 +237,23 @@ __device__ __forceinline__ void named_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
+// ------------------------------------------------------------ SiLU
+
+// x / (1 + 2^(-x log2 e)) with the approximate base-2 exponential and
+// reciprocal instructions (relative error of each ~2^-22; denormals flush to
+// zero); for large negative x, 2^(...) is +inf and the result -0.
+__device__ __forceinline__ float silu_approx(float x) {
+  float e, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x * -1.4426950408889634f));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
+  return x * r;
+}
+// the depthwise conv of one channel at one token (taps x0 .. x3, x3 the current token), then SiLU
+__device__ __forceinline__ float conv4_silu_approx(float w0, float w1, float w2, float w3, float x0, float x1, float x2,
+                                                   float x3) {
+  return silu_approx(fmaf(w3, x3, fmaf(w2, x2, fmaf(w1, x1, w0 * x0))));
+}
+
 // ------------------------------------------------------------ split fp16
 
 __device__ __forceinline__ void split2(float a, float b, uint32_t &hi, uint32_t &lo) {
@@ -357,7 +374,7 @@ __global__ void __launch_bounds__(256, 4) front_kernel(LayerArgs A, Rows R, int 
     }
 #pragma unroll
     for (int t = 0; t < 4; ++t)
-      y[t][e] = (slot >= 0 && pos0 + t < len) ? conv4_silu_fast(w0, w1, w2, w3, x[t], x[t + 1], x[t + 2], x[t + 3])
+      y[t][e] = (slot >= 0 && pos0 + t < len) ? conv4_silu_approx(w0, w1, w2, w3, x[t], x[t + 1], x[t + 2], x[t + 3])
                                               : 0.0f;
   }
   // q, k: L2 norm per token over the 16 lanes of the half-warp; then the
@@ -1399,8 +1416,8 @@ __device__ __forceinline__ bool state_chain(unsigned char *sm, uint64_t *bars, c
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const float z0 = __uint_as_float(zw[e] << 16), z1 = __uint_as_float(zw[e] & 0xffff0000u);
-              const float y0 = ov[2 * e] * rs * (wn[2 * e] * silu_fast(z0));
-              const float y1 = ov[2 * e + 1] * rs * (wn[2 * e + 1] * silu_fast(z1));
+              const float y0 = ov[2 * e] * rs * (wn[2 * e] * silu_approx(z0));
+              const float y1 = ov[2 * e + 1] * rs * (wn[2 * e + 1] * silu_approx(z1));
               const __nv_bfloat162 b2 = __floats2bfloat162_rn(y0, y1);
               pw[e] = *reinterpret_cast<const uint32_t *>(&b2);
             }
@@ -1669,7 +1686,7 @@ __global__ void __launch_bounds__(256, 2) output_kernel(LayerArgs A, Rows R, int
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
       const int i = 32 * hh + e;
-      const float gz = wv * silu_fast(__bfloat162float(os[i * HD + v]));
+      const float gz = wv * silu_approx(__bfloat162float(os[i * HD + v]));
       os[i * HD + v] = __float2bfloat16_rn(o[e] * rstd[i] * gz);
     }
     fence_proxy_async_smem();

@@ -41,21 +41,6 @@ __device__ __forceinline__ float conv4_silu(float w0, float w1, float w2, float 
   return silu_f(acc);
 }
 
-// Fast variants for the chunked prefill (no bit-exactness constraint there):
-// x / (1 + 2^(-x log2 e)) with the approximate base-2 exponential and
-// reciprocal instructions (relative error of each ~2^-22; denormals flush to
-// zero). Large negative x: 2^(...) is +inf and the result -0.
-__device__ __forceinline__ float silu_fast(float x) {
-  float e, r;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x * -1.4426950408889634f));
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
-  return x * r;
-}
-__device__ __forceinline__ float conv4_silu_fast(float w0, float w1, float w2, float w3, float x0, float x1,
-                                                 float x2, float x3) {
-  return silu_fast(fmaf(w3, x3, fmaf(w2, x2, fmaf(w1, x1, w0 * x0))));
-}
-
 // L2-normalise a D-vector in shared memory in place and multiply by `scale`
 // (use_qk_l2norm_in_kernel: x / sqrt(sum x^2 + eps)). Called by one whole warp.
 template <int D>
