@@ -180,8 +180,9 @@ struct Rows {
 };
 
 // (row, chunk) of slot s after the front kernel of the same call: packed rows
-// read the front kernel's map (one load through L2 instead of a binary search
-// over the row offsets); dense rows compute it.
+// read the front kernel's map (one load through L2, and callable by a single
+// thread, unlike the warp-wide search over the row offsets); dense rows
+// compute it.
 __device__ __forceinline__ void slot_row(const Rows &R, const Ws &W, int s, int Ttot, int &r, int &c) {
   if (R.cu) {
     const int2 v = __ldcg(W.slot_rc + s);
