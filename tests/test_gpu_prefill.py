@@ -255,3 +255,46 @@ def test_many_chains_rejected_and_padded_rows(oracle_mod):
     assert_out(o[pad, :33], ref["out"][pad, :33])
     assert_state(S[keep], ref["state"])
     assert torch.equal(conv[keep].cpu().double(), torch.from_numpy(ref["conv_state"]))
+
+
+def test_packed_rows_beyond_one_warp_of_offsets(oracle_mod):
+    """Head size 128, 45 packed rows: the slot -> row lookup reads the row
+    offsets 32 at a time, so rows 32-44 sit in a second window. Real lengths
+    from 0 to 200 tokens (a row of padding only among them), each padded to a
+    multiple of 16 with mask zeros, each row from its own state: outputs at
+    real tokens, zeros at padding, final states and conv tails (bit for bit)
+    against the oracle, row by row."""
+    shape = I.Shape(nk=2, nv=4, dk=128, dv=128)
+    B = 45
+    real = [(37 * r + 11) % 201 for r in range(B)]
+    real[20] = 0                  # padding only: the row stays as it was
+    real[3], real[40] = 64, 129   # a whole chunk, and one token past two
+    padded = [max(16, (n + 15) // 16 * 16) for n in real]
+    cu = [0]
+    for p in padded:
+        cu.append(cu[-1] + p)
+    total = cu[-1]
+    d = I.decode_batch(seed=97, B=B, shape=shape)
+    acts = I.activations(shape, 1, total, torch.Generator().manual_seed(98))
+    mask = torch.zeros((1, total))
+    for r in range(B):
+        mask[0, cu[r]:cu[r] + real[r]] = 1.0
+    w = _wd(d)
+    conv, S = dev(d["conv_state"]).clone(), dev(d["state"]).clone()
+    cu_d = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    out = _prefill(shape, w, {n: dev(a) for n, a in acts.items()}, conv, S, mask=dev(mask), cu=cu_d, B=B)
+    gdn.check_status()
+    out_h, S_h, conv_h = out.cpu(), S.cpu(), conv.cpu()
+    for r in range(B):
+        a, b_ = cu[r], cu[r + 1]
+        Lr = real[r]
+        assert torch.count_nonzero(out_h[:, a + Lr:b_]) == 0, f"row {r}"
+        if Lr == 0:
+            assert torch.equal(S_h[r], d["state"][r]) and torch.equal(conv_h[r], d["conv_state"][r])
+            continue
+        ra = {n: acts[n][:, a:b_] for n in ACTS}
+        ref = oracle_layer(oracle_mod, shape, d, ra, d["conv_state"][r:r + 1], d["state"][r:r + 1],
+                           mask=mask[:, a:b_])
+        assert_out(out_h[:, a:a + Lr], ref["out"][:, :Lr], f"row {r}")
+        assert_state(S_h[r], ref["state"][0], f"row {r}")
+        assert torch.equal(conv_h[r].double(), torch.from_numpy(ref["conv_state"][0]))
