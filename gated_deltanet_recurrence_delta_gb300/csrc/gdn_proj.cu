@@ -27,6 +27,7 @@ namespace gdn {
 namespace proj {
 
 constexpr int BM = 128;     // output features per tile (TMEM lanes)
+constexpr int kGroupF = 16;  // feature tiles per group of the grouped tile order
 constexpr int BK = 64;      // K elements per stage: one 128-byte swizzled row per operand row
 // Stages of the K ring: decode-sized calls stream their weights and want many
 // bytes in flight per SM; prefill-sized ones keep two CTAs per SM.
@@ -88,7 +89,9 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t remote) {
 // memory (each CTA parks its tile in its own stage ring, free by then, and
 // CTA r sums every CTA's columns [r BN/SPLIT, (r+1) BN/SPLIT) and writes them).
 // For calls with too few output tiles to occupy the GPU.
-template <int BN, int SPLIT>
+// GROUPED (SPLIT 1, weights far larger than a share of L2): the tiles are
+// visited in groups of kGroupF feature tiles by all token tiles.
+template <int BN, int SPLIT, bool GROUPED>
 __global__ void __launch_bounds__(128, 1) gemm_kernel(const __grid_constant__ CUtensorMap wmap,
                                                       const __grid_constant__ CUtensorMap xmap, int Nout, int M,
                                                       int K, Epi epi, unsigned int *status) {
@@ -104,7 +107,20 @@ __global__ void __launch_bounds__(128, 1) gemm_kernel(const __grid_constant__ CU
   __shared__ int s_abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = SPLIT > 1 ? cluster_rank() : 0u;
-  const int f0 = (blockIdx.x / SPLIT) * BM, t0 = blockIdx.y * BN;
+  int fb = blockIdx.x / SPLIT, tb = blockIdx.y;  // feature tile, token tile
+  if (GROUPED) {
+    // consecutive CTAs take kGroupF feature tiles by all token tiles, feature
+    // tile fastest, so the CTAs resident at one time share their weight and
+    // token tiles in L2 (in row-major order the 101 MB in-projection weights
+    // streamed from DRAM once per ~3 token tiles)
+    const int nf = (int)gridDim.x, nt = (int)gridDim.y;
+    const int pid = (int)blockIdx.y * nf + (int)blockIdx.x, per_group = kGroupF * nt;
+    const int g = pid / per_group, f_first = g * kGroupF, gsize = min(nf - f_first, kGroupF);
+    const int r = pid - g * per_group;
+    fb = f_first + r % gsize;
+    tb = r / gsize;
+  }
+  const int f0 = fb * BM, t0 = tb * BN;
   const int nkt = K / BK, kb0 = (int)(nkt * (long long)rank / SPLIT), kb1 = (int)(nkt * (long long)(rank + 1) / SPLIT);
   const int nk = kb1 - kb0;  // this CTA's K-slices: kb0 + 0 .. kb0 + nk - 1
   if (tid == 0) {
@@ -271,13 +287,14 @@ gdn_status encode_operand(CUtensorMap *map, const void *base, long long rows, lo
   return GDN_OK;
 }
 
-template <int BN, int SPLIT>
+template <int BN, int SPLIT, bool GROUPED = false>
 gdn_status launch_t(const void *w, const void *x, int Nout, int M, int K, const Epi &epi, cudaStream_t stream) {
   static_assert(SPLIT == 1 || BN * BM * 4 <= Smem<BN>::kBar, "the partial tile fits in the stage ring");
+  static_assert(!GROUPED || SPLIT == 1, "grouped order for unsplit tiles");
   const DeviceInfo &dev = device_info();
   static std::atomic<bool> attr_set[kMaxDevices];
   if (!attr_set[dev.id].load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(gemm_kernel<BN, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(gemm_kernel<BN, SPLIT, GROUPED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Smem<BN>::kBytes) != cudaSuccess)
       return fail(GDN_ERR_CUDA, "projection: cannot reserve shared memory");
     attr_set[dev.id].store(true, std::memory_order_release);
@@ -299,7 +316,7 @@ gdn_status launch_t(const void *w, const void *x, int Nout, int M, int K, const 
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  if (cudaLaunchKernelEx(&cfg, gemm_kernel<BN, SPLIT>, wmap, xmap, Nout, M, K, epi, dev.status) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, gemm_kernel<BN, SPLIT, GROUPED>, wmap, xmap, Nout, M, K, epi, dev.status) != cudaSuccess)
     return check_launch("projection");
   return check_launch("projection");
 }
@@ -315,6 +332,8 @@ gdn_status launch(const void *w, const void *x, int Nout, int M, int K, const Ep
     if (2 * tiles <= sms && nkt >= 2) return launch_t<64, 2>(w, x, Nout, M, K, epi, stream);
     return launch_t<64, 1>(w, x, Nout, M, K, epi, stream);
   }
+  // weights beyond half of L2 would stream from DRAM once per few token tiles in row-major order
+  if ((long long)Nout * K * 2 > (64LL << 20)) return launch_t<128, 1, true>(w, x, Nout, M, K, epi, stream);
   return launch_t<128, 1>(w, x, Nout, M, K, epi, stream);
 }
 
