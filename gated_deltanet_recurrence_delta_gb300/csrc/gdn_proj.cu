@@ -30,10 +30,11 @@ constexpr int BM = 128;     // output features per tile (TMEM lanes)
 constexpr int kGroupF = 16;  // feature tiles per group of the grouped tile order
 constexpr int BK = 64;      // K elements per stage: one 128-byte swizzled row per operand row
 // Stages of the K ring: decode-sized calls stream their weights and want many
-// bytes in flight per SM; prefill-sized ones keep two CTAs per SM.
+// bytes in flight per SM; prefill-sized ones keep two CTAs per SM (each one's
+// epilogue then runs under the other's products).
 template <int BN>
 struct Stages {
-  static constexpr int value = BN <= 64 ? 8 : 3;
+  static constexpr int value = BN <= 64 ? 8 : (BN == 128 ? 3 : 2);
 };
 
 // Output features [n0, n1) go to dst[token * ld + (feature - n0)].
@@ -321,8 +322,9 @@ gdn_status launch_t(const void *w, const void *x, int Nout, int M, int K, const 
   return check_launch("projection");
 }
 
-// Token tile: 64 for decode-sized calls (one tile), 128 otherwise. Calls with
-// too few output tiles for the GPU split K over a cluster (2 or 4 CTAs).
+// Token tile: 64 for decode-sized calls (one tile), 128 up to 128 tokens, 256
+// beyond. Calls with too few output tiles for the GPU split K over a cluster
+// (2 or 4 CTAs).
 gdn_status launch(const void *w, const void *x, int Nout, int M, int K, const Epi &epi, cudaStream_t stream) {
   const int sms = device_info().sms;
   const long long tiles = (long long)((Nout + BM - 1) / BM) * ((M + (M <= 64 ? 64 : 128) - 1) / (M <= 64 ? 64 : 128));
@@ -333,8 +335,11 @@ gdn_status launch(const void *w, const void *x, int Nout, int M, int K, const Ep
     return launch_t<64, 1>(w, x, Nout, M, K, epi, stream);
   }
   // weights beyond half of L2 would stream from DRAM once per few token tiles in row-major order
-  if ((long long)Nout * K * 2 > (64LL << 20)) return launch_t<128, 1, true>(w, x, Nout, M, K, epi, stream);
-  return launch_t<128, 1>(w, x, Nout, M, K, epi, stream);
+  const bool grouped = (long long)Nout * K * 2 > (64LL << 20);
+  if (M <= 128) return grouped ? launch_t<128, 1, true>(w, x, Nout, M, K, epi, stream)
+                               : launch_t<128, 1>(w, x, Nout, M, K, epi, stream);
+  // 256-token tiles: a quarter less shared-memory traffic per product than 128
+  return grouped ? launch_t<256, 1, true>(w, x, Nout, M, K, epi, stream) : launch_t<256, 1>(w, x, Nout, M, K, epi, stream);
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
