@@ -68,9 +68,11 @@ def test_in_proj_split_small(oracle_mod, M):
         _check(o[n], ref[n], n)
 
 
-@pytest.mark.parametrize("M", [64, 512])
+@pytest.mark.parametrize("M", [64, 100, 512])
 def test_in_proj_qwen_layer(oracle_mod, M):
-    """The Qwen3.5-9B-like layer: H = 4096, 12352 features (16/32 heads, d=128)."""
+    """The Qwen3.5-9B-like layer: H = 4096, 12352 features (16/32 heads, d=128):
+    one 64-token tile, one partial 128-token tile and two 256-token tiles, the
+    last two in the grouped tile order (101 MB of weights)."""
     shape = I.QWEN35_9B
     g = torch.Generator().manual_seed(210 + M)
     H = 4096
