@@ -298,3 +298,24 @@ def test_packed_rows_beyond_one_warp_of_offsets(oracle_mod):
         assert_out(out_h[:, a:a + Lr], ref["out"][:, :Lr], f"row {r}")
         assert_state(S_h[r], ref["state"][0], f"row {r}")
         assert torch.equal(conv_h[r].double(), torch.from_numpy(ref["conv_state"][0]))
+
+
+@pytest.mark.parametrize("B", [19, 20])
+def test_chain_grid_boundary(oracle_mod, B):
+    """Head size 128, 4 value heads, two chunks per row. 19 rows make 76
+    chains on a grid of 152 chunk units: the few-chain grid at its limit, half
+    of its CTAs running chains (each first runs its own chain's first chunk)
+    and the other half the second chunks. 20 rows (80 chains) take the
+    separate chunk and state kernels. Both against the oracle."""
+    shape = I.Shape(nk=2, nv=4, dk=128, dv=128)
+    T = 128
+    d = I.decode_batch(seed=99 + B, B=B, shape=shape)
+    acts = I.activations(shape, B, T, torch.Generator().manual_seed(100 + B))
+    w = _wd(d)
+    conv, S = dev(d["conv_state"]).clone(), dev(d["state"]).clone()
+    out = _prefill(shape, w, {n: dev(a) for n, a in acts.items()}, conv, S)
+    gdn.check_status()
+    ref = oracle_layer(oracle_mod, shape, d, acts, d["conv_state"], d["state"])
+    assert_out(out, ref["out"])
+    assert_state(S, ref["state"])
+    assert torch.equal(conv.cpu().double(), torch.from_numpy(ref["conv_state"]))
