@@ -1192,14 +1192,21 @@ __device__ __forceinline__ bool state_chain(unsigned char *sm, uint64_t *bars, c
   }
 
   // chunk ci's W|Q' image, the fp16 K image (hi) of the key head, U and exp(G_C - G)
-  auto issue_loads = [&](int ci) {  // thread 0
+  constexpr uint32_t kLdBytes = 32768 + 16384 + 16384 + kSecRec * 4;
+  // copy `part` (0-3, or all four with -1) of chunk ci's loads
+  auto issue_part = [&](int ci, int part) {
     const int buf = ci & 1, s = s0 + ci;
     const size_t sh = (size_t)s * A.nv + h;
-    mbar_arrive_expect_tx(&bar_ld[buf], 32768 + 16384 + 16384 + kSecRec * 4);
-    bulk_g2s(sm + kSOffWQ + buf * 32768, W.wq + sh * kWQ, 32768, &bar_ld[buf]);
-    bulk_g2s(sm + kSOffKT + buf * 16384, W.kimg + ((size_t)s * A.nk + kh) * 2 * kImg, 16384, &bar_ld[buf]);
-    bulk_g2s(sm + kSOffUT + buf * 16384, W.ut + sh * kRowF, 16384, &bar_ld[buf]);
-    bulk_g2s(sm + kSOffSec + buf * kSecRec * 4, W.gate + sh * kGateRec + kSecOff, kSecRec * 4, &bar_ld[buf]);
+    if (part < 0 || part == 0) bulk_g2s(sm + kSOffWQ + buf * 32768, W.wq + sh * kWQ, 32768, &bar_ld[buf]);
+    if (part < 0 || part == 1)
+      bulk_g2s(sm + kSOffKT + buf * 16384, W.kimg + ((size_t)s * A.nk + kh) * 2 * kImg, 16384, &bar_ld[buf]);
+    if (part < 0 || part == 2) bulk_g2s(sm + kSOffUT + buf * 16384, W.ut + sh * kRowF, 16384, &bar_ld[buf]);
+    if (part < 0 || part == 3)
+      bulk_g2s(sm + kSOffSec + buf * kSecRec * 4, W.gate + sh * kGateRec + kSecOff, kSecRec * 4, &bar_ld[buf]);
+  };
+  auto issue_loads = [&](int ci) {  // thread 0
+    mbar_arrive_expect_tx(&bar_ld[ci & 1], kLdBytes);
+    issue_part(ci, -1);
   };
   // thread 0: the last chunk whose loads are issued, and the last chunk up to
   // which every unit is known published and acquired; gave_up: a unit's flag
@@ -1288,7 +1295,15 @@ __device__ __forceinline__ bool state_chain(unsigned char *sm, uint64_t *bars, c
     const int buf = ci & 1, t0 = ci * CH;
     const int ntok = min(CH, len - t0), nreal = max(0, min(CH, Lr - t0));
     int seen = -1;  // thread 0: the last chunk up to which the units read as published (unordered reads)
-    if (tid == 0) {  // a chunk not prefetched is waited for; the next one is prefetched when ready
+    // without unit flags (every chunk published before this grid), the next
+    // chunk's four copies are issued by four threads once the product below is
+    // on its way (threads 0, 32, 64, 96), their byte count expected here first
+    const bool split_next = !wait_units && ci + 1 < n_chunks;
+    if (split_next && tid == 0) {
+      mbar_arrive_expect_tx(&bar_ld[(ci + 1) & 1], kLdBytes);
+      issued = ci + 1;
+    }
+    if (wait_units && tid == 0) {  // a chunk not prefetched is waited for; the next one is prefetched when ready
       if (issued < ci) issue_when_ready(ci, true);
       if (issued == ci && ci + 1 < n_chunks) {
         if (ci + 1 <= acquired) {
@@ -1318,6 +1333,7 @@ __device__ __forceinline__ bool state_chain(unsigned char *sm, uint64_t *bars, c
         issued = ci + 1;
       }
     }
+    if (split_next && (tid & 31) == 0 && tid < 128) issue_part(ci + 1, tid >> 5);
     if (!cta_wait(bar_mma, 0, A.status)) {
       ok = false;
       break;
