@@ -208,6 +208,22 @@ __device__ __forceinline__ bool cta_wait(uint64_t *bar, uint32_t parity, unsigne
   return true;
 }
 
+// The same for two barriers at once (one CTA barrier instead of two).
+__device__ __forceinline__ bool cta_wait2(uint64_t *b0, uint32_t p0, uint64_t *b1, uint32_t p1, unsigned int *status) {
+  const bool lead = threadIdx.x == 0;
+  bool ok = true;
+  if (lead) ok = mbar_wait_bounded(b0, p0) && mbar_wait_bounded(b1, p1);
+  if (__syncthreads_or(!ok)) {
+    if (lead) set_status(status, GDN_ERR_TIMEOUT);
+    return false;
+  }
+  if (!lead) {
+    (void)mbar_try_wait(b0, p0);
+    (void)mbar_try_wait(b1, p1);
+  }
+  return true;
+}
+
 // A chunk unit's completion flag: set with release semantics at GPU scope,
 // read with acquire semantics (both through L2).
 __device__ __forceinline__ void release_flag(int *flag) {
@@ -1369,7 +1385,7 @@ __device__ __forceinline__ bool state_chain(unsigned char *sm, uint64_t *bars, c
     // ---- the chunk's outputs while dS forms: O = O_S + O_local (value row v =
     //      TMEM lane, tokens 32hh .. 32hh+31 = TMEM columns 64 + 32hh ..), then
     //      the gated RMSNorm over the 128 value rows of each token
-    if (OUT && (!cta_wait(bar_ol, (uint32_t)(ci & 1), A.status) || !cta_wait(bar_z, (uint32_t)(ci & 1), A.status))) {
+    if (OUT && !cta_wait2(bar_ol, (uint32_t)(ci & 1), bar_z, (uint32_t)(ci & 1), A.status)) {
       ok = false;
       break;
     }
