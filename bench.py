@@ -198,7 +198,7 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
-def timed(world, steps, warmup, step_fn):
+def timed(world, steps, warmup, step_fn, start_fn=None, end_fn=None):
     """Run warmup steps, then `steps` timed steps bracketed by a barrier and a
     synchronize on both sides; returns ms per step, max over ranks. One event
     pair brackets the whole region: an event recorded between two launches
@@ -221,8 +221,12 @@ def timed(world, steps, warmup, step_fn):
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda._sleep(int(min(0.5, 2.0 * host_s * (steps + 1) + 2e-3) * SPIN_HZ))
     s.record()
+    if start_fn:
+        start_fn()  # work on other streams waits for the start event
     for i in range(steps):
         step_fn(warmup + i, None)
+    if end_fn:
+        end_fn()  # the current stream waits for work on other streams
     e.record()
     torch.cuda.synchronize()
     barrier(world)
@@ -305,14 +309,43 @@ def phase_decode(gdn, world, steps, warmup, peak_hbm, local=0, e2e=True):
         h2d = sum(src[n].numel() * src[n].element_size() for n in ACTS)
         d2h = out_h.numel() * out_h.element_size()
 
-        def e2e_step(i, _):
-            dd = sets[i % n_sets]
-            dbuf, inp = dev_in[i % n_sets]
-            dbuf.copy_(hbuf, non_blocking=True)
-            gdn.decode_step(dd["dims"], inp, dd["conv_state"], dd["state"], dd["out"])
-            out_h.copy_(dd["out"], non_blocking=True)
+        # copies on two copy streams, so that step i + 1's inputs travel while
+        # step i decodes and step i's outputs travel while step i + 1 decodes;
+        # events order each buffer's writes and reads across the streams
+        comp = torch.cuda.current_stream()
+        h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
+        ev_in = [torch.cuda.Event() for _ in range(n_sets)]    # set k's inputs are on the device
+        ev_dec = [torch.cuda.Event() for _ in range(n_sets)]   # set k's decode is done
+        ev_out = [torch.cuda.Event() for _ in range(n_sets)]   # set k's outputs are on the host
 
-        ems = timed(world, steps, warmup, e2e_step)
+        def e2e_step(i, _):
+            k = i % n_sets
+            dd = sets[k]
+            dbuf, inp = dev_in[k]
+            if i >= n_sets:
+                h2d_s.wait_event(ev_dec[k])  # the decode n_sets steps ago has read this input buffer
+            with torch.cuda.stream(h2d_s):
+                dbuf.copy_(hbuf, non_blocking=True)
+            ev_in[k].record(h2d_s)
+            comp.wait_event(ev_in[k])
+            if i >= n_sets:
+                comp.wait_event(ev_out[k])  # the outputs n_sets steps ago have left this buffer
+            gdn.decode_step(dd["dims"], inp, dd["conv_state"], dd["state"], dd["out"])
+            ev_dec[k].record(comp)
+            d2h_s.wait_event(ev_dec[k])
+            with torch.cuda.stream(d2h_s):
+                out_h.copy_(dd["out"], non_blocking=True)
+            ev_out[k].record(d2h_s)
+
+        def e2e_join():  # the timed region ends once the last outputs are on the host
+            comp.wait_stream(h2d_s)
+            comp.wait_stream(d2h_s)
+
+        def e2e_start():  # and starts before the first inputs leave the host
+            h2d_s.wait_stream(comp)
+            d2h_s.wait_stream(comp)
+
+        ems = timed(world, steps, warmup, e2e_step, start_fn=e2e_start, end_fn=e2e_join)
         res["e2e"] = {"value": B * world / (ems * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                       "d2h_bytes_per_step": d2h}
         del dev_in
