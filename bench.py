@@ -210,7 +210,10 @@ def timed(world, steps, warmup, step_fn, start_fn=None, end_fn=None):
     queued just before the start event, long enough to cover the host's
     enqueue of all timed steps (measured on the warm-up steps): the start event
     is then reached only once every step is queued behind it, so the events
-    time the device work and not the Python launch overhead between launches."""
+    time the device work and not the Python launch overhead between launches.
+    start_fn / end_fn (optional): called right after the start event and
+    before the end event, for steps that also use other streams (those streams
+    wait for the start, and the timing stream waits for them at the end)."""
     t0 = time.perf_counter()
     for i in range(warmup):
         step_fn(i, None)
