@@ -80,3 +80,41 @@ def test_mxfp8_decode(oracle_mod, shape, B):
     assert e_out <= 0.15, f"outputs {e_out:.3e} off the bf16-input result (relative Frobenius)"
     assert e_state <= 0.1, f"state {e_state:.3e} off the bf16-input result (relative Frobenius)"
     assert np.isfinite(e_out) and np.isfinite(e_state)
+
+
+def test_mxfp8_decode_masked_rows_and_state_pool():
+    """The benchmark's size (64 rows, 16/32 heads, d=128) with two masked rows
+    and each row's state in a pool slot of its own (a permutation of 70 slots):
+    the MXFP8 step equals the bf16 step on the dequantized inputs bit for bit,
+    masked rows and unused slots untouched."""
+    shape, B, n_slots = I.QWEN35_9B, 64, 70
+    d = I.decode_batch(seed=147, B=B, shape=shape)
+    enc = {n: I.mxfp8(d[n]) for n in MX}
+    deq = {n: dequant(*enc[n]).to(torch.bfloat16) for n in MX}
+    acts_deq = {**{n: d[n] for n in ACTS}, **deq}
+    w = {n: dev(d[n]) for n in WEIGHTS}
+    g = torch.Generator().manual_seed(148)
+    slots = torch.randperm(n_slots, generator=g)[:B].to(torch.int32)
+    mask = torch.ones(B)
+    mask[[5, 40]] = 0.0
+    pool_S = torch.randn((n_slots, shape.nv, shape.dk, shape.dv), generator=g) * 0.1
+    pool_c = (torch.randn((n_slots, 3, shape.C), generator=g)).to(torch.bfloat16)
+    dm = dims(shape, B, 1, n_slots)
+    conv8, S8 = dev(pool_c).clone(), dev(pool_S).clone()
+    out8 = torch.empty((B, 1, shape.nv, shape.dv), dtype=torch.bfloat16, device="cuda")
+    mx = {n: (dev(enc[n][0]), dev(enc[n][1])) for n in MX}
+    inp8 = gdn.make_inputs_mxfp8(mx["q"][0], mx["k"][0], mx["v"][0], mx["z"][0], mx["q"][1], mx["k"][1],
+                                 mx["v"][1], mx["z"][1], dev(d["a"]), dev(d["b"]), w["A_log"], w["dt_bias"],
+                                 w["conv_w"], w["norm_w"], mask=dev(mask), state_idx=dev(slots))
+    gdn.decode_step_mxfp8(dm, inp8, conv8, S8, out8)
+    convb, Sb = dev(pool_c).clone(), dev(pool_S).clone()
+    outb = torch.empty_like(out8)
+    gdn.decode_step(dm, inputs(w, {n: dev(a) for n, a in acts_deq.items()}, mask=dev(mask), state_idx=dev(slots)),
+                    convb, Sb, outb)
+    gdn.check_status()
+    assert torch.equal(out8, outb) and torch.equal(S8, Sb) and torch.equal(conv8, convb)
+    untouched = sorted(set(range(n_slots)) - set(slots.tolist())) + [int(slots[5]), int(slots[40])]
+    for s_ in untouched:
+        assert torch.equal(S8[s_].cpu(), pool_S[s_]) and torch.equal(conv8[s_].cpu(), pool_c[s_]), f"slot {s_}"
+    assert all(not torch.equal(S8[int(slots[r])].cpu(), pool_S[int(slots[r])]) for r in (0, 1, 63))
+    assert torch.count_nonzero(out8[[5, 40]]) == 0
