@@ -123,7 +123,15 @@ typedef struct gdn_inputs {
  *   conv_state       bf16 [n_slots][conv_k-1][C]   in/out
  *   recurrent_state  fp32 [n_slots][nv][dk][dv]    in/out
  *   out              bf16 [B][1][nv][dv]           gated-RMSNorm output
- * A row whose mask is 0 is left untouched and gets zero output. */
+ * A row whose mask is 0 is left untouched and gets zero output.
+ * Zero-copy: the activations q, k, v, z, a, b and `out` may also be
+ * page-locked host memory that is mapped into the device's address space at
+ * the same address (cudaHostAlloc / cudaMallocHost under unified addressing);
+ * the kernel then reads the inputs and writes the output rows across the
+ * host link itself (NVLink-C2C on a Grace-Blackwell node), with results bit
+ * for bit those of device buffers. The caller keeps such host buffers
+ * untouched from the call until the stream has passed it. The states stay in
+ * device memory. */
 gdn_status gdn_decode_step(const gdn_dims *dims, const gdn_inputs *in, void *conv_state,
                            float *recurrent_state, void *out, void *stream);
 

@@ -92,6 +92,45 @@ def test_decode_mask_and_state_pool(oracle_mod):
         assert torch.equal(S[slot].cpu(), S0[slot]) and torch.equal(conv[slot].cpu(), conv0[slot])
 
 
+def _host_mapped(t):
+    """True when the pinned host tensor t is mapped into the device's address
+    space at its own address (driver pointer attributes: memory type = host,
+    device pointer = the host pointer)."""
+    import ctypes
+    cu = ctypes.CDLL("libcuda.so.1")
+    cu.cuPointerGetAttribute.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64]
+    mt, dp = ctypes.c_uint(0), ctypes.c_uint64(0)
+    CU_POINTER_ATTRIBUTE_MEMORY_TYPE, CU_POINTER_ATTRIBUTE_DEVICE_POINTER, CU_MEMORYTYPE_HOST = 2, 3, 1
+    if cu.cuPointerGetAttribute(ctypes.byref(mt), CU_POINTER_ATTRIBUTE_MEMORY_TYPE, t.data_ptr()) != 0:
+        return False
+    if cu.cuPointerGetAttribute(ctypes.byref(dp), CU_POINTER_ATTRIBUTE_DEVICE_POINTER, t.data_ptr()) != 0:
+        return False
+    return mt.value == CU_MEMORYTYPE_HOST and dp.value == t.data_ptr()
+
+
+def test_decode_zero_copy_host_activations(oracle_mod):
+    """The activations and the output rows in pinned host memory (the kernel
+    reads and writes them across the host link): bit for bit the call on
+    device buffers, and the oracle's result."""
+    d = I.decode_batch(seed=21, B=64)
+    s = d["shape"]
+    w, acts = _wd(d), _acts(d)
+    hacts = {n: d[n].contiguous().pin_memory() for n in ACTS}
+    hout = torch.zeros((64, 1, s.nv, s.dv), dtype=torch.bfloat16).pin_memory()
+    if not all(_host_mapped(t) for t in list(hacts.values()) + [hout]):
+        pytest.skip("pinned host memory is not mapped at its own address on this system")
+    conv_d, S_d = dev(d["conv_state"]).clone(), dev(d["state"]).clone()
+    conv_h, S_h = conv_d.clone(), S_d.clone()
+    out_d = _decode(s, w, acts, conv_d, S_d)
+    gdn.decode_step(dims(s, 64, 1, 64), inputs(w, hacts), conv_h, S_h, hout)
+    torch.cuda.synchronize()
+    gdn.check_status()
+    assert torch.equal(hout, out_d.cpu())
+    assert torch.equal(S_h, S_d) and torch.equal(conv_h, conv_d)
+    ref = oracle_layer(oracle_mod, s, d, d, d["conv_state"], d["state"])
+    assert_out(hout, ref["out"])
+
+
 @pytest.mark.parametrize("shape,T", [(I.TINY, 8), (I.QWEN35_9B, 8), (I.Shape(nk=1, nv=4, dk=128, dv=128), 8),
                                      (I.Shape(nk=1, nv=4, dk=128, dv=128), 1), (I.Shape(nk=1, nv=4, dk=128, dv=128), 2),
                                      (I.Shape(nk=1, nv=4, dk=128, dv=128), 3), (I.Shape(nk=1, nv=4, dk=128, dv=128), 5),
