@@ -118,3 +118,45 @@ def test_mxfp8_decode_masked_rows_and_state_pool():
         assert torch.equal(S8[s_].cpu(), pool_S[s_]) and torch.equal(conv8[s_].cpu(), pool_c[s_]), f"slot {s_}"
     assert all(not torch.equal(S8[int(slots[r])].cpu(), pool_S[int(slots[r])]) for r in (0, 1, 63))
     assert torch.count_nonzero(out8[[5, 40]]) == 0
+
+
+def test_mxfp8_every_code_at_several_scales():
+    """Every finite e4m3 code (254 of the 256 bytes; S.1111.111 is NaN), with
+    block scales from 2^-117 to 2^7, so that every dequantized value, from the
+    smallest subnormal code to 448, lands in bf16's normal range: the MXFP8
+    step equals the bf16 step on the dequantized inputs bit for bit. This pins
+    the kernel's e4m3 decoding (subnormals, the sign, the largest code) and its
+    scaling against torch's float8_e4m3fn conversion."""
+    shape, B = I.QWEN35_9B, 4
+    d = I.decode_batch(seed=149, B=B, shape=shape)
+    codes = torch.tensor([c for c in range(256) if c & 0x7F != 0x7F], dtype=torch.uint8)
+    scales = torch.tensor([10, 100, 127, 134, 120], dtype=torch.uint8)  # 2^(s - 127)
+    enc = {}
+    for i, n in enumerate(MX):
+        numel = d[n].numel()
+        e = codes[(torch.arange(numel) + 37 * i) % codes.numel()].reshape(d[n].shape)
+        s = scales[(torch.arange(numel // 32) + i) % scales.numel()].reshape(*d[n].shape[:-1], -1)
+        enc[n] = (e, s)
+    assert all(set(enc[n][0].flatten().tolist()) == set(codes.tolist()) for n in MX)
+    deq = {n: dequant(*enc[n]).to(torch.bfloat16) for n in MX}
+    for n in MX:  # every dequantized value is exact in bf16 and normal (or zero)
+        f = dequant(*enc[n])
+        assert torch.equal(deq[n].float(), f)
+        nz = f[f != 0].abs()
+        assert float(nz.min()) >= 2.0 ** -126 and float(nz.max()) <= 448.0 * 2.0 ** 7
+    acts_deq = {**{n: d[n] for n in ACTS}, **deq}
+    w = {n: dev(d[n]) for n in WEIGHTS}
+    dm = dims(shape, B, 1, B)
+    conv8, S8 = dev(d["conv_state"]).clone(), dev(d["state"]).clone()
+    out8 = torch.empty((B, 1, shape.nv, shape.dv), dtype=torch.bfloat16, device="cuda")
+    mx = {n: (dev(enc[n][0]), dev(enc[n][1])) for n in MX}
+    inp8 = gdn.make_inputs_mxfp8(mx["q"][0], mx["k"][0], mx["v"][0], mx["z"][0], mx["q"][1], mx["k"][1],
+                                 mx["v"][1], mx["z"][1], dev(d["a"]), dev(d["b"]), w["A_log"], w["dt_bias"],
+                                 w["conv_w"], w["norm_w"])
+    gdn.decode_step_mxfp8(dm, inp8, conv8, S8, out8)
+    convb, Sb = dev(d["conv_state"]).clone(), dev(d["state"]).clone()
+    outb = torch.empty_like(out8)
+    gdn.decode_step(dm, inputs(w, {n: dev(a) for n, a in acts_deq.items()}), convb, Sb, outb)
+    gdn.check_status()
+    assert torch.isfinite(out8.float()).all() and torch.isfinite(S8).all()
+    assert torch.equal(out8, outb) and torch.equal(S8, Sb) and torch.equal(conv8, convb)
