@@ -25,15 +25,17 @@ def inputs(w, acts, mask=None, cu=None, state_idx=None):
                            w["dt_bias"], w["conv_w"], w["norm_w"], mask=mask, cu_seqlens=cu, state_idx=state_idx)
 
 
-def dims(shape, B, T, n_slots):
-    return gdn.make_dims(B=B, T=T, nk=shape.nk, nv=shape.nv, dk=shape.dk, dv=shape.dv, n_slots=n_slots)
+def dims(shape, B, T, n_slots, **params):
+    """params: scale, l2_eps, rms_eps (the library's defaults when absent)."""
+    return gdn.make_dims(B=B, T=T, nk=shape.nk, nv=shape.nv, dk=shape.dk, dv=shape.dv, n_slots=n_slots, **params)
 
 
-def oracle_layer(oracle, shape, w, acts, conv_state, state, mask=None, checkpoints=False):
+def oracle_layer(oracle, shape, w, acts, conv_state, state, mask=None, checkpoints=False, **params):
+    """params: scale, l2_eps, rms_eps, passed to the oracle as given."""
     return oracle.layer(**{n: acts[n].cpu() for n in ACTS}, **{n: w[n].cpu() for n in WEIGHTS},
                         conv_state=conv_state.cpu(), state=state.cpu(),
                         mask=None if mask is None else mask.cpu(), nk=shape.nk, nv=shape.nv, dk=shape.dk,
-                        dv=shape.dv, checkpoints=checkpoints)
+                        dv=shape.dv, checkpoints=checkpoints, **params)
 
 
 def max_abs(gpu, ref):
