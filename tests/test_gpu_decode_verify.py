@@ -51,6 +51,22 @@ def test_decode_batch_qwen_layout(oracle_mod):
     assert torch.equal(conv.cpu().double(), torch.from_numpy(ref["conv_state"]))
 
 
+def test_decode_many_rows(oracle_mod):
+    """200 rows of the 16/32-head d=128 layer: 3200 (row, key head) units over
+    one CTA per SM, so each CTA streams ~42 heads through its three-stage copy
+    ring (many wraps of the ring's phases) and the last units are ragged."""
+    d = I.decode_batch(seed=31, B=200)
+    s = d["shape"]
+    w, acts = _wd(d), _acts(d)
+    conv, S = dev(d["conv_state"]).clone(), dev(d["state"]).clone()
+    out = _decode(s, w, acts, conv, S)
+    gdn.check_status()
+    ref = oracle_layer(oracle_mod, s, d, d, d["conv_state"], d["state"])
+    assert_out(out, ref["out"])
+    assert_state(S, ref["state"])
+    assert torch.equal(conv.cpu().double(), torch.from_numpy(ref["conv_state"]))
+
+
 @pytest.mark.parametrize("shape", [I.TINY, I.Shape(nk=4, nv=8, dk=64, dv=64), I.Shape(nk=2, nv=2, dk=128, dv=128),
                                    I.Shape(nk=1, nv=4, dk=128, dv=128)])
 def test_decode_head_sizes(oracle_mod, shape):

@@ -319,3 +319,52 @@ def test_chain_grid_boundary(oracle_mod, B):
     assert_out(out, ref["out"])
     assert_state(S, ref["state"])
     assert torch.equal(conv.cpu().double(), torch.from_numpy(ref["conv_state"]))
+
+
+@pytest.mark.parametrize("shape,packed", [(I.Shape(nk=2, nv=4, dk=128, dv=128), False),
+                                          (I.Shape(nk=2, nv=4, dk=128, dv=128), True), (I.TINY, False)])
+def test_state_pool_slots(oracle_mod, shape, packed):
+    """Rows continue from pool slots chosen by state_idx (3 rows over 7 slots,
+    out of order): every path reads and writes its row's slot -- the one-grid
+    tensor-core form (dense rows), the separate-kernel form (packed rows) and
+    the CUDA-core form (head size 32) -- and the 4 unused slots stay as they
+    were, bit for bit."""
+    B, n_slots = 3, 7
+    idx = torch.tensor([5, 0, 3], dtype=torch.int32)
+    g = torch.Generator().manual_seed(170)
+    pool = I.states(shape, n_slots, g)
+    d = I.decode_batch(seed=171, B=B, shape=shape)
+    w = _wd(d)
+    conv, S = dev(pool["conv_state"]).clone(), dev(pool["state"]).clone()
+    if packed:
+        real = [70, 16, 129]
+        cu = [0]
+        for n in real:
+            cu.append(cu[-1] + (n + 15) // 16 * 16)
+        acts = I.activations(shape, 1, cu[-1], g)
+        mask = torch.zeros((1, cu[-1]))
+        for r in range(B):
+            mask[0, cu[r]:cu[r] + real[r]] = 1.0
+        out = _prefill(shape, w, {n: dev(a) for n, a in acts.items()}, conv, S, mask=dev(mask),
+                       cu=torch.tensor(cu, dtype=torch.int32, device="cuda"), B=B, state_idx=dev(idx),
+                       n_slots=n_slots)
+    else:
+        T = 100
+        acts = I.activations(shape, B, T, g)
+        out = _prefill(shape, w, {n: dev(a) for n, a in acts.items()}, conv, S, state_idx=dev(idx), n_slots=n_slots)
+    gdn.check_status()
+    out_h, S_h, conv_h = out.cpu(), S.cpu(), conv.cpu()
+    for r in range(B):
+        sl = int(idx[r])
+        c0, s0 = pool["conv_state"][sl:sl + 1], pool["state"][sl:sl + 1]
+        if packed:
+            a, b_ = cu[r], cu[r + 1]
+            ref = oracle_layer(oracle_mod, shape, d, {n: acts[n][:, a:b_] for n in ACTS}, c0, s0, mask=mask[:, a:b_])
+            assert_out(out_h[:, a:a + real[r]], ref["out"][:, :real[r]], f"row {r}")
+        else:
+            ref = oracle_layer(oracle_mod, shape, d, {n: acts[n][r:r + 1] for n in ACTS}, c0, s0)
+            assert_out(out_h[r:r + 1], ref["out"], f"row {r}")
+        assert_state(S_h[sl], ref["state"][0], f"row {r} (slot {sl})")
+        assert torch.equal(conv_h[sl].double(), torch.from_numpy(ref["conv_state"][0])), f"row {r} conv tail"
+    for sl in sorted(set(range(n_slots)) - set(idx.tolist())):
+        assert torch.equal(S_h[sl], pool["state"][sl]) and torch.equal(conv_h[sl], pool["conv_state"][sl]), sl
