@@ -51,11 +51,13 @@ def test_decode_batch_qwen_layout(oracle_mod):
     assert torch.equal(conv.cpu().double(), torch.from_numpy(ref["conv_state"]))
 
 
-def test_decode_many_rows(oracle_mod):
-    """200 rows of the 16/32-head d=128 layer: 3200 (row, key head) units over
-    one CTA per SM, so each CTA streams ~42 heads through its three-stage copy
-    ring (many wraps of the ring's phases) and the last units are ragged."""
-    d = I.decode_batch(seed=31, B=200)
+@pytest.mark.parametrize("B", [1, 200])
+def test_decode_row_counts(oracle_mod, B):
+    """The 16/32-head d=128 layer with 1 row (16 units: most CTAs have none)
+    and with 200 rows (3200 (row, key head) units over one CTA per SM: each
+    CTA streams ~42 heads through its three-stage copy ring, many wraps of the
+    ring's phases, and the last units are ragged)."""
+    d = I.decode_batch(seed=31, B=B)
     s = d["shape"]
     w, acts = _wd(d), _acts(d)
     conv, S = dev(d["conv_state"]).clone(), dev(d["state"]).clone()
@@ -174,6 +176,35 @@ def test_verify_checkpoints_equal_decode_steps_bitwise(shape, T):
         assert torch.equal(S, ck_s[:, t]), f"state checkpoint {t} differs"
         assert torch.equal(conv, ck_c[:, t]), f"conv checkpoint {t} differs"
     gdn.check_status()
+
+
+def test_verify_rows_over_a_state_pool(oracle_mod):
+    """Verify rows read their states from pool slots through state_idx: rows 0
+    and 3 share slot 4, rows 1 and 2 read slots 0 and 6 (out of order, 7
+    slots). Outputs and every checkpoint against the oracle from each row's
+    slot; the pool is read only."""
+    shape, B, T, n_slots = I.Shape(nk=2, nv=4, dk=128, dv=128), 4, 6, 7
+    idx = torch.tensor([4, 0, 6, 4], dtype=torch.int32)
+    g = torch.Generator().manual_seed(180)
+    pool = I.states(shape, n_slots, g)
+    d = I.decode_batch(seed=181, B=B, shape=shape)
+    acts = I.activations(shape, B, T, g)
+    w = _wd(d)
+    conv, S = dev(pool["conv_state"]).clone(), dev(pool["state"]).clone()
+    out = torch.empty((B, T, shape.nv, shape.dv), dtype=torch.bfloat16, device="cuda")
+    ck_s = torch.empty((B, T, shape.nv, shape.dk, shape.dv), dtype=torch.float32, device="cuda")
+    ck_c = torch.empty((B, T, 3, shape.C), dtype=torch.bfloat16, device="cuda")
+    gdn.verify_with_checkpoints(dims(shape, B, T, n_slots), inputs(w, {n: dev(a) for n, a in acts.items()},
+                                                                   state_idx=dev(idx)), conv, S, out, ck_s, ck_c)
+    gdn.check_status()
+    il = idx.long()
+    ref = oracle_layer(oracle_mod, shape, d, acts, pool["conv_state"][il], pool["state"][il], checkpoints=True)
+    assert_out(out, ref["out"])
+    for r in range(B):
+        for t in range(T):
+            assert_state(ck_s[r, t], ref["ckpt_state"][r, t], f"ckpt[{r},{t}]")
+    assert torch.equal(ck_c.cpu().double(), torch.from_numpy(ref["ckpt_conv"]))
+    assert torch.equal(S.cpu(), pool["state"]) and torch.equal(conv.cpu(), pool["conv_state"])
 
 
 def test_verify_paths_and_commit(oracle_mod):
