@@ -202,8 +202,8 @@ def timed(world, steps, warmup, step_fn, start_fn=None, end_fn=None):
     """Run warmup steps, then `steps` timed steps bracketed by a barrier and a
     synchronize on both sides; returns ms per step, max over ranks. One event
     pair brackets the whole region: an event recorded between two launches
-    would stand between a kernel and its programmatic dependent and serialise
-    them, so no per-launch events are taken. A kernel's average launch duration
+    may stand between a kernel and its programmatic dependent, so no
+    per-launch events are taken. A kernel's average launch duration
     is measured as a region of that kernel alone, launched back to back.
 
     The device is kept busy by a bounded spin kernel (torch.cuda._sleep)
