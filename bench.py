@@ -368,9 +368,51 @@ def phase_decode(gdn, world, steps, warmup, peak_hbm, local=0, e2e=True):
             d2h_s.wait_stream(comp)
 
         ems = timed(world, steps, warmup, e2e_step, start_fn=e2e_start, end_fn=e2e_join)
-        res["e2e"] = {"value": B * world / (ems * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                      "d2h_bytes_per_step": d2h}
+        res["e2e_copy_engine"] = {"value": B * world / (ems * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                                  "d2h_bytes_per_step": d2h,
+                                  "how": "one cudaMemcpyAsync each way per step on two copy streams, events "
+                                         "ordering each buffer's reuse"}
+        res["e2e"] = dict(res["e2e_copy_engine"])
         del dev_in
+
+        # the same copies without a copy engine (the contract's e2e when the
+        # host buffers are device-mapped): right after step i's decode, one
+        # gdn_copy_overlapped call uploads step i+1's activations and reads back
+        # step i-1's output rows while step i runs, on the decode's own stream;
+        # host sets rotate over more than L2, so every step's bytes cross the
+        # link. The last step's rows come back after it, inside the region.
+        if _host_mapped(hbuf):
+            n_h = math.ceil(L2_BYTES / (h2d + d2h)) + 1
+            hs = []
+            for _ in range(n_h):
+                hb, hv = pack([src[n] for n in ACTS], "cpu")
+                for v, n in zip(hv, ACTS):
+                    v.copy_(src[n])
+                hs.append((hb, torch.empty(src["out"].shape, dtype=src["out"].dtype).pin_memory()))
+            staged = [pack([d[n] for n in ACTS], "cuda") for d in sets]
+            staged_inp = [_inp(gdn, d, acts=dict(zip(ACTS, views))) for d, (_, views) in zip(sets, staged)]
+            assert hs[0][0].numel() == h2d  # the packed activations have no padding between them
+            last = [0]
+
+            def st_step(i, _):
+                k = i % n_sets
+                d = sets[k]
+                gdn.decode_step(d["dims"], staged_inp[k], d["conv_state"], d["state"], d["out"])
+                gdn.copy_overlapped([(staged[(i + 1) % n_sets][0], hs[(i + 1) % n_h][0], h2d),
+                                     (hs[(i - 1) % n_h][1], sets[(i - 1) % n_sets]["out"], d2h)])
+                last[0] = i
+
+            def st_end():
+                hs[last[0] % n_h][1].copy_(sets[last[0] % n_sets]["out"], non_blocking=True)
+
+            gdn.copy_overlapped([(staged[0][0], hs[0][0], h2d)])  # step 0's activations, before the warm-up
+            sms = timed(world, steps, warmup, st_step, end_fn=st_end)
+            res["e2e"] = {"value": B * world / (sms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                          "d2h_bytes_per_step": d2h, "host_sets": n_h,
+                          "how": "per step one gdn_copy_overlapped kernel on the decode's stream: step i+1's "
+                                 "activations up and step i-1's output rows down from / to pinned host memory "
+                                 "while step i runs"}
+            del hs, staged, staged_inp
 
         # zero-copy through the same call: the activations and the output rows
         # stay in pinned host memory, which the kernel reads and writes across

@@ -21,7 +21,8 @@ STATUS = {0: "GDN_OK", 1: "GDN_ERR_ARG", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_MASK", 
 EXPORTS = ("gdn_decode_step", "gdn_verify_with_checkpoints", "gdn_prefill_chunked",
            "gdn_prefill_workspace_size", "gdn_state_copy", "gdn_check_status", "gdn_last_error",
            "gdn_prefill_chunked_static_scratch", "gdn_commit_accepted", "gdn_decode_step_mxfp8",
-           "gdn_prefill_chunked_ckpt", "gdn_in_proj", "gdn_out_proj")
+           "gdn_prefill_chunked_ckpt", "gdn_in_proj", "gdn_out_proj", "gdn_copy_overlapped")
+MAX_OVERLAPPED_COPIES = 8
 
 
 class GdnError(RuntimeError):
@@ -44,6 +45,10 @@ class Inputs(ctypes.Structure):
 class InputsMxfp8(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("q", "k", "v", "z", "q_scale", "k_scale", "v_scale", "z_scale", "a",
                                                "b", "A_log", "dt_bias", "conv_w", "norm_w", "mask", "state_idx")]
+
+
+class Copy(ctypes.Structure):
+    _fields_ = [("dst", ctypes.c_void_p), ("src", ctypes.c_void_p), ("bytes", ctypes.c_size_t)]
 
 
 _lib = None
@@ -74,11 +79,13 @@ def load_library(path: Path | str | None = None):
     lib.gdn_out_proj.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, P, P, P, P]
     lib.gdn_decode_step_mxfp8.argtypes = [DP, ctypes.POINTER(InputsMxfp8), P, P, P, P]
     lib.gdn_commit_accepted.argtypes = [DP, ctypes.c_int32, ctypes.c_int32, P, P, P, P, P, P, P, P]
+    lib.gdn_copy_overlapped.argtypes = [ctypes.POINTER(Copy), ctypes.c_int32, P]
     lib.gdn_check_status.argtypes = [P]
     lib.gdn_last_error.restype = ctypes.c_char_p
     for name in ("gdn_decode_step", "gdn_verify_with_checkpoints", "gdn_prefill_chunked", "gdn_state_copy",
                  "gdn_check_status", "gdn_prefill_chunked_static_scratch", "gdn_commit_accepted",
-                 "gdn_decode_step_mxfp8", "gdn_prefill_chunked_ckpt", "gdn_in_proj", "gdn_out_proj"):
+                 "gdn_decode_step_mxfp8", "gdn_prefill_chunked_ckpt", "gdn_in_proj", "gdn_out_proj",
+                 "gdn_copy_overlapped"):
         getattr(lib, name).restype = ctypes.c_int
     if path is None:
         _lib = lib
@@ -139,6 +146,16 @@ def make_inputs_mxfp8(q, k, v, z, q_scale, k_scale, v_scale, z_scale, a, b, A_lo
 def decode_step_mxfp8(dims: Dims, inputs: InputsMxfp8, conv_state, recurrent_state, out, stream=None):
     _check(load_library().gdn_decode_step_mxfp8(ctypes.byref(dims), ctypes.byref(inputs), _ptr(conv_state),
                                                 _ptr(recurrent_state), _ptr(out), _stream(stream)))
+
+
+def copy_overlapped(copies, stream=None):
+    """gdn_copy_overlapped: up to MAX_OVERLAPPED_COPIES copies given as
+    (dst, src, nbytes) -- tensors or raw addresses, device memory or pinned
+    host memory -- done by one kernel that runs alongside the kernel before it
+    on the stream and completes after it. The caller keeps the buffers alive
+    and untouched until the stream has passed the call."""
+    arr = (Copy * max(1, len(copies)))(*[Copy(_ptr(d), _ptr(s), int(n)) for d, s, n in copies])
+    _check(load_library().gdn_copy_overlapped(arr, len(copies), _stream(stream)))
 
 
 def decode_step(dims: Dims, inputs: Inputs, conv_state, recurrent_state, out, stream=None):

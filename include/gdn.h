@@ -336,6 +336,34 @@ gdn_status gdn_in_proj(const gdn_dims *dims, int32_t M, int32_t H, const void *h
  * Same GEMM and precision as gdn_in_proj. */
 gdn_status gdn_out_proj(int32_t M, int32_t H, int32_t V, const void *o, const void *w_out, void *y, void *stream);
 
+/* Staging copies that overlap the kernel before them on the stream.
+ * Up to GDN_MAX_OVERLAPPED_COPIES copies of `bytes` bytes from src to dst, done
+ * by one kernel launched with programmatic dependent launch: it starts while
+ * the kernel before it on `stream` is still running, copies, and completes only
+ * after that kernel has completed, so work queued after the call sees both the
+ * copies and everything before them. Built for a decode loop fed from host
+ * memory (as in a serving step): step i+1's activations go up and step i-1's
+ * output rows come down while step i's kernel runs, with no copy engine
+ * involved (ordering kernels against copy-engine work costs a decode step
+ * ~3 us; this keeps the steps back to back).
+ *   copies   array of n descriptors (n in [0, GDN_MAX_OVERLAPPED_COPIES]);
+ *            a copy of 0 bytes is skipped
+ *   dst, src device memory, or page-locked host memory mapped into the
+ *            device's address space at the same address (cudaHostAlloc /
+ *            cudaMallocHost under unified addressing); both and `bytes`
+ *            multiples of 16 bytes; ranges must not overlap
+ * The copies run concurrently with the kernel before the call: the caller
+ * guarantees that no work still running on the stream writes a source or
+ * reads or writes a destination. GDN_ERR_ARG for NULL or misaligned
+ * arguments, GDN_ERR_SHAPE for a bad count; nothing is launched then. */
+#define GDN_MAX_OVERLAPPED_COPIES 8
+typedef struct gdn_copy {
+  void *dst;
+  const void *src;
+  size_t bytes;
+} gdn_copy;
+gdn_status gdn_copy_overlapped(const gdn_copy *copies, int32_t n, void *stream);
+
 /* Synchronise `stream`, then return (and clear) a device-detected error
  * recorded on the current device since the last check (GDN_ERR_MASK,
  * GDN_ERR_INDEX, GDN_ERR_TIMEOUT; the lowest code wins when several were

@@ -208,6 +208,30 @@ def test_decode_mxfp8_validation(lib):
     assert f(ctypes.byref(_good_dims(B=0)), ctypes.byref(inp), P, P, P, None) == 0
 
 
+def test_copy_overlapped_validation(lib):
+    """Host checks run before anything touches CUDA: a bad count, a NULL list
+    or pointer, or an address or size off the 16-byte grid returns an error
+    and launches nothing; empty copies are a no-op."""
+    f = lib.gdn_copy_overlapped
+    C = gdn.Copy
+
+    def call(copies, n=None):
+        arr = (C * max(1, len(copies)))(*copies)
+        return gdn.STATUS[f(arr, len(copies) if n is None else n, None)]
+
+    good = C(1 << 20, 1 << 21, 4096)
+    assert call([good] * 9) == "GDN_ERR_SHAPE"
+    assert call([good], n=-1) == "GDN_ERR_SHAPE"
+    assert gdn.STATUS[f(None, 1, None)] == "GDN_ERR_ARG"
+    assert call([C(None, 1 << 21, 4096)]) == "GDN_ERR_ARG"
+    assert call([C(1 << 20, None, 4096)]) == "GDN_ERR_ARG"
+    assert call([C((1 << 20) + 8, 1 << 21, 4096)]) == "GDN_ERR_ARG"
+    assert call([C(1 << 20, (1 << 21) + 4, 4096)]) == "GDN_ERR_ARG"
+    assert call([C(1 << 20, 1 << 21, 4100)]) == "GDN_ERR_ARG"
+    assert call([]) == "GDN_OK"
+    assert call([C(None, None, 0), C(1 << 20, 1 << 21, 0)]) == "GDN_OK"
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError):
         gdn.load_library(tmp_path / "missing" / "libgdn.so")

@@ -358,3 +358,73 @@ def test_tiny_layer_prefill_decode_verify(oracle_mod):
     assert_out(out_v, r["out"])
     for t in range(8):
         assert_state(ck_s[0, t], r["ckpt_state"][0, t])
+
+
+def test_copy_overlapped_bytes():
+    """One gdn_copy_overlapped call with an upload from pinned host memory, a
+    read-back into it and a device-to-device copy, of ragged sizes: every
+    destination equals its source byte for byte, and the bytes around the
+    destinations are untouched."""
+    g = torch.Generator().manual_seed(190)
+    sizes = [16, 4112, 1581056]
+    srcs_h = [torch.randint(0, 256, (n,), dtype=torch.uint8, generator=g).pin_memory() for n in sizes]
+    if not all(_host_mapped(t) for t in srcs_h):
+        pytest.skip("pinned host memory is not mapped at its own address on this system")
+    dev_src = torch.randint(0, 256, (sizes[2],), dtype=torch.uint8, generator=g).cuda()
+    pad = 64
+    up = torch.full((sizes[2] + 2 * pad,), 7, dtype=torch.uint8, device="cuda")
+    down = torch.full((sizes[1] + 2 * pad,), 9, dtype=torch.uint8).pin_memory()
+    d2d = torch.full((sizes[2] + 2 * pad,), 5, dtype=torch.uint8, device="cuda")
+    gdn.copy_overlapped([(up[pad:].data_ptr(), srcs_h[2], sizes[2]),
+                         (down[pad:].data_ptr(), dev_src[:sizes[1]], sizes[1]),
+                         (d2d[pad:].data_ptr(), dev_src, sizes[2]),
+                         (up.data_ptr(), srcs_h[0], 0)])
+    torch.cuda.synchronize()
+    gdn.check_status()
+    assert torch.equal(up[pad:pad + sizes[2]].cpu(), srcs_h[2])
+    assert torch.equal(down[pad:pad + sizes[1]], dev_src[:sizes[1]].cpu())
+    assert torch.equal(d2d[pad:pad + sizes[2]], dev_src)
+    assert (up[:pad] == 7).all() and (up[pad + sizes[2]:] == 7).all()
+    assert (down[:pad] == 9).all() and (down[pad + sizes[1]:] == 9).all()
+    assert (d2d[:pad] == 5).all() and (d2d[pad + sizes[2]:] == 5).all()
+
+
+def test_decode_loop_staged_through_overlapped_copies():
+    """A 6-step decode loop fed from pinned host memory, one state carried
+    from step to step: step i+1's activations go up and step i-1's output rows
+    come down in one gdn_copy_overlapped call queued right after step i (two
+    device input sets, two device output sets). Every step's rows on the host
+    and the final state and conv tail equal 6 plain steps on device inputs,
+    bit for bit."""
+    shape, B, K = I.Shape(nk=2, nv=4, dk=128, dv=128), 8, 6
+    d = I.decode_batch(seed=191, B=B, shape=shape)
+    w = _wd(d)
+    steps = [I.activations(shape, B, 1, torch.Generator().manual_seed(192 + i)) for i in range(K)]
+    host_in = [{n: s[n].contiguous().pin_memory() for n in ACTS} for s in steps]
+    host_out = [torch.zeros((B, 1, shape.nv, shape.dv), dtype=torch.bfloat16).pin_memory() for _ in range(K)]
+    if not all(_host_mapped(t) for h in host_in for t in h.values()):
+        pytest.skip("pinned host memory is not mapped at its own address on this system")
+    dev_in = [{n: torch.empty_like(steps[0][n], device="cuda") for n in ACTS} for _ in range(2)]
+    dev_out = [torch.empty((B, 1, shape.nv, shape.dv), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    dm = dims(shape, B, 1, B)
+    conv, S = dev(d["conv_state"]).clone(), dev(d["state"]).clone()
+
+    def up(i):
+        return [(dev_in[i % 2][n], host_in[i][n], host_in[i][n].numel() * host_in[i][n].element_size())
+                for n in ACTS]
+
+    def down(i):
+        return [(host_out[i], dev_out[i % 2], host_out[i].numel() * 2)]
+
+    gdn.copy_overlapped(up(0))
+    for i in range(K):
+        gdn.decode_step(dm, inputs(w, dev_in[i % 2]), conv, S, dev_out[i % 2])
+        gdn.copy_overlapped((up(i + 1) if i + 1 < K else []) + (down(i - 1) if i >= 1 else []))
+    host_out[K - 1].copy_(dev_out[(K - 1) % 2])  # the last step's rows, once the stream has passed it
+    torch.cuda.synchronize()
+    gdn.check_status()
+    conv_r, S_r = dev(d["conv_state"]).clone(), dev(d["state"]).clone()
+    for i in range(K):
+        out_r = _decode(shape, w, {n: dev(steps[i][n]) for n in ACTS}, conv_r, S_r)
+        assert torch.equal(host_out[i], out_r.cpu()), f"step {i}"
+    assert torch.equal(S, S_r) and torch.equal(conv, conv_r)
